@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark of the SplitZip BF16 codec on GB300.
+
+One step = the whole hot path once over the KV-cache-shaped workload
+(64 layers x {K,V} x 8 KV heads x 2048 tokens x 128 head dim = 268,435,456
+BF16 values, chunk 1024): calibrate the Top-16 codebook on a 1 Mi-value
+sample, encode the tensor, decode the stream. ``value`` is raw BF16 bytes per
+second through that step; encode-only and decode-only rates, the compression
+ratio and the roofline of the dominant kernel are reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the plain CPU oracle (the only other
+implementation of this codec) on the host cores over a bounded slice of the
+same workload. Under torchrun (N > 1) every rank runs an independent replica
+on its own GPU (weak scaling, no collective on the data path); rank 0 prints
+one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "encode/decode GB/s (raw BF16 bytes) @256M elems; ratio; % of HBM peak"
+WORKLOAD = "kv_cache [64,2,8,2048,128] bf16 = 268,435,456 values, chunk 1024, calibration sample 1 Mi values"
+CHUNK = 1024
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------- distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return ws, rank
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(v: float, device=None) -> float:
+    """Largest value of v over all ranks (v itself on a single process)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(v)
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampler for the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"samples": 0, "note": "nvidia-smi unavailable"}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:9]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i + 1].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        j = json.load(open(path))
+        return float(j["hbm_gbs"]), "of measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "of fallback"
+
+
+def profile_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    src = {"encode": "encode.cu", "decode": "decode.cu"}[kernel]
+    path = os.path.join(ROOT, "profiles", f"{kernel}_kv_cache.md")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(os.path.join(ROOT, "lossless_bf16_exponent_gb300", "csrc", src), "rb")
+                             .read()).hexdigest()[:16]
+        m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+        m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9]+)", text)
+        if m_sha and m_b and m_sha.group(1) == sha:
+            return int(m_b.group(1))
+    except OSError:
+        pass
+    return None
+
+
+def cpu_cores_used() -> int:
+    return 1  # the oracle is single-threaded C
+
+
+# ------------------------------------------------------------ our (GPU) arm
+
+def run_ours(args):
+    import torch
+
+    import lossless_bf16_exponent_gb300 as uz
+    import lossless_bf16_exponent_gb300.workloads as W
+    from lossless_bf16_exponent_gb300 import build as B
+
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist("nccl")
+    if rank == 0 and B.stale():
+        B.build()
+    barrier()
+    uz.load()
+
+    x, sample = W.workload(2, device=dev)
+    n = x.numel()
+    raw = 2 * n
+    cb = uz.new_codebook(dev)
+    out = torch.empty(uz.max_compressed_size(n, CHUNK), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(uz.workspace_bytes(n, CHUNK), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        uz.calibrate(sample, codebook=cb)
+        if ev: ev[1].record(stream)
+        uz.encode(x, cb, CHUNK, out=out, workspace=wsb, sync=False)
+        if ev: ev[2].record(stream)
+        uz.decode(out, n, out=y)
+        if ev: ev[3].record(stream)
+
+    # correctness first (bit-exact round trip), then warm-up
+    step()
+    info = uz.stream_info(out)
+    assert info["status"] == 0, info
+    assert torch.equal(y.view(torch.int16), x.view(torch.int16)), "round trip is not bit-exact"
+    nbytes, m = int(info["total_bytes"]), int(info["escapes"])
+    for _ in range(args.warmup):
+        step()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if rank == 0 else {}
+    elapsed_ms = t0.elapsed_time(t1)
+    cal_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    enc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    max_ms = max_over_ranks(elapsed_ms, dev)
+    total_raw = sum_over_ranks(raw * args.steps, dev)
+
+    # end to end through the public API with host buffers
+    xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    xh.copy_(x)
+    sh = torch.empty(sample.shape, dtype=sample.dtype, pin_memory=True)
+    sh.copy_(sample)
+    yh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    xd, sd = torch.empty_like(x), torch.empty_like(sample)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        sd.copy_(sh, non_blocking=True)
+        uz.calibrate(sd, codebook=cb)
+        uz.encode(xd, cb, CHUNK, out=out, workspace=wsb, sync=False)
+        uz.decode(out, n, out=y)
+        yh.copy_(y, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(max(3, args.warmup)):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), dev)
+    assert torch.equal(yh.view(torch.int16), xh.view(torch.int16)), "e2e round trip is not bit-exact"
+    e2e_raw = sum_over_ranks(raw * e2e_steps, dev)
+
+    cpu = cpu_baseline(x, sample) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+
+    if rank != 0:
+        return None
+    peak, peak_src = measured_peak()
+    enc_bytes = raw + nbytes  # read the BF16 tensor, write the stream
+    dec_bytes = nbytes + raw  # read the stream, write the BF16 tensor
+    enc_gbs = enc_bytes / (enc_ms * 1e-3) / 1e9
+    dec_gbs = dec_bytes / (dec_ms * 1e-3) / 1e9
+    dominant = "encode" if enc_ms >= dec_ms else "decode"
+    dom_gbs = enc_gbs if dominant == "encode" else dec_gbs
+    line = {
+        "metric": METRIC,
+        "value": round(total_raw / (max_ms * 1e-3) / 1e9, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "u16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "step": "calibrate + encode + decode",
+                   "l2": "inputs larger than L2 (512 MiB BF16 tensor, 403 MB stream)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "encode_gbs_raw": round(raw / (enc_ms * 1e-3) / 1e9, 1),
+        "decode_gbs_raw": round(raw / (dec_ms * 1e-3) / 1e9, 1),
+        "calibrate_us": round(cal_ms * 1e3, 2),
+        "encode_us": round(enc_ms * 1e3, 2),
+        "decode_us": round(dec_ms * 1e3, 2),
+        "ratio": round(raw / nbytes, 5),
+        "ratio_payload": round(raw / (n + (n + 1) // 2 + 3 * m), 5),
+        "escape_rate": m / n,
+        "hbm": {"encode": {"gbs": round(enc_gbs, 1), "frac": round(enc_gbs / peak, 4)},
+                "decode": {"gbs": round(dec_gbs, 1), "frac": round(dec_gbs / peak, 4)},
+                "peak_gbs": peak, "peak_source": peak_src, "vs_8tbs": {
+                    "encode": round(enc_gbs / 8000, 4), "decode": round(dec_gbs / 8000, 4)}},
+        "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(dom_gbs / peak, 4), "peak_source": peak_src,
+                     "traffic": profile_traffic(dominant),
+                     "algorithmic_bytes": enc_bytes if dominant == "encode" else dec_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(e2e_raw / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": raw + 2 * sample.numel(), "d2h_bytes_per_step": raw,
+                "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+def cpu_baseline(x, sample, budget_s: float = 12.0):
+    """The oracle, as it stands, on the host: calibrate on the sample, encode
+    and decode the whole workload, repeated while the budget lasts."""
+    import numpy as np
+
+    import lossless_bf16_exponent_gb300.workloads as W
+    import oracle
+
+    o = oracle.Oracle()
+    xh, sh = W.as_u16(x), W.as_u16(sample)
+    t_total, raw_total, reps = 0.0, 0, 0
+    while reps < 1 or (t_total < budget_s and reps < 5):
+        t = time.perf_counter()
+        exps = o.calibrate(sh)
+        rc, s = o.encode(xh, exps, CHUNK)
+        rc2, y = o.decode(s, xh.size)
+        t_total += time.perf_counter() - t
+        assert rc == 0 and rc2 == 0 and np.array_equal(y, xh)
+        raw_total += 2 * xh.size
+        reps += 1
+    return {"value": round(raw_total / t_total / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
+            "kind": "oracle",
+            "sample": f"whole workload ({xh.size} values) x{reps}: calibrate 1 Mi sample + encode + decode, "
+                      f"{t_total:.1f} s"}
+
+
+# ------------------------------------------------------ reference (oracle) arm
+
+def run_reference(args):
+    import numpy as np
+    import torch
+
+    import lossless_bf16_exponent_gb300.workloads as W
+    import oracle
+
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return None  # rank 0 alone runs the CPU reference
+    o = oracle.Oracle()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x, sample = W.workload(2, device=dev)
+    xh, sh = W.as_u16(x), W.as_u16(sample)
+    del x
+    # Size each step's slice so the whole run stays within about two minutes.
+    probe = xh[: 1 << 22]
+    t = time.perf_counter()
+    rc, s = o.encode(probe, o.calibrate(sh), CHUNK)
+    o.decode(s, probe.size)
+    per_val = (time.perf_counter() - t) / probe.size
+    steps_total = args.steps + args.warmup
+    n_slice = int(min(xh.size, max(1 << 20, 110.0 / max(steps_total, 1) / per_val)))
+    n_slice -= n_slice % 8192
+    n_slice = max(n_slice, 8192)
+    times = []
+    for k in range(steps_total):
+        off = (k * n_slice) % (xh.size - n_slice + 1)
+        sl = xh[off:off + n_slice]
+        t = time.perf_counter()
+        exps = o.calibrate(sh)
+        rc, s = o.encode(sl, exps, CHUNK)
+        rc2, y = o.decode(s, sl.size)
+        dt = time.perf_counter() - t
+        assert rc == 0 and rc2 == 0 and np.array_equal(y, sl)
+        if k >= args.warmup:
+            times.append(dt)
+    elapsed = sum(times)
+    value = 2 * n_slice * len(times) / elapsed / 1e9
+    sample_txt = (f"slice of {n_slice} values of the workload per step (calibrate 1 Mi sample + encode + "
+                  f"decode), single thread")
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed / len(times) * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "step": "calibrate + encode + decode (CPU oracle, bounded slice)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores_used(), "kind": "oracle",
+                         "sample": sample_txt},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,225 @@
+/*
+ * uzip.h -- C ABI of libuzip, a fixed-length lossless BF16 exponent codec for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method is SplitZip's, as the review page "SplitZip: Ultra Fast Lossless
+ * KV Compression for Disaggregated LLM Serving" states it:
+ *   §3.2  each BF16 bit pattern x is split into an 8-bit exponent
+ *         e = (x >> 7) & 0xff and an exact sign-mantissa byte
+ *         a = ((x >> 8) & 0x80) | (x & 0x7f); e is mapped through a Top-16
+ *         codebook to a 4-bit code (two codes per byte); exponents outside the
+ *         Top-16 are escapes, stored as a 16-bit position inside their chunk plus
+ *         the raw 8-bit exponent; size N + N/2 + 3M bytes for M escapes.
+ *         Decoding unpacks the codes, looks them up in a 16-entry table,
+ *         rebuilds x = ((a & 0x80) << 8) | (e << 7) | (a & 0x7f), then overwrites
+ *         each escape with its exact exponent.
+ *   §3.3  the Top-16 codebook is calibrated once, offline, from the exponent
+ *         histogram of a representative sample, giving three lookup tables.
+ *   §3.4  all 16 codes are real exponents; an escape carries a dummy code.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named d_* are device memory owned by the caller; h_* are host
+ *     memory owned by the caller. The library allocates nothing, keeps no
+ *     global state between calls and is safe to call from several host threads
+ *     on different streams with different buffers.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and is asynchronous unless an entry point says it synchronises.
+ *   - BF16 data are raw 16-bit patterns (any value, including NaN, Inf,
+ *     subnormals and -0, round-trips bit-exactly).
+ *   - Device pointers must be 16-byte aligned (UZIP_ERR_ALIGN otherwise).
+ *   - Errors found on the host return at once and enqueue nothing. Errors found
+ *     on the device are reported through a status word (see each call); no
+ *     kernel traps, and every device-side wait is bounded in time.
+ *
+ * Compressed stream format, version 1 (all integers little endian; every part
+ * before the escape section starts on a 16-byte boundary and is padded with
+ * zero bytes to one):
+ *   header  64 B   [0,4) "UZP1" | [4,6) u16 version = 1 | [6,8) u16 status
+ *                  flags (0 = valid) | [8,16) u64 n | [16,20) u32 chunk |
+ *                  [20,24) u32 nc = ceil(n / chunk) | [24,32) u64 M escapes |
+ *                  [32,48) u8 exps[16] (code k <-> exponent exps[k]) |
+ *                  [48,56) u64 total stream bytes | [56,64) zero
+ *   A       n B    sign-mantissa bytes a_i
+ *   B  ceil(n/2) B 4-bit codes, element 2j in the low nibble of byte j; an
+ *                  escape carries the dummy code 0; a missing last high
+ *                  nibble is 0
+ *   C  4(nc+1) B   u32 offsets[c] = number of escapes in chunks < c
+ *                  (offsets[nc] = M)
+ *   D  3M B        chunk c's escape block starts at byte 3 * offsets[c]: its
+ *                  k = offsets[c+1] - offsets[c] positions (u16, element index
+ *                  minus c * chunk, ascending), then its k raw exponents
+ *   total = 64 + pad16(n) + pad16(ceil(n/2)) + pad16(4(nc+1)) + 3M.
+ * The page's size N + N/2 + 3M is the A + B + D payload; header, offsets and
+ * padding are the metadata.
+ */
+#ifndef UZIP_H
+#define UZIP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define UZIP_API __attribute__((visibility("default")))
+#else
+#define UZIP_API
+#endif
+
+/* Same type as cudaStream_t, so no CUDA header is needed to use this one. */
+typedef struct CUstream_st *uzip_stream_t;
+
+enum uzip_status {
+    UZIP_OK = 0,
+    UZIP_ERR_ARG = 1,       /* null pointer, size out of range, bad codebook  */
+    UZIP_ERR_ALIGN = 2,     /* a device pointer is not 16-byte aligned         */
+    UZIP_ERR_CHUNK = 3,     /* chunk not a multiple of 8 in [8, 65536]         */
+    UZIP_ERR_CAPACITY = 4,  /* output or workspace buffer too small            */
+    UZIP_ERR_CORRUPT = 5,   /* stream header or escape data inconsistent       */
+    UZIP_ERR_TIMEOUT = 6,   /* a bounded device-side wait ran out              */
+    UZIP_ERR_CUDA = 7       /* a CUDA runtime call failed                      */
+};
+
+#define UZIP_VERSION 1
+#define UZIP_HEADER_BYTES 64
+#define UZIP_CODEBOOK_BYTES 4096
+#define UZIP_MIN_CHUNK 8
+#define UZIP_MAX_CHUNK 65536
+#define UZIP_MAX_N 0xFFFFFFFFull /* offsets and M are stored in 32 bits */
+
+/* Header status flags, set by the encoder's kernel. */
+#define UZIP_FLAG_CAPACITY 0x1u /* the escapes did not fit in out_capacity   */
+#define UZIP_FLAG_TIMEOUT 0x2u  /* the chunk-offset look-back wait ran out   */
+
+/* Codebook blob (UZIP_CODEBOOK_BYTES of device memory, written by
+ * uzip_calibrate or uzip_codebook_from_exps):
+ *   [0,4) "UZCB" | [4,8) u32 version 1 | [8,16) u64 calibration sample size |
+ *   [16,32) u8 exps[16], most frequent first | [32,48) u8 decode table
+ *   (code -> exponent, equal to exps) | [48,304) u8 encode table
+ *   (exponent -> code, 0 for an escape) | [304,560) u8 escape table
+ *   (exponent -> 1 if not in the Top-16) | [1024,3072) u64 histogram[256] of
+ *   the calibration sample (zero for uzip_codebook_from_exps). */
+#define UZIP_CB_EXPS 16
+#define UZIP_CB_DEC 32
+#define UZIP_CB_ENC 48
+#define UZIP_CB_ESC 304
+#define UZIP_CB_HIST 1024
+
+/* Offline calibration (§3.3): histogram of all exponents of the sample, the 16
+ * most frequent exponents (code k = k-th most frequent; equal counts -> the
+ * smaller exponent first; exponents the sample lacks fill the remaining codes
+ * in ascending order), then the three lookup tables.
+ *   d_sample_bf16  n_sample BF16 values (n_sample may be 0: codes 0..15 map to
+ *                  exponents 0..15).
+ *   d_codebook     UZIP_CODEBOOK_BYTES, overwritten.
+ * Returns UZIP_ERR_ARG / UZIP_ERR_ALIGN / UZIP_ERR_CUDA, else UZIP_OK. Async. */
+UZIP_API int uzip_calibrate(const void *d_sample_bf16, size_t n_sample, void *d_codebook,
+                            uzip_stream_t stream);
+
+/* Codebook from 16 given exponents (host array, code k -> h_exps16[k]); the
+ * values must be distinct (UZIP_ERR_ARG otherwise). Builds the same three
+ * tables as uzip_calibrate, histogram zero. Async; h_exps16 may be reused as
+ * soon as the call returns. */
+UZIP_API int uzip_codebook_from_exps(const uint8_t *h_exps16, void *d_codebook,
+                                     uzip_stream_t stream);
+
+/* Exact stream bytes for n values of which n_escapes are escapes (see the
+ * format above); n_escapes = n gives the worst case. Returns 0 for an invalid
+ * chunk, n > UZIP_MAX_N or n_escapes > n. Host only. */
+UZIP_API size_t uzip_compressed_size(size_t n, size_t n_escapes, uint32_t chunk);
+
+/* Device workspace bytes uzip_encode needs for (n, chunk); 0 for an invalid
+ * chunk or n. Host only. */
+UZIP_API size_t uzip_encode_workspace_bytes(size_t n, uint32_t chunk);
+
+/* Encode n BF16 values (§3.2) in one fused pass: the dense stage (sign-mantissa
+ * bytes and packed codes) and the escape stage (per-chunk counts, an exclusive
+ * scan over the chunks by decoupled look-back, escape blocks in ascending
+ * element order).
+ *   d_in_bf16      n BF16 values (may be NULL when n == 0).
+ *   chunk          escape-position chunk, a multiple of 8 in [8, 65536].
+ *   d_codebook     from uzip_calibrate / uzip_codebook_from_exps.
+ *   d_out          stream buffer of out_capacity bytes. out_capacity must hold
+ *                  at least uzip_compressed_size(n, 0, chunk) (UZIP_ERR_CAPACITY
+ *                  at once otherwise); uzip_compressed_size(n, n, chunk) can
+ *                  never overflow. If the escapes do not fit, the kernel writes
+ *                  none past out_capacity and sets UZIP_FLAG_CAPACITY in the
+ *                  header.
+ *   d_workspace    at least uzip_encode_workspace_bytes(n, chunk) bytes; cleared
+ *                  by the call; must not be shared with a concurrent call.
+ *   h_out_bytes    NULL: fully asynchronous; read the total from the header.
+ *                  Non-NULL: the call synchronises `stream`, stores the exact
+ *                  stream size and returns UZIP_ERR_CAPACITY / UZIP_ERR_TIMEOUT
+ *                  if the kernel set the matching header flag.
+ * Bytes of d_out past the stream's total are not written. */
+UZIP_API int uzip_encode(const void *d_in_bf16, size_t n, uint32_t chunk, const void *d_codebook,
+                         void *d_out, size_t out_capacity, void *d_workspace,
+                         size_t workspace_bytes, size_t *h_out_bytes, uzip_stream_t stream);
+
+/* Decode a stream produced by uzip_encode (§3.2): dense unpack and lookup,
+ * then the escape fix-up, fused per tile so each output byte is written once.
+ *   d_stream       stream_bytes bytes (at least the header's total).
+ *   d_out_bf16     n BF16 values; n must equal the header's n.
+ *   d_status       NULL or one device uint32_t that receives UZIP_OK or the
+ *                  error code. The kernel checks the header (magic, version,
+ *                  status flags, n, chunk, nc, M, total <= stream_bytes) before
+ *                  it writes any output; with a bad header it writes no output
+ *                  and stores UZIP_ERR_CORRUPT. Escape entries that point
+ *                  outside their chunk or offsets that do not rise are skipped
+ *                  and also give UZIP_ERR_CORRUPT (the output is then not
+ *                  trustworthy). No read or write leaves the buffers.
+ * Returns host-detected errors only (UZIP_ERR_ARG, UZIP_ERR_ALIGN,
+ * UZIP_ERR_CAPACITY if stream_bytes < 64, UZIP_ERR_CUDA). Async. */
+UZIP_API int uzip_decode(const void *d_stream, size_t stream_bytes, void *d_out_bf16, size_t n,
+                         uint32_t *d_status, uzip_stream_t stream);
+
+/* Host view of a stream header. */
+typedef struct {
+    uint64_t n;
+    uint64_t escapes;     /* M */
+    uint64_t total_bytes; /* whole stream */
+    uint64_t payload_bytes; /* n + ceil(n/2) + 3M: the page's size */
+    uint32_t chunk;
+    uint32_t nc;
+    uint32_t version;
+    uint32_t flags;       /* UZIP_FLAG_* */
+    uint8_t exps[16];
+} uzip_info_t;
+
+/* Copy the header to the host (synchronises `stream`) and check it. Returns
+ * UZIP_ERR_CORRUPT for a bad magic, version or inconsistent sizes, else
+ * UZIP_OK (h_info is filled in both cases when the header was readable). */
+UZIP_API int uzip_stream_info(const void *d_stream, size_t stream_bytes, uzip_info_t *h_info,
+                              uzip_stream_t stream);
+
+/* Options of uzip_encode_ex. Zero-initialise and set what you need. */
+typedef struct {
+    uint64_t lookback_timeout_ns; /* limit of each look-back wait; 0 = 1 s     */
+    uint32_t withhold_first_unit; /* failure injection for tests: the first
+                                     unit never publishes its escape count, so
+                                     every look-back that reaches it waits the
+                                     full limit and the stream is flagged
+                                     UZIP_FLAG_TIMEOUT (the kernel still ends) */
+    uint32_t reserved;
+} uzip_encode_opts_t;
+
+/* uzip_encode with options (opts may be NULL: same as uzip_encode). Same
+ * arguments, errors and asynchrony as uzip_encode. */
+UZIP_API int uzip_encode_ex(const void *d_in_bf16, size_t n, uint32_t chunk, const void *d_codebook,
+                            void *d_out, size_t out_capacity, void *d_workspace,
+                            size_t workspace_bytes, size_t *h_out_bytes,
+                            const uzip_encode_opts_t *opts, uzip_stream_t stream);
+
+/* Static text for a status code. */
+UZIP_API const char *uzip_status_string(int status);
+
+/* UZIP_VERSION of the loaded library. */
+UZIP_API int uzip_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UZIP_H */

@@ -1,0 +1,146 @@
+"""PyTorch front end of libuzip: device buffers and the current CUDA stream
+go in, the C ABI does all the work. Tensors must be contiguous CUDA tensors
+with 16-byte aligned storage; BF16 data may be any 2-byte dtype (the codec
+works on bit patterns)."""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import CODEBOOK_BYTES, HEADER_BYTES, UzipError, check
+
+
+def _sp(device=None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _p(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+
+
+def _flat16(x: torch.Tensor) -> torch.Tensor:
+    if not x.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if x.element_size() != 2:
+        raise ValueError(f"expected 16-bit values, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.reshape(-1)
+
+
+def load():
+    return _lib.load()
+
+
+# ---------------------------------------------------------------- codebook
+
+def new_codebook(device="cuda") -> torch.Tensor:
+    return torch.empty(CODEBOOK_BYTES, dtype=torch.uint8, device=device)
+
+
+def calibrate(sample: torch.Tensor, codebook: torch.Tensor | None = None) -> torch.Tensor:
+    """Top-16 codebook from the exponent histogram of ``sample`` (offline
+    calibration, SplitZip §3.3). Returns the 4096-byte device codebook."""
+    s = _flat16(sample)
+    cb = new_codebook(s.device) if codebook is None else codebook
+    check(load().uzip_calibrate(_p(s), s.numel(), _p(cb), _sp(s.device)), "uzip_calibrate")
+    return cb
+
+
+def codebook_from_exps(exps, device="cuda", codebook: torch.Tensor | None = None) -> torch.Tensor:
+    vals = [int(v) for v in exps]
+    if len(vals) != 16:
+        raise ValueError("need 16 exponents")
+    arr = (ctypes.c_uint8 * 16)(*vals)
+    cb = new_codebook(device) if codebook is None else codebook
+    check(load().uzip_codebook_from_exps(arr, _p(cb), _sp(cb.device)), "uzip_codebook_from_exps")
+    return cb
+
+
+def codebook_exps(codebook: torch.Tensor) -> list[int]:
+    """The 16 exponents of a codebook (copies to the host)."""
+    return codebook[_lib.CB_EXPS:_lib.CB_EXPS + 16].cpu().tolist()
+
+
+def codebook_histogram(codebook: torch.Tensor) -> list[int]:
+    h = codebook[_lib.CB_HIST:_lib.CB_HIST + 2048].cpu().view(torch.int64)
+    return [int(v) for v in h.tolist()]
+
+
+# ------------------------------------------------------------------- sizes
+
+def compressed_size(n: int, n_escapes: int, chunk: int = 1024) -> int:
+    return int(load().uzip_compressed_size(n, n_escapes, chunk))
+
+
+def max_compressed_size(n: int, chunk: int = 1024) -> int:
+    return compressed_size(n, n, chunk)
+
+
+def workspace_bytes(n: int, chunk: int = 1024) -> int:
+    return int(load().uzip_encode_workspace_bytes(n, chunk))
+
+
+# ------------------------------------------------------------------ codec
+
+def encode(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, out: torch.Tensor | None = None,
+           workspace: torch.Tensor | None = None, sync: bool = True, timeout_ns: int = 0,
+           withhold_first_unit: bool = False):
+    """Encode ``x`` (SplitZip §3.2). Returns ``(stream, nbytes)``; ``stream``
+    is the whole output buffer, ``nbytes`` the exact stream size (None when
+    ``sync=False``: read it later with :func:`stream_info`)."""
+    v = _flat16(x)
+    n = v.numel()
+    if out is None:
+        out = torch.empty(max_compressed_size(n, chunk), dtype=torch.uint8, device=v.device)
+    if workspace is None:
+        workspace = torch.empty(max(16, workspace_bytes(n, chunk)), dtype=torch.uint8, device=v.device)
+    nbytes = ctypes.c_size_t(0)
+    L = load()
+    args = (_p(v), n, chunk, _p(codebook), _p(out), out.numel(), _p(workspace), workspace.numel(),
+            ctypes.byref(nbytes) if sync else None)
+    if timeout_ns or withhold_first_unit:
+        opts = _lib.EncodeOpts(timeout_ns, 1 if withhold_first_unit else 0, 0)
+        rc = L.uzip_encode_ex(*args, ctypes.byref(opts), _sp(v.device))
+    else:
+        rc = L.uzip_encode(*args, _sp(v.device))
+    check(rc, "uzip_encode")
+    return out, (nbytes.value if sync else None)
+
+
+def decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = None, status: torch.Tensor | None = None,
+           stream_bytes: int | None = None, dtype=torch.bfloat16) -> torch.Tensor:
+    """Decode ``n`` values from a stream (SplitZip §3.2). Device-side errors
+    land in ``status`` (a 1-element int32 CUDA tensor) when given."""
+    if out is None:
+        out = torch.empty(n, dtype=dtype, device=stream.device)
+    o = _flat16(out) if n else out
+    nb = stream.numel() if stream_bytes is None else stream_bytes
+    check(load().uzip_decode(_p(stream), nb, _p(o) if n else None, n, _p(status), _sp(stream.device)),
+          "uzip_decode")
+    return out
+
+
+def stream_info(stream: torch.Tensor, stream_bytes: int | None = None) -> dict:
+    info = _lib.Info()
+    nb = stream.numel() if stream_bytes is None else stream_bytes
+    rc = load().uzip_stream_info(_p(stream), nb, ctypes.byref(info), _sp(stream.device))
+    d = {f: getattr(info, f) for f, _ in _lib.Info._fields_ if f != "exps"}
+    d["exps"] = list(info.exps)
+    d["status"] = rc
+    return d
+
+
+def roundtrip_ok(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024) -> bool:
+    s, nb = encode(x, codebook, chunk)
+    y = decode(s, x.numel(), stream_bytes=nb, dtype=x.dtype)
+    return bool(torch.equal(y.view(torch.int16), _flat16(x).view(torch.int16)))
+
+
+__all__ = [
+    "HEADER_BYTES", "CODEBOOK_BYTES", "UzipError", "load", "new_codebook", "calibrate", "codebook_from_exps",
+    "codebook_exps", "codebook_histogram", "compressed_size", "max_compressed_size", "workspace_bytes",
+    "encode", "decode", "stream_info", "roundtrip_ok",
+]

@@ -1,0 +1,170 @@
+// calibrate.cu -- offline codebook calibration of the SplitZip codec.
+//
+// SplitZip review page, §3.3: extract every exponent of a representative
+// sample, count them, keep the 16 most frequent and build three lookup tables
+// (exponent -> 4-bit code, code -> exponent, exponent -> escape membership).
+// §3.4: all 16 codes are real exponents; an escape gets a dummy code (0 here).
+//
+// Kernels:
+//   hist256_kernel  grid-stride over the sample with 16-byte loads; one
+//                   256-bin shared-memory histogram per warp; equal exponents
+//                   inside a warp are merged with __match_any_sync so a
+//                   concentrated distribution does not serialise on one bin;
+//                   per-block totals go to the blob's u64 histogram.
+//   top16_kernel    one CTA: thread j ranks bin j against all 256 counts
+//                   (count descending, exponent ascending) and the 16 lowest
+//                   ranks become the codebook; then the three tables.
+//   luts_kernel     same tables from 16 caller-given exponents.
+#include "uzip_internal.cuh"
+
+namespace uzip {
+namespace {
+
+constexpr int kHistThreads = 256;
+constexpr int kHistWarps = kHistThreads / 32;
+
+__device__ __forceinline__ void warp_hist_add(uint32_t* h, uint32_t e, bool valid) {
+    // Lanes holding the same exponent add once, with their count.
+    const uint32_t key = valid ? e : (0x100u | (threadIdx.x & 31));
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    if (valid && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&h[e], __popc(peers));
+}
+
+__global__ void __launch_bounds__(kHistThreads) hist256_kernel(const uint16_t* __restrict__ x, uint64_t n,
+                                                               unsigned long long* __restrict__ hist) {
+    __shared__ uint32_t sh[kHistWarps][256];
+    for (int i = threadIdx.x; i < kHistWarps * 256; i += kHistThreads) (&sh[0][0])[i] = 0;
+    __syncthreads();
+    uint32_t* h = sh[threadIdx.x / 32];
+
+    const uint64_t groups = n / 8;
+    const uint64_t stride = (uint64_t)gridDim.x * kHistThreads;
+    // Warp-uniform trip count so __match_any_sync always sees the full warp.
+    const uint64_t warp_first = (uint64_t)blockIdx.x * kHistThreads + (threadIdx.x & ~31u);
+    for (uint64_t wg = warp_first; wg < groups; wg += stride) {
+        const uint64_t g = wg + (threadIdx.x & 31);
+        const bool valid = g < groups;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (valid) v = ld_stream_v4(x + 8 * g);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            warp_hist_add(h, (w[q] >> 7) & 0xFF, valid);
+            warp_hist_add(h, (w[q] >> 23) & 0xFF, valid);
+        }
+    }
+    // Ragged tail (< 8 values): block 0's first warp.
+    if (blockIdx.x == 0 && threadIdx.x < 32) {
+        const uint64_t i = groups * 8 + threadIdx.x;
+        const bool valid = i < n && threadIdx.x < 8;
+        warp_hist_add(h, valid ? (uint32_t)(x[i] >> 7) & 0xFF : 0, valid);
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < 256; b += kHistThreads) {
+        uint32_t s = 0;
+#pragma unroll
+        for (int w = 0; w < kHistWarps; w++) s += sh[w][b];
+        if (s) atomicAdd(&hist[b], (unsigned long long)s);
+    }
+}
+
+// Tables from exps[16] (shared memory), written by a 256-thread CTA.
+__device__ void write_tables(const uint8_t* exps, uint8_t* cb, uint64_t n_sample) {
+    const int t = threadIdx.x;
+    uint8_t code = 0, esc = 1;
+#pragma unroll
+    for (int k = 0; k < 16; k++)
+        if (exps[k] == t) {
+            code = (uint8_t)k;
+            esc = 0;
+        }
+    cb[UZIP_CB_ENC + t] = code;
+    cb[UZIP_CB_ESC + t] = esc;
+    if (t < 16) {
+        cb[UZIP_CB_EXPS + t] = exps[t];
+        cb[UZIP_CB_DEC + t] = exps[t];
+    }
+    if (t == 0) {
+        reinterpret_cast<uint32_t*>(cb)[0] = kCodebookMagic;
+        reinterpret_cast<uint32_t*>(cb)[1] = 1;
+        reinterpret_cast<uint64_t*>(cb)[1] = n_sample;
+    }
+}
+
+__global__ void __launch_bounds__(256) top16_kernel(uint8_t* __restrict__ cb, uint64_t n_sample) {
+    __shared__ unsigned long long cnt[256];
+    __shared__ uint8_t exps[16];
+    const int t = threadIdx.x;
+    const unsigned long long* hist = reinterpret_cast<const unsigned long long*>(cb + UZIP_CB_HIST);
+    cnt[t] = hist[t];
+    __syncthreads();
+    const unsigned long long mine = cnt[t];
+    int rank = 0;
+    for (int i = 0; i < 256; i++) {
+        const unsigned long long c = cnt[i];
+        rank += (c > mine) || (c == mine && i < t);
+    }
+    if (rank < 16) exps[rank] = (uint8_t)t;
+    __syncthreads();
+    write_tables(exps, cb, n_sample);
+}
+
+struct Exps16 {
+    uint8_t v[16];
+};
+
+__global__ void __launch_bounds__(256) luts_kernel(Exps16 in, uint8_t* __restrict__ cb) {
+    __shared__ uint8_t exps[16];
+    if (threadIdx.x < 16) exps[threadIdx.x] = in.v[threadIdx.x];
+    unsigned long long* hist = reinterpret_cast<unsigned long long*>(cb + UZIP_CB_HIST);
+    hist[threadIdx.x] = 0;
+    __syncthreads();
+    write_tables(exps, cb, 0);
+}
+
+}  // namespace
+}  // namespace uzip
+
+using namespace uzip;
+
+extern "C" UZIP_API int uzip_calibrate(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
+                                       uzip_stream_t stream) {
+    if (!d_codebook || (n_sample > 0 && !d_sample_bf16)) return UZIP_ERR_ARG;
+    if (!aligned16(d_codebook) || (n_sample > 0 && !aligned16(d_sample_bf16))) return UZIP_ERR_ALIGN;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* cb = static_cast<uint8_t*>(d_codebook);
+    UZIP_CUDA_TRY(cudaMemsetAsync(cb + UZIP_CB_HIST, 0, 256 * sizeof(unsigned long long), s));
+    if (n_sample > 0) {
+        int dev = 0, sms = 0;
+        UZIP_CUDA_TRY(cudaGetDevice(&dev));
+        UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        const uint64_t groups = n_sample / 8;
+        uint64_t blocks = (groups + kHistThreads - 1) / kHistThreads;
+        const uint64_t cap = (uint64_t)sms * 4;
+        if (blocks > cap) blocks = cap;
+        if (blocks == 0) blocks = 1;
+        hist256_kernel<<<(unsigned)blocks, kHistThreads, 0, s>>>(
+            static_cast<const uint16_t*>(d_sample_bf16), n_sample,
+            reinterpret_cast<unsigned long long*>(cb + UZIP_CB_HIST));
+        UZIP_CUDA_TRY(cudaGetLastError());
+    }
+    top16_kernel<<<1, 256, 0, s>>>(cb, n_sample);
+    UZIP_CUDA_TRY(cudaGetLastError());
+    return UZIP_OK;
+}
+
+extern "C" UZIP_API int uzip_codebook_from_exps(const uint8_t* h_exps16, void* d_codebook,
+                                                uzip_stream_t stream) {
+    if (!h_exps16 || !d_codebook) return UZIP_ERR_ARG;
+    if (!aligned16(d_codebook)) return UZIP_ERR_ALIGN;
+    Exps16 e;
+    bool seen[256] = {false};
+    for (int k = 0; k < 16; k++) {
+        if (seen[h_exps16[k]]) return UZIP_ERR_ARG;
+        seen[h_exps16[k]] = true;
+        e.v[k] = h_exps16[k];
+    }
+    luts_kernel<<<1, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(e, static_cast<uint8_t*>(d_codebook));
+    UZIP_CUDA_TRY(cudaGetLastError());
+    return UZIP_OK;
+}

@@ -1,0 +1,194 @@
+// decode.cu -- SplitZip decoder for sm_103a.
+//
+// SplitZip review page, §3.2: decoding unpacks each byte into two 4-bit codes,
+// looks every code up in the 16-entry decode table, rebuilds the BF16 value
+// from the stored sign-mantissa byte, and then a sparse fix-up overwrites the
+// exponent of every recorded escape with its exact raw value. §3.4: the dense
+// path is the same table lookup for every value (no sentinel test).
+//
+// One CTA decodes one tile of 8192 values; the two stages are fused so each
+// output byte is written once:
+//   1. every thread issues its dense loads (8 sign-mantissa bytes + one word
+//      of eight codes per group of eight values) into registers;
+//   2. meanwhile the warps walk the escape blocks of the chunks that overlap
+//      the tile and scatter (position -> raw exponent) into a shared-memory
+//      bitmap + byte array;
+//   3. each group is decoded with the 16-byte decode table held in four
+//      registers and selected by byte permutes (three PRMTs per four values),
+//      escapes are patched from shared memory, and 16 bytes are stored.
+// The header is validated by every CTA before any output is written; escape
+// data that point outside their chunk are skipped and reported.
+#include "uzip_internal.cuh"
+
+namespace uzip {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kGroupsPerThread = 4;
+constexpr uint32_t kTileGroups = kThreads * kGroupsPerThread;  // 1024
+constexpr uint32_t kTile = kTileGroups * 8;                   // 8192 values
+
+struct Params {
+    const uint8_t* s;
+    uint64_t stream_bytes;
+    uint16_t* out;
+    uint64_t n;
+    uint32_t* status;
+};
+
+// Four codes (nibbles of c16, value i in nibble i) -> four exponent bytes.
+__device__ __forceinline__ uint32_t lookup4(uint32_t c16, uint32_t d0, uint32_t d1, uint32_t d2, uint32_t d3) {
+    const uint32_t sel = c16 & 0x7777u;
+    const uint32_t lo = prmt(d0, d1, sel);  // codes 0..7
+    const uint32_t hi = prmt(d2, d3, sel);  // codes 8..15
+    return prmt(lo, hi, 0x3210u | ((c16 & 0x8888u) >> 1));
+}
+
+// Four exponent bytes + four sign-mantissa bytes -> four BF16 values.
+__device__ __forceinline__ uint2 rebuild4(uint32_t e4, uint32_t a4) {
+    const uint32_t hi = (a4 & 0x80808080u) | ((e4 >> 1) & 0x7F7F7F7Fu);  // sign | exponent bits 7..1
+    const uint32_t lo = ((e4 << 7) & 0x80808080u) | (a4 & 0x7F7F7F7Fu);  // exponent bit 0 | mantissa
+    return make_uint2(prmt(lo, hi, 0x5140u), prmt(lo, hi, 0x7362u));
+}
+
+__device__ __forceinline__ uint32_t ld_u32_le(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+__global__ void __launch_bounds__(kThreads) decode_kernel(const Params p) {
+    __shared__ uint32_t s_mask[kTile / 32];
+    __shared__ uint8_t s_val[kTile];
+    __shared__ int s_bad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint4* h = reinterpret_cast<const uint4*>(p.s);
+    const uint4 h0 = h[0], h1 = h[1], h2 = h[2], h3 = h[3];
+    const uint64_t hn = (uint64_t)h0.z | ((uint64_t)h0.w << 32);
+    const uint32_t chunk = h1.x;
+    const uint64_t nc = h1.y;
+    const uint64_t m = (uint64_t)h1.z | ((uint64_t)h1.w << 32);
+    const uint64_t total = (uint64_t)h3.x | ((uint64_t)h3.y << 32);
+    bool ok = h0.x == kStreamMagic && (h0.y & 0xFFFF) == 1 && (h0.y >> 16) == 0 && hn == p.n &&
+              chunk_valid(chunk) && m <= hn;
+    Layout L;
+    if (ok) {
+        L = layout_of(hn, chunk);
+        ok = nc == L.nc && total == L.off_d + 3 * m && total <= p.stream_bytes;
+    }
+    if (!ok) {
+        if (blockIdx.x == 0 && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
+        return;
+    }
+
+    const uint64_t e0 = (uint64_t)blockIdx.x * kTile;
+    if (e0 >= p.n) return;  // n == 0: the single CTA only checked the header
+    const uint32_t tlen = (uint32_t)min((uint64_t)kTile, p.n - e0);
+    const uint32_t tgroups = (tlen + 7) / 8;
+    const uint8_t* A = p.s + L.off_a;
+    const uint8_t* B = p.s + L.off_b;
+    const uint8_t* C = p.s + L.off_c;
+    const uint8_t* D = p.s + L.off_d;
+
+    // 1. dense loads (the padded sections make whole-group loads safe).
+    uint2 av[kGroupsPerThread];
+    uint32_t cv[kGroupsPerThread];
+#pragma unroll
+    for (int r = 0; r < kGroupsPerThread; r++) {
+        const uint32_t g = tid + r * kThreads;
+        if (g < tgroups) {
+            const uint64_t ge = e0 + 8ull * g;
+            av[r] = *reinterpret_cast<const uint2*>(A + ge);
+            cv[r] = *reinterpret_cast<const uint32_t*>(B + ge / 2);
+        }
+    }
+    for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[i] = 0;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    // 2. escape scatter for the chunks overlapping [e0, e0 + tlen).
+    const uint64_t c_first = e0 / chunk, c_last = (e0 + tlen - 1) / chunk;
+    bool bad = false;
+    for (uint64_t c = c_first + warp; c <= c_last; c += kThreads / 32) {
+        const uint32_t o = ld_u32_le(C + 4 * c);
+        const uint32_t o1 = ld_u32_le(C + 4 * (c + 1));
+        const uint64_t cbase = c * chunk;
+        const uint32_t clen = (uint32_t)min((uint64_t)chunk, p.n - cbase);
+        if (o1 < o || o1 > m || o1 - o > clen) {
+            bad = true;
+            continue;
+        }
+        const uint32_t k = o1 - o;
+        const uint8_t* blk = D + 3ull * o;
+        for (uint32_t j = lane; j < k; j += 32) {
+            const uint32_t pos = (uint32_t)blk[2 * j] | ((uint32_t)blk[2 * j + 1] << 8);
+            if (pos >= clen) {
+                bad = true;
+                continue;
+            }
+            const uint64_t el = cbase + pos;
+            if (el >= e0 && el < e0 + tlen) {
+                const uint32_t li = (uint32_t)(el - e0);
+                s_val[li] = blk[2ull * k + j];
+                atomicOr(&s_mask[li >> 5], 1u << (li & 31));
+            }
+        }
+    }
+    if (bad) s_bad = 1;
+    __syncthreads();
+
+    // 3. decode, patch, store.
+    const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;
+#pragma unroll
+    for (int r = 0; r < kGroupsPerThread; r++) {
+        const uint32_t g = tid + r * kThreads;
+        if (g >= tgroups) continue;
+        uint32_t e_lo = lookup4(cv[r] & 0xFFFF, d0, d1, d2, d3);
+        uint32_t e_hi = lookup4(cv[r] >> 16, d0, d1, d2, d3);
+        const uint32_t fix = (s_mask[g >> 2] >> ((g & 3) * 8)) & 0xFF;
+        if (fix) {
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                if (fix & (1u << i)) {
+                    const uint32_t sh = 8 * (i & 3);
+                    const uint32_t v = (uint32_t)s_val[8 * g + i] << sh;
+                    if (i < 4) e_lo = (e_lo & ~(0xFFu << sh)) | v;
+                    else e_hi = (e_hi & ~(0xFFu << sh)) | v;
+                }
+            }
+        }
+        const uint2 lo = rebuild4(e_lo, av[r].x);
+        const uint2 hi = rebuild4(e_hi, av[r].y);
+        const uint64_t ge = e0 + 8ull * g;
+        if (ge + 8 <= p.n) {
+            *reinterpret_cast<uint4*>(p.out + ge) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        } else {
+            const uint32_t w[4] = {lo.x, lo.y, hi.x, hi.y};
+            for (uint32_t i = 0; ge + i < p.n; i++) p.out[ge + i] = (uint16_t)(w[i / 2] >> (16 * (i & 1)));
+        }
+    }
+    if (s_bad && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
+}
+
+}  // namespace
+}  // namespace uzip
+
+using namespace uzip;
+
+extern "C" UZIP_API int uzip_decode(const void* d_stream, size_t stream_bytes, void* d_out_bf16, size_t n,
+                                    uint32_t* d_status, uzip_stream_t stream) {
+    if (!d_stream || (n > 0 && !d_out_bf16) || n > UZIP_MAX_N) return UZIP_ERR_ARG;
+    if (!aligned16(d_stream) || (n > 0 && !aligned16(d_out_bf16)) ||
+        (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3)))
+        return UZIP_ERR_ALIGN;
+    if (stream_bytes < UZIP_HEADER_BYTES) return UZIP_ERR_CAPACITY;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (d_status) UZIP_CUDA_TRY(cudaMemsetAsync(d_status, 0, sizeof(uint32_t), s));
+    Params p;
+    p.s = static_cast<const uint8_t*>(d_stream);
+    p.stream_bytes = stream_bytes;
+    p.out = static_cast<uint16_t*>(d_out_bf16);
+    p.n = n;
+    p.status = d_status;
+    const uint64_t tiles = n == 0 ? 1 : (n + kTile - 1) / kTile;
+    decode_kernel<<<(unsigned)tiles, kThreads, 0, s>>>(p);
+    UZIP_CUDA_TRY(cudaGetLastError());
+    return UZIP_OK;
+}
