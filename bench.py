@@ -192,7 +192,11 @@ def run_ours(args):
     barrier()
     uz.load()
 
-    x, sample = W.workload(2, device=dev)
+    if args.tokens == W.KV_SHAPE[3]:
+        x, sample = W.workload(2, device=dev)
+    else:  # a smaller cache of the same law (profiling cases)
+        shape = W.KV_SHAPE[:3] + (args.tokens,) + W.KV_SHAPE[4:]
+        x, sample = W.kv_cache(shape, device=dev).reshape(-1), W.kv_cache_sample(device=dev)
     n = x.numel()
     raw = 2 * n
     cb = uz.new_codebook(dev)
@@ -241,7 +245,23 @@ def run_ours(args):
     max_ms = max_over_ranks(elapsed_ms, dev)
     total_raw = sum_over_ranks(raw * args.steps, dev)
 
-    # end to end through the public API with host buffers
+    if args.no_e2e:
+        e2e = None
+    else:
+        e2e = e2e_measure(args, x, sample, cb, out, wsb, y, n, raw, stream, dev)
+
+    cpu = cpu_baseline(x, sample) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+    return report(args, ws, rank, n, raw, nbytes, m, max_ms, total_raw, cal_ms, enc_ms, dec_ms, e2e, cpu,
+                  clocks, sample)
+
+
+def e2e_measure(args, x, sample, cb, out, wsb, y, n, raw, stream, dev):
+    """Same step through the public API from pinned host buffers: H2D of the
+    tensor and the sample, calibrate, encode, decode, D2H of the result."""
+    import torch
+
+    import lossless_bf16_exponent_gb300 as uz
+
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     xh.copy_(x)
     sh = torch.empty(sample.shape, dtype=sample.dtype, pin_memory=True)
@@ -271,9 +291,12 @@ def run_ours(args):
     e2e_ms = max_over_ranks(a.elapsed_time(b), dev)
     assert torch.equal(yh.view(torch.int16), xh.view(torch.int16)), "e2e round trip is not bit-exact"
     e2e_raw = sum_over_ranks(raw * e2e_steps, dev)
+    return {"value": round(e2e_raw / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": raw + 2 * sample.numel(), "d2h_bytes_per_step": raw, "steps": e2e_steps}
 
-    cpu = cpu_baseline(x, sample) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
 
+def report(args, ws, rank, n, raw, nbytes, m, max_ms, total_raw, cal_ms, enc_ms, dec_ms, e2e, cpu, clocks,
+           sample):
     if rank != 0:
         return None
     peak, peak_src = measured_peak()
@@ -296,7 +319,8 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "u16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "step": "calibrate + encode + decode",
+        "config": {"workload": WORKLOAD if n == 268435456 else f"kv_cache tokens={args.tokens} ({n} values)",
+                   "step": "calibrate + encode + decode",
                    "l2": "inputs larger than L2 (512 MiB BF16 tensor, 403 MB stream)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "encode_gbs_raw": round(raw / (enc_ms * 1e-3) / 1e9, 1),
@@ -316,9 +340,7 @@ def run_ours(args):
                      "traffic": profile_traffic(dominant),
                      "algorithmic_bytes": enc_bytes if dominant == "encode" else dec_bytes},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(e2e_raw / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": raw + 2 * sample.numel(), "d2h_bytes_per_step": raw,
-                "steps": e2e_steps},
+        "e2e": e2e,
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
     }
@@ -412,6 +434,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--tokens", type=int, default=2048,
+                    help="tokens of the KV-cache workload (2048 = the benchmark; smaller for profiling)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
