@@ -29,7 +29,7 @@
  *   - Device pointers must be 16-byte aligned (UZIP_ERR_ALIGN otherwise).
  *   - Errors found on the host return at once and enqueue nothing. Errors found
  *     on the device are reported through a status word (see each call); no
- *     kernel traps, and every device-side wait is bounded in time.
+ *     kernel traps or waits on another block.
  *
  * Compressed stream format, version 1 (all integers little endian; every part
  * before the escape section starts on a 16-byte boundary and is padded with
@@ -78,7 +78,7 @@ enum uzip_status {
     UZIP_ERR_CHUNK = 3,     /* chunk not a multiple of 8 in [8, 65536]         */
     UZIP_ERR_CAPACITY = 4,  /* output or workspace buffer too small            */
     UZIP_ERR_CORRUPT = 5,   /* stream header or escape data inconsistent       */
-    UZIP_ERR_TIMEOUT = 6,   /* a bounded device-side wait ran out              */
+    UZIP_ERR_TIMEOUT = 6,   /* reserved: no entry point waits on the device    */
     UZIP_ERR_CUDA = 7       /* a CUDA runtime call failed                      */
 };
 
@@ -89,9 +89,8 @@ enum uzip_status {
 #define UZIP_MAX_CHUNK 65536
 #define UZIP_MAX_N 0xFFFFFFFFull /* offsets and M are stored in 32 bits */
 
-/* Header status flags, set by the encoder's kernel. */
+/* Header status flags, set by the encoder's kernels. */
 #define UZIP_FLAG_CAPACITY 0x1u /* the escapes did not fit in out_capacity   */
-#define UZIP_FLAG_TIMEOUT 0x2u  /* the chunk-offset look-back wait ran out   */
 
 /* Codebook blob (UZIP_CODEBOOK_BYTES of device memory, written by
  * uzip_calibrate or uzip_codebook_from_exps):
@@ -130,14 +129,15 @@ UZIP_API int uzip_codebook_from_exps(const uint8_t *h_exps16, void *d_codebook,
  * chunk, n > UZIP_MAX_N or n_escapes > n. Host only. */
 UZIP_API size_t uzip_compressed_size(size_t n, size_t n_escapes, uint32_t chunk);
 
-/* Device workspace bytes uzip_encode needs for (n, chunk); 0 for an invalid
- * chunk or n. Host only. */
+/* Device workspace bytes uzip_encode needs for (n, chunk): about n/8 + 64
+ * (escape masks, per-2048-value escape counts, segment totals); 0 for an
+ * invalid chunk or n. Host only. */
 UZIP_API size_t uzip_encode_workspace_bytes(size_t n, uint32_t chunk);
 
-/* Encode n BF16 values (§3.2) in one fused pass: the dense stage (sign-mantissa
- * bytes and packed codes) and the escape stage (per-chunk counts, an exclusive
- * scan over the chunks by decoupled look-back, escape blocks in ascending
- * element order).
+/* Encode n BF16 values (§3.2), reading the input from HBM once: a dense kernel
+ * (sign-mantissa bytes, packed codes, escape masks and counts) and an escape
+ * kernel (chunk offsets from the escape-count prefix, escape blocks in
+ * ascending element order).
  *   d_in_bf16      n BF16 values (may be NULL when n == 0).
  *   chunk          escape-position chunk, a multiple of 8 in [8, 65536].
  *   d_codebook     from uzip_calibrate / uzip_codebook_from_exps.
@@ -151,8 +151,8 @@ UZIP_API size_t uzip_encode_workspace_bytes(size_t n, uint32_t chunk);
  *                  by the call; must not be shared with a concurrent call.
  *   h_out_bytes    NULL: fully asynchronous; read the total from the header.
  *                  Non-NULL: the call synchronises `stream`, stores the exact
- *                  stream size and returns UZIP_ERR_CAPACITY / UZIP_ERR_TIMEOUT
- *                  if the kernel set the matching header flag.
+ *                  stream size and returns UZIP_ERR_CAPACITY if the kernels
+ *                  set that header flag.
  * Bytes of d_out past the stream's total are not written. */
 UZIP_API int uzip_encode(const void *d_in_bf16, size_t n, uint32_t chunk, const void *d_codebook,
                          void *d_out, size_t out_capacity, void *d_workspace,
@@ -193,24 +193,6 @@ typedef struct {
  * UZIP_OK (h_info is filled in both cases when the header was readable). */
 UZIP_API int uzip_stream_info(const void *d_stream, size_t stream_bytes, uzip_info_t *h_info,
                               uzip_stream_t stream);
-
-/* Options of uzip_encode_ex. Zero-initialise and set what you need. */
-typedef struct {
-    uint64_t lookback_timeout_ns; /* limit of each look-back wait; 0 = 1 s     */
-    uint32_t withhold_first_unit; /* failure injection for tests: the first
-                                     unit never publishes its escape count, so
-                                     every look-back that reaches it waits the
-                                     full limit and the stream is flagged
-                                     UZIP_FLAG_TIMEOUT (the kernel still ends) */
-    uint32_t reserved;
-} uzip_encode_opts_t;
-
-/* uzip_encode with options (opts may be NULL: same as uzip_encode). Same
- * arguments, errors and asynchrony as uzip_encode. */
-UZIP_API int uzip_encode_ex(const void *d_in_bf16, size_t n, uint32_t chunk, const void *d_codebook,
-                            void *d_out, size_t out_capacity, void *d_workspace,
-                            size_t workspace_bytes, size_t *h_out_bytes,
-                            const uzip_encode_opts_t *opts, uzip_stream_t stream);
 
 /* Static text for a status code. */
 UZIP_API const char *uzip_status_string(int status);

@@ -14,12 +14,12 @@ OK, ERR_ARG, ERR_ALIGN, ERR_CHUNK, ERR_CAPACITY, ERR_CORRUPT, ERR_TIMEOUT, ERR_C
 HEADER_BYTES = 64
 CODEBOOK_BYTES = 4096
 CB_EXPS, CB_DEC, CB_ENC, CB_ESC, CB_HIST = 16, 32, 48, 304, 1024
-FLAG_CAPACITY, FLAG_TIMEOUT = 0x1, 0x2
+FLAG_CAPACITY = 0x1
 MAX_N = 0xFFFFFFFF
 
 EXPORTS = (
     "uzip_calibrate", "uzip_codebook_from_exps", "uzip_compressed_size", "uzip_encode_workspace_bytes",
-    "uzip_encode", "uzip_encode_ex", "uzip_decode", "uzip_stream_info", "uzip_status_string", "uzip_version",
+    "uzip_encode", "uzip_decode", "uzip_stream_info", "uzip_status_string", "uzip_version",
 )
 
 
@@ -29,11 +29,6 @@ class Info(ctypes.Structure):
         ("payload_bytes", ctypes.c_uint64), ("chunk", ctypes.c_uint32), ("nc", ctypes.c_uint32),
         ("version", ctypes.c_uint32), ("flags", ctypes.c_uint32), ("exps", ctypes.c_uint8 * 16),
     ]
-
-
-class EncodeOpts(ctypes.Structure):
-    _fields_ = [("lookback_timeout_ns", ctypes.c_uint64), ("withhold_first_unit", ctypes.c_uint32),
-                ("reserved", ctypes.c_uint32)]
 
 
 class UzipError(RuntimeError):
@@ -67,14 +62,12 @@ def load(path: str | None = None):
     L.uzip_encode_workspace_bytes.argtypes = [sz, u32]
     L.uzip_encode_workspace_bytes.restype = sz
     L.uzip_encode.argtypes = [vp, sz, u32, vp, vp, sz, vp, sz, ctypes.POINTER(sz), vp]
-    L.uzip_encode_ex.argtypes = [vp, sz, u32, vp, vp, sz, vp, sz, ctypes.POINTER(sz),
-                                 ctypes.POINTER(EncodeOpts), vp]
     L.uzip_decode.argtypes = [vp, sz, vp, sz, vp, vp]
     L.uzip_stream_info.argtypes = [vp, sz, ctypes.POINTER(Info), vp]
     L.uzip_status_string.argtypes = [i]
     L.uzip_status_string.restype = ctypes.c_char_p
     L.uzip_version.argtypes = []
-    for f in ("uzip_calibrate", "uzip_codebook_from_exps", "uzip_encode", "uzip_encode_ex", "uzip_decode",
+    for f in ("uzip_calibrate", "uzip_codebook_from_exps", "uzip_encode", "uzip_decode",
               "uzip_stream_info", "uzip_version"):
         getattr(L, f).restype = i
     if path is None:

@@ -86,8 +86,7 @@ def workspace_bytes(n: int, chunk: int = 1024) -> int:
 # ------------------------------------------------------------------ codec
 
 def encode(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, out: torch.Tensor | None = None,
-           workspace: torch.Tensor | None = None, sync: bool = True, timeout_ns: int = 0,
-           withhold_first_unit: bool = False):
+           workspace: torch.Tensor | None = None, sync: bool = True):
     """Encode ``x`` (SplitZip §3.2). Returns ``(stream, nbytes)``; ``stream``
     is the whole output buffer, ``nbytes`` the exact stream size (None when
     ``sync=False``: read it later with :func:`stream_info`)."""
@@ -101,12 +100,7 @@ def encode(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, out: torc
     L = load()
     args = (_p(v), n, chunk, _p(codebook), _p(out), out.numel(), _p(workspace), workspace.numel(),
             ctypes.byref(nbytes) if sync else None)
-    if timeout_ns or withhold_first_unit:
-        opts = _lib.EncodeOpts(timeout_ns, 1 if withhold_first_unit else 0, 0)
-        rc = L.uzip_encode_ex(*args, ctypes.byref(opts), _sp(v.device))
-    else:
-        rc = L.uzip_encode(*args, _sp(v.device))
-    check(rc, "uzip_encode")
+    check(L.uzip_encode(*args, _sp(v.device)), "uzip_encode")
     return out, (nbytes.value if sync else None)
 
 

@@ -1,5 +1,5 @@
 // api.cu -- host-only entry points of libuzip: exact stream sizes, header
-// inspection, status text, and the encoder variant with explicit options.
+// inspection and status text.
 #include "uzip_internal.cuh"
 
 using namespace uzip;
@@ -42,20 +42,6 @@ extern "C" UZIP_API int uzip_stream_info(const void* d_stream, size_t stream_byt
     return UZIP_OK;
 }
 
-extern "C" UZIP_API int uzip_encode_ex(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_codebook,
-                                       void* d_out, size_t out_capacity, void* d_workspace,
-                                       size_t workspace_bytes, size_t* h_out_bytes,
-                                       const uzip_encode_opts_t* opts, uzip_stream_t stream) {
-    uint64_t timeout = kDefaultTimeoutNs;
-    uint32_t withhold = 0;
-    if (opts) {
-        if (opts->lookback_timeout_ns) timeout = opts->lookback_timeout_ns;
-        withhold = opts->withhold_first_unit ? 1u : 0u;
-    }
-    return encode_impl(d_in_bf16, n, chunk, d_codebook, d_out, out_capacity, d_workspace, workspace_bytes,
-                       h_out_bytes, stream, timeout, withhold);
-}
-
 extern "C" UZIP_API const char* uzip_status_string(int status) {
     switch (status) {
         case UZIP_OK: return "ok";
@@ -64,7 +50,7 @@ extern "C" UZIP_API const char* uzip_status_string(int status) {
         case UZIP_ERR_CHUNK: return "chunk must be a multiple of 8 in [8, 65536]";
         case UZIP_ERR_CAPACITY: return "output or workspace buffer too small";
         case UZIP_ERR_CORRUPT: return "corrupt or inconsistent stream";
-        case UZIP_ERR_TIMEOUT: return "device-side wait timed out";
+        case UZIP_ERR_TIMEOUT: return "device-side wait timed out (not produced by this version)";
         case UZIP_ERR_CUDA: return "CUDA runtime error";
         default: return "unknown status";
     }

@@ -6,8 +6,9 @@
 // exponent of every recorded escape with its exact raw value. §3.4: the dense
 // path is the same table lookup for every value (no sentinel test).
 //
-// One CTA decodes one tile of 8192 values; the two stages are fused so each
-// output byte is written once:
+// Persistent CTAs (header checked and layout derived once per CTA) walk tiles
+// of 8192 values; the two stages are fused so each output byte is written
+// once:
 //   1. every thread issues its dense loads (8 sign-mantissa bytes + one word
 //      of eight codes per group of eight values) into registers;
 //   2. meanwhile the warps walk the escape blocks of the chunks that overlap
@@ -18,15 +19,27 @@
 //      escapes are patched from shared memory, and 16 bytes are stored.
 // The header is validated by every CTA before any output is written; escape
 // data that point outside their chunk are skipped and reported.
+#include <algorithm>
+
 #include "uzip_internal.cuh"
 
 namespace uzip {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kGroupsPerThread = 4;
-constexpr uint32_t kTileGroups = kThreads * kGroupsPerThread;  // 1024
-constexpr uint32_t kTile = kTileGroups * 8;                   // 8192 values
+// Tile shape (build-time tunables; the defaults are the measured best).
+#ifndef UZIP_DEC_THREADS
+#define UZIP_DEC_THREADS 256
+#endif
+#ifndef UZIP_DEC_GROUPS_PER_THREAD
+#define UZIP_DEC_GROUPS_PER_THREAD 4
+#endif
+#ifndef UZIP_DEC_MIN_BLOCKS
+#define UZIP_DEC_MIN_BLOCKS 6
+#endif
+constexpr int kThreads = UZIP_DEC_THREADS;
+constexpr int kGroupsPerThread = UZIP_DEC_GROUPS_PER_THREAD;
+constexpr uint32_t kTileGroups = kThreads * kGroupsPerThread;
+constexpr uint32_t kTile = kTileGroups * 8;  // values per tile
 
 struct Params {
     const uint8_t* s;
@@ -53,8 +66,20 @@ __device__ __forceinline__ uint2 rebuild4(uint32_t e4, uint32_t a4) {
 
 __device__ __forceinline__ uint32_t ld_u32_le(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
 
-__global__ void __launch_bounds__(kThreads) decode_kernel(const Params p) {
-    __shared__ uint32_t s_mask[kTile / 32];
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(const Params p) {
+    __shared__ uint32_t s_mask[2][kTile / 32];  // escape bitmap, double-buffered by tile parity
     __shared__ uint8_t s_val[kTile];
     __shared__ int s_bad;
 
@@ -77,92 +102,103 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const Params p) {
         if (blockIdx.x == 0 && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
         return;
     }
-
-    const uint64_t e0 = (uint64_t)blockIdx.x * kTile;
-    if (e0 >= p.n) return;  // n == 0: the single CTA only checked the header
-    const uint32_t tlen = (uint32_t)min((uint64_t)kTile, p.n - e0);
-    const uint32_t tgroups = (tlen + 7) / 8;
+    const uint32_t n32 = (uint32_t)p.n;  // n < 2^32
     const uint8_t* A = p.s + L.off_a;
     const uint8_t* B = p.s + L.off_b;
     const uint8_t* C = p.s + L.off_c;
     const uint8_t* D = p.s + L.off_d;
+    const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;  // decode table: code k -> byte k
+    const uint32_t tiles = (n32 + kTile - 1) / kTile;
 
-    // 1. dense loads (the padded sections make whole-group loads safe).
-    uint2 av[kGroupsPerThread];
-    uint32_t cv[kGroupsPerThread];
-#pragma unroll
-    for (int r = 0; r < kGroupsPerThread; r++) {
-        const uint32_t g = tid + r * kThreads;
-        if (g < tgroups) {
-            const uint64_t ge = e0 + 8ull * g;
-            av[r] = *reinterpret_cast<const uint2*>(A + ge);
-            cv[r] = *reinterpret_cast<const uint32_t*>(B + ge / 2);
-        }
-    }
-    for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[i] = 0;
+    for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[0][i] = 0;
     if (tid == 0) s_bad = 0;
     __syncthreads();
 
-    // 2. escape scatter for the chunks overlapping [e0, e0 + tlen).
-    const uint64_t c_first = e0 / chunk, c_last = (e0 + tlen - 1) / chunk;
-    bool bad = false;
-    for (uint64_t c = c_first + warp; c <= c_last; c += kThreads / 32) {
-        const uint32_t o = ld_u32_le(C + 4 * c);
-        const uint32_t o1 = ld_u32_le(C + 4 * (c + 1));
-        const uint64_t cbase = c * chunk;
-        const uint32_t clen = (uint32_t)min((uint64_t)chunk, p.n - cbase);
-        if (o1 < o || o1 > m || o1 - o > clen) {
-            bad = true;
-            continue;
+    int par = 0;
+    for (uint32_t t = blockIdx.x; t < tiles; t += gridDim.x, par ^= 1) {
+        const uint32_t e0 = t * kTile;
+        const uint32_t tlen = min(kTile, n32 - e0);
+        const uint32_t tgroups = (tlen + 7) / 8;
+        const uint8_t* At = A + e0;
+        const uint8_t* Bt = B + e0 / 2;
+
+        // 1. dense loads first, so their latency overlaps the escape pass (the
+        //    padded sections make whole-group loads safe at the ragged tail).
+        uint2 av[kGroupsPerThread];
+        uint32_t cv[kGroupsPerThread];
+#pragma unroll
+        for (int r = 0; r < kGroupsPerThread; r++) {
+            const uint32_t g = tid + r * kThreads;
+            if (g < tgroups) {
+                av[r] = ld_stream_v2(At + 8 * g);
+                cv[r] = ld_stream_u32(Bt + 4 * g);
+            }
         }
-        const uint32_t k = o1 - o;
-        const uint8_t* blk = D + 3ull * o;
-        for (uint32_t j = lane; j < k; j += 32) {
-            const uint32_t pos = (uint32_t)blk[2 * j] | ((uint32_t)blk[2 * j + 1] << 8);
-            if (pos >= clen) {
+        // 2. clear the other bitmap for the next tile; scatter this tile's
+        //    escapes (chunks overlapping [e0, e0 + tlen)) into this one.
+        for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[par ^ 1][i] = 0;
+        const uint32_t c_first = e0 / chunk, c_last = (e0 + tlen - 1) / chunk;
+        bool bad = false;
+        for (uint32_t c = c_first + warp; c <= c_last; c += kThreads / 32) {
+            const uint32_t o = ld_u32_le(C + 4ull * c);
+            const uint32_t o1 = ld_u32_le(C + 4ull * (c + 1));
+            const uint32_t cbase = c * chunk;
+            const uint32_t clen = min(chunk, n32 - cbase);
+            if (o1 < o || o1 > m || o1 - o > clen) {
                 bad = true;
                 continue;
             }
-            const uint64_t el = cbase + pos;
-            if (el >= e0 && el < e0 + tlen) {
-                const uint32_t li = (uint32_t)(el - e0);
-                s_val[li] = blk[2ull * k + j];
-                atomicOr(&s_mask[li >> 5], 1u << (li & 31));
-            }
-        }
-    }
-    if (bad) s_bad = 1;
-    __syncthreads();
-
-    // 3. decode, patch, store.
-    const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;
-#pragma unroll
-    for (int r = 0; r < kGroupsPerThread; r++) {
-        const uint32_t g = tid + r * kThreads;
-        if (g >= tgroups) continue;
-        uint32_t e_lo = lookup4(cv[r] & 0xFFFF, d0, d1, d2, d3);
-        uint32_t e_hi = lookup4(cv[r] >> 16, d0, d1, d2, d3);
-        const uint32_t fix = (s_mask[g >> 2] >> ((g & 3) * 8)) & 0xFF;
-        if (fix) {
-#pragma unroll
-            for (int i = 0; i < 8; i++) {
-                if (fix & (1u << i)) {
-                    const uint32_t sh = 8 * (i & 3);
-                    const uint32_t v = (uint32_t)s_val[8 * g + i] << sh;
-                    if (i < 4) e_lo = (e_lo & ~(0xFFu << sh)) | v;
-                    else e_hi = (e_hi & ~(0xFFu << sh)) | v;
+            const uint32_t k = o1 - o;
+            const uint8_t* blk = D + 3ull * o;
+            for (uint32_t j = lane; j < k; j += 32) {
+                const uint32_t pos = (uint32_t)blk[2 * j] | ((uint32_t)blk[2 * j + 1] << 8);
+                if (pos >= clen) {
+                    bad = true;
+                    continue;
+                }
+                const uint32_t el = cbase + pos;
+                if (el >= e0 && el < e0 + tlen) {
+                    const uint32_t li = el - e0;
+                    s_val[li] = blk[2 * k + j];
+                    atomicOr(&s_mask[par][li >> 5], 1u << (li & 31));
                 }
             }
         }
-        const uint2 lo = rebuild4(e_lo, av[r].x);
-        const uint2 hi = rebuild4(e_hi, av[r].y);
-        const uint64_t ge = e0 + 8ull * g;
-        if (ge + 8 <= p.n) {
-            *reinterpret_cast<uint4*>(p.out + ge) = make_uint4(lo.x, lo.y, hi.x, hi.y);
-        } else {
-            const uint32_t w[4] = {lo.x, lo.y, hi.x, hi.y};
-            for (uint32_t i = 0; ge + i < p.n; i++) p.out[ge + i] = (uint16_t)(w[i / 2] >> (16 * (i & 1)));
+        if (bad) s_bad = 1;
+        __syncthreads();
+
+        // 3. decode, patch, store.
+#pragma unroll
+        for (int r = 0; r < kGroupsPerThread; r++) {
+            const uint32_t g = tid + r * kThreads;
+            if (g >= tgroups) continue;
+            uint32_t e_lo = lookup4(cv[r] & 0xFFFF, d0, d1, d2, d3);
+            uint32_t e_hi = lookup4(cv[r] >> 16, d0, d1, d2, d3);
+            const uint32_t fix = (s_mask[par][g >> 2] >> ((g & 3) * 8)) & 0xFF;
+            if (fix) {
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    if (fix & (1u << i)) {
+                        const uint32_t sh = 8 * (i & 3);
+                        const uint32_t v = (uint32_t)s_val[8 * g + i] << sh;
+                        if (i < 4) e_lo = (e_lo & ~(0xFFu << sh)) | v;
+                        else e_hi = (e_hi & ~(0xFFu << sh)) | v;
+                    }
+                }
+            }
+            const uint2 lo = rebuild4(e_lo, av[r].x);
+            const uint2 hi = rebuild4(e_hi, av[r].y);
+            const uint32_t ge = e0 + 8 * g;
+            if (ge + 8 <= n32) {
+                *reinterpret_cast<uint4*>(p.out + ge) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            } else {
+                const uint32_t w[4] = {lo.x, lo.y, hi.x, hi.y};
+#pragma unroll
+                for (uint32_t i = 0; i < 8; i++)
+                    if (ge + i < n32) p.out[ge + i] = (uint16_t)(w[i / 2] >> (16 * (i & 1)));
+            }
         }
+        __syncthreads();  // s_val and this bitmap are rewritten by the next tile
     }
     if (s_bad && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
 }
@@ -187,8 +223,14 @@ extern "C" UZIP_API int uzip_decode(const void* d_stream, size_t stream_bytes, v
     p.out = static_cast<uint16_t*>(d_out_bf16);
     p.n = n;
     p.status = d_status;
-    const uint64_t tiles = n == 0 ? 1 : (n + kTile - 1) / kTile;
-    decode_kernel<<<(unsigned)tiles, kThreads, 0, s>>>(p);
+    int dev = 0, sms = 0, per_sm = 0;
+    UZIP_CUDA_TRY(cudaGetDevice(&dev));
+    UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, 0));
+    if (per_sm < 1) return UZIP_ERR_CUDA;
+    const uint64_t tiles = (n + kTile - 1) / kTile;
+    const uint64_t grid = std::max<uint64_t>(1, std::min<uint64_t>(tiles, (uint64_t)sms * per_sm));
+    decode_kernel<<<(unsigned)grid, kThreads, 0, s>>>(p);
     UZIP_CUDA_TRY(cudaGetLastError());
     return UZIP_OK;
 }

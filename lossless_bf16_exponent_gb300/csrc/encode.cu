@@ -1,71 +1,89 @@
-// encode.cu -- fused single-pass SplitZip encoder for sm_103a.
+// encode.cu -- SplitZip encoder for sm_103a: one pass over the input, two kernels.
 //
 // SplitZip review page, §3.2: encoding is (1) a dense transform -- split each
 // BF16 value into its exponent and sign-mantissa byte, store the latter
 // verbatim, map the exponent through the Top-16 code table and pack two 4-bit
 // codes per byte -- and (2) a scan of the exponent stream that pushes every
 // exponent outside the Top-16 into chunked escape position / value arrays.
-// Appendix A (Quad64): both stages fused into one kernel over wide words; here
-// each thread moves 16-byte vectors (eight values) instead of 64-bit words.
+// Appendix A (Quad64): the dense work is fused into one pass over wide words;
+// here each thread moves 16-byte vectors (eight values).
 //
-// One CTA encodes one "unit": a run of whole chunks (about 8192 values; one
-// chunk when the chunk is longer, walked in 8192-value sub-tiles). Unit ids
-// come from an atomic ticket, so a unit's predecessors are always held by CTAs
-// that already run. Per unit:
-//   dense   16-byte loads -> exponent / sign-mantissa bytes with byte permutes
-//           -> code + escape bit from a 256-byte shared table -> 8-byte
-//           sign-mantissa store + 4-byte code store, both coalesced; an 8-bit
-//           escape mask per group of eight values goes to shared memory.
-//   count   each thread sums the escape masks of a contiguous run of groups; a
-//           block scan gives every run's escape rank inside the unit and every
-//           chunk's first rank.
-//   scan    decoupled look-back (one warp, 32 predecessors per step) over
-//           64-bit unit descriptors {flag, count}: the unit publishes its
-//           aggregate at once, sums predecessors' aggregates until it meets an
-//           inclusive prefix, then publishes its own inclusive prefix. Every
-//           wait is bounded by a time limit; running out sets a header flag.
-//   write   chunk offsets (u32), then each escape: its chunk-relative position
-//           into the chunk's position array and its raw exponent (re-read from
-//           the input, which is still in L2) into the chunk's value array, in
-//           ascending element order. Writes past out_capacity are dropped and
-//           flagged.
-//   finish  the last CTA to finish writes the 64-byte header and the padding.
+// The only serial dependency is the escape prefix (where each chunk's escape
+// block starts), which a single-pass decoupled look-back resolves through a
+// chain of inclusive prefixes; on GB300 that chain, not HBM, set the pace
+// (one window of predecessors per loaded-L2 round trip). So the prefix is
+// resolved by the kernel boundary instead:
+//   dense kernel   each warp owns fixed units of 2048 values (grid-stride, no
+//                  tickets, no barriers): 16-byte loads -> exponent and
+//                  sign-mantissa bytes with byte permutes -> code + escape bit
+//                  from a 256-byte shared table -> coalesced 8-byte
+//                  sign-mantissa and 4-byte code stores; one escape-mask byte
+//                  per group of eight values into the workspace (N/8 bytes),
+//                  the unit's escape count, and the count added to its
+//                  segment's total (64+ units per segment).
+//   escape kernel  every CTA scans the segment totals in shared memory; each
+//                  warp takes ranges of whole chunks, finds the range's first
+//                  escape rank from the segment prefix, unit counts and masks,
+//                  writes the chunk offsets, and writes each escape's
+//                  chunk-relative position and raw exponent (re-read from the
+//                  input, eight loads in flight per lane) in ascending element
+//                  order, bounds-checked against out_capacity. The last CTA to
+//                  finish writes the 64-byte header.
+// The input is read from HBM once; the masks add N/8 bytes written and read.
+#include <algorithm>
+
 #include "uzip_internal.cuh"
 
 namespace uzip {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kGroupsPerThread = 4;                        // 16-byte groups per thread per sub-tile
-constexpr int kSubGroups = kThreads * kGroupsPerThread;    // 1024 groups
-constexpr uint32_t kSubElems = kSubGroups * 8;             // 8192 values
+constexpr uint32_t kUnit = 2048;              // values per counting unit (one warp)
+constexpr uint32_t kUnitGroups = kUnit / 8;   // its mask bytes
+constexpr int kThreads = 256;                 // both kernels
+constexpr int kWarps = kThreads / 32;
+constexpr uint32_t kMaxSegments = 2048;       // segment totals one CTA scans
+constexpr uint32_t kRangeValues = 16384;      // target values per escape-kernel range
+constexpr uint32_t kMaxRangeChunks = 256;     // bounds the per-warp chunk table
+constexpr int kBatch = 8;                     // escape exponents re-read per lane at once
+#ifndef UZIP_ENC_MIN_BLOCKS
+#define UZIP_ENC_MIN_BLOCKS 4
+#endif
+#ifndef UZIP_ENC_ITER_UNROLL
+#define UZIP_ENC_ITER_UNROLL 2
+#endif
+constexpr int kIterUnroll = UZIP_ENC_ITER_UNROLL;  // 2: both 4-load batches of a unit in flight per lane
 
-constexpr uint64_t kFlagAgg = 1ull << 62;
-constexpr uint64_t kFlagInc = 2ull << 62;
-constexpr uint64_t kValMask = (1ull << 62) - 1;
-
-// Start of the caller's workspace; the unit descriptors follow at +64.
-struct Workspace {
-    unsigned int ticket;
+// Start of the caller's workspace.
+struct WsHeader {
     unsigned int done;
     unsigned int flags;
-    unsigned int pad0;
     unsigned long long m;
-    unsigned long long pad1[5];
+    unsigned long long pad[6];
 };
-static_assert(sizeof(Workspace) == 64, "workspace header is 64 bytes");
+static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
 
 struct Geometry {
-    uint32_t chunks_per_unit;  // whole chunks in a full unit
-    uint32_t unit_elems;       // values in a full unit
-    uint64_t units;
+    uint64_t units;         // counting units of kUnit values
+    uint32_t seg_units;     // units per segment (power of two, >= 64)
+    uint32_t nseg;          // segments
+    uint32_t range_chunks;  // chunks per escape-kernel range
+    uint64_t ranges;
+    uint64_t off_segs, off_counts, off_masks, bytes;  // workspace layout
 };
 
 __host__ Geometry geometry_of(uint64_t n, uint32_t chunk) {
     Geometry g;
-    g.chunks_per_unit = chunk <= kSubElems ? kSubElems / chunk : 1;
-    g.unit_elems = g.chunks_per_unit * chunk;
-    g.units = (n + g.unit_elems - 1) / g.unit_elems;
+    g.units = (n + kUnit - 1) / kUnit;
+    g.seg_units = 64;
+    while ((g.units + g.seg_units - 1) / g.seg_units > kMaxSegments) g.seg_units *= 2;
+    g.nseg = (uint32_t)((g.units + g.seg_units - 1) / g.seg_units);
+    g.range_chunks = std::max<uint32_t>(1, std::min<uint32_t>(kRangeValues / chunk, kMaxRangeChunks));
+    const uint64_t nc = (n + chunk - 1) / chunk;
+    g.ranges = (nc + g.range_chunks - 1) / g.range_chunks;
+    g.off_segs = sizeof(WsHeader);
+    g.off_counts = g.off_segs + pad16(4ull * g.nseg);
+    g.off_masks = g.off_counts + pad16(4ull * g.units);
+    g.bytes = g.off_masks + pad16((n + 7) / 8);
     return g;
 }
 
@@ -73,16 +91,19 @@ struct Params {
     const uint16_t* in;
     uint64_t n;
     uint32_t chunk;
-    uint32_t unit_elems;
+    uint32_t seg_units;
+    uint32_t nseg;
+    uint32_t range_chunks;
     uint64_t units;
+    uint64_t ranges;
     const uint8_t* cb;
     uint8_t* out;
     uint64_t cap;
     Layout L;
-    Workspace* ws;
-    unsigned long long* desc;
-    uint64_t timeout_ns;
-    uint32_t withhold_first;  // failure-injection: unit 0 never publishes
+    WsHeader* ws;
+    uint32_t* segs;
+    uint32_t* counts;
+    uint8_t* masks;
 };
 
 // Eight values -> 8 sign-mantissa bytes (a_lo, a_hi), 8 packed codes (one
@@ -90,7 +111,7 @@ struct Params {
 __device__ __forceinline__ void encode_group(const uint4 v, const uint8_t* tab, uint32_t& a_lo,
                                              uint32_t& a_hi, uint32_t& codes, uint32_t& mask) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t packed[2], esc[2];
+    uint32_t packed[2], esc[2], am[2];
 #pragma unroll
     for (int h = 0; h < 2; h++) {
         // Bytes of four values: high bytes (sign + exponent bits 7..1) and
@@ -98,91 +119,24 @@ __device__ __forceinline__ void encode_group(const uint4 v, const uint8_t* tab, 
         const uint32_t hi = prmt(w[2 * h], w[2 * h + 1], 0x7531);
         const uint32_t lo = prmt(w[2 * h], w[2 * h + 1], 0x6420);
         const uint32_t e4 = ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
-        const uint32_t a4 = (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
-        if (h == 0) a_lo = a4; else a_hi = a4;
+        am[h] = (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
         // Table byte = code | escape << 7.
         const uint32_t t0 = tab[e4 & 0xFF];
         const uint32_t t1 = tab[(e4 >> 8) & 0xFF];
         const uint32_t t2 = tab[(e4 >> 16) & 0xFF];
         const uint32_t t3 = tab[e4 >> 24];
-        const uint32_t t4 = t0 | (t1 << 8) | (t2 << 16) | (t3 << 24);
+        const uint32_t t4 = prmt(prmt(t0, t1, 0x0040), prmt(t2, t3, 0x0040), 0x5410);
         const uint32_t c = t4 & 0x0F0F0F0Fu;
         packed[h] = c | (c >> 4);  // byte 0 = c0 | c1 << 4, byte 2 = c2 | c3 << 4
         esc[h] = t4 & 0x80808080u;
     }
+    a_lo = am[0];
+    a_hi = am[1];
     codes = prmt(packed[0], packed[1], 0x6420);
     // Bit 7 of byte i -> bit i (the four shifted copies never overlap).
     const uint32_t m_lo = (((esc[0] >> 7) * 0x204081u) >> 21) & 0xF;
     const uint32_t m_hi = (((esc[1] >> 7) * 0x204081u) >> 21) & 0xF;
     mask = m_lo | (m_hi << 4);
-}
-
-__device__ __forceinline__ void block_exclusive_scan(uint32_t v, uint32_t& excl, uint32_t& total,
-                                                     uint32_t* s_warp) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    uint32_t before = 0, all = 0;
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; w++) {
-        const uint32_t s = s_warp[w];
-        before += (w < warp) ? s : 0;
-        all += s;
-    }
-    excl = before + incl - v;
-    total = all;
-}
-
-// Decoupled look-back by warp 0; returns the unit's exclusive escape prefix.
-__device__ uint64_t lookback(const Params& p, uint64_t u, uint32_t total) {
-    const int lane = threadIdx.x & 31;
-    if (u == 0) {
-        if (lane == 0 && !p.withhold_first) st_relaxed_u64(p.desc, kFlagInc | total);
-        return 0;
-    }
-    if (lane == 0) st_relaxed_u64(p.desc + u, kFlagAgg | total);
-    uint64_t prefix = 0;
-    int64_t nearest = (int64_t)u - 1;
-    const uint64_t t0 = globaltimer_ns();
-    bool timed_out = false;
-    for (;;) {
-        const int64_t idx = nearest - lane;
-        uint64_t d;
-        for (;;) {
-            d = idx >= 0 ? ld_relaxed_u64(p.desc + idx) : kFlagInc;
-            if (!__any_sync(0xffffffffu, (d >> 62) == 0)) break;
-            if (__any_sync(0xffffffffu, globaltimer_ns() - t0 > p.timeout_ns)) {
-                timed_out = true;
-                break;
-            }
-            __nanosleep(32);
-        }
-        if (timed_out) break;
-        const uint32_t inc = __ballot_sync(0xffffffffu, (d >> 62) == 2);
-        const int stop = inc ? __ffs(inc) - 1 : 31;
-        uint64_t val = lane <= stop ? (d & kValMask) : 0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) val += __shfl_xor_sync(0xffffffffu, val, o);
-        prefix += val;
-        if (inc) break;
-        nearest -= 32;
-    }
-    if (lane == 0) {
-        if (timed_out) atomicOr(&p.ws->flags, UZIP_FLAG_TIMEOUT);
-        st_relaxed_u64(p.desc + u, kFlagInc | ((prefix + total) & kValMask));
-    }
-    return prefix;
-}
-
-__device__ __forceinline__ void put_byte(const Params& p, uint64_t off, uint8_t v, bool& overflow) {
-    if (off < p.cap) p.out[off] = v;
-    else overflow = true;
 }
 
 __device__ void write_header(const Params& p, uint64_t m, uint32_t flags) {
@@ -200,137 +154,345 @@ __device__ void zero_words(uint8_t* out, uint64_t from, uint64_t to) {
     for (uint64_t o = from; o < to; o += 4) *reinterpret_cast<uint32_t*>(out + o) = 0;
 }
 
-__global__ void __launch_bounds__(kThreads) encode_kernel(const Params p) {
-    extern __shared__ __align__(16) uint8_t dyn[];
+__device__ __forceinline__ uint32_t warp_sum(uint32_t v) { return __reduce_add_sync(0xffffffffu, v); }
+
+// ------------------------------------------------------------ dense kernel
+
+__global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_kernel(const Params p) {
     __shared__ uint32_t s_tab_words[64];
-    __shared__ uint32_t s_warp[kThreads / 32];
-    __shared__ unsigned long long s_unit, s_prefix;
-
-    const int tid = threadIdx.x;
     uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_tab_words);
-    uint8_t* s_mask = dyn;
-    uint32_t* s_cpref = reinterpret_cast<uint32_t*>(dyn + pad16(p.unit_elems / 8));
-
-    if (tid == 0) s_unit = atomicAdd(&p.ws->ticket, 1u);
-    s_tab[tid] = p.cb[UZIP_CB_ENC + tid] | (p.cb[UZIP_CB_ESC + tid] ? 0x80 : 0);
+    s_tab[threadIdx.x] = p.cb[UZIP_CB_ENC + threadIdx.x] | (p.cb[UZIP_CB_ESC + threadIdx.x] ? 0x80 : 0);
     __syncthreads();
 
-    const uint64_t u = s_unit;
-    const uint64_t ubase = u * p.unit_elems;
-    const uint32_t ulen = (uint32_t)min((uint64_t)p.unit_elems, p.n - ubase);
-    const uint32_t ugroups = (ulen + 7) / 8;
-    const uint4* in4 = reinterpret_cast<const uint4*>(p.in);
-
-    // ---------------------------------------------------------------- dense
-    for (uint32_t g0 = 0; g0 < ugroups; g0 += kSubGroups) {
-        uint4 v[kGroupsPerThread];
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t stride = (uint64_t)gridDim.x * kWarps;
+    for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride) {
+        const uint64_t ubase = u * kUnit;
+        const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
+        const uint4* src = reinterpret_cast<const uint4*>(p.in + ubase);
+        uint8_t* dst_a = p.out + p.L.off_a + ubase;
+        uint8_t* dst_b = p.out + p.L.off_b + ubase / 2;
+        uint8_t* gmask = p.masks + u * kUnitGroups;
+        uint32_t cnt = 0;
+#pragma unroll kIterUnroll
+        for (int it = 0; it < 2; it++) {
+            uint4 v[4];
 #pragma unroll
-        for (int r = 0; r < kGroupsPerThread; r++) {
-            const uint32_t g = g0 + tid + r * kThreads;
-            const uint64_t e0 = ubase + 8ull * g;
-            v[r] = make_uint4(0, 0, 0, 0);
-            if (g < ugroups) {
-                if (e0 + 8 <= p.n) {
-                    v[r] = ld_stream_v4(in4 + (e0 >> 3));
-                } else {
+            for (int r = 0; r < 4; r++) {
+                const uint32_t g = it * 128 + r * 32 + lane;
+                v[r] = make_uint4(0, 0, 0, 0);
+                if (8 * g + 8 <= ulen) {
+                    v[r] = ld_stream_v4(src + g);
+                } else if (8 * g < ulen) {  // ragged tail of the tensor (< 8 values)
                     uint32_t w[4] = {0, 0, 0, 0};
-                    for (uint32_t i = 0; e0 + i < p.n; i++) w[i / 2] |= (uint32_t)p.in[e0 + i] << (16 * (i & 1));
+#pragma unroll
+                    for (uint32_t i = 0; i < 8; i++)
+                        if (8 * g + i < ulen) w[i / 2] |= (uint32_t)p.in[ubase + 8 * g + i] << (16 * (i & 1));
                     v[r] = make_uint4(w[0], w[1], w[2], w[3]);
                 }
             }
+#pragma unroll
+            for (int r = 0; r < 4; r++) {
+                const uint32_t g = it * 128 + r * 32 + lane;
+                if (8 * g >= ulen) continue;
+                uint32_t a_lo, a_hi, codes, mask;
+                encode_group(v[r], s_tab, a_lo, a_hi, codes, mask);
+                if (8 * g + 8 > ulen) {  // codes and escapes of real values only
+                    const uint32_t valid = ulen - 8 * g;
+                    mask &= (1u << valid) - 1;
+                    codes &= (1u << (4 * valid)) - 1;
+                }
+                *reinterpret_cast<uint2*>(dst_a + 8 * g) = make_uint2(a_lo, a_hi);
+                *reinterpret_cast<uint32_t*>(dst_b + 4 * g) = codes;
+                gmask[g] = (uint8_t)mask;
+                cnt += __popc(mask);
+            }
+        }
+        cnt = warp_sum(cnt);
+        if (lane == 0) {
+            p.counts[u] = cnt;
+            if (cnt) atomicAdd(&p.segs[u / p.seg_units], cnt);
+        }
+    }
+}
+
+// ----------------------------------------------------------- escape kernel
+
+// Escapes before value s (s a multiple of 8): the segment prefix, the counts
+// of the earlier units of its segment, the mask bytes of its own unit. A
+// segment holds at most 64 units at this size, so each lane loads at most two
+// counts and eight mask bytes, all at once.
+__device__ uint64_t escapes_before(const Params& p, const uint32_t* s_segpref, uint32_t s) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t us = s / kUnit;
+    const uint32_t seg = us / p.seg_units;
+    uint32_t part = 0;
+    uint32_t i = seg * p.seg_units + lane;
+    for (; i + 32 < us; i += 64) part += p.counts[i] + p.counts[i + 32];
+    if (i < us) part += p.counts[i];
+    const uint32_t bend = s / 8;
+    uint32_t b = us * kUnitGroups + lane;
+    uint32_t m[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) m[j] = (b + 32 * j < bend) ? p.masks[b + 32 * j] : 0;
+#pragma unroll
+    for (int j = 0; j < 8; j++) part += __popc(m[j]);
+    return (uint64_t)s_segpref[seg] + warp_sum(part);
+}
+
+constexpr uint32_t kWinValues = 16384;  // values per mask window (2 KiB of mask bytes)
+constexpr int kVecPerLane = 5;           // 16-byte mask vectors per lane per window (128 + 2 slack)
+
+// One lane's share of a window of mask bytes: the 16-byte vectors [v0, v1) of
+// the aligned span around the window's bytes, bytes outside the window
+// cleared, kept in shared memory transposed (word k of lane l at
+// sw[k * 32 + l]) so a warp touching word k of every lane hits 32 different
+// banks. Bit i of word k stands for value 8 * (a_first + 4 * k) + i.
+constexpr int kLaneWords = kVecPerLane * 4;
+
+struct LaneSpan {
+    uint32_t a_first;  // byte address of the lane's word 0 in the mask section
+    uint32_t nwords;   // words the lane holds (<= kLaneWords)
+};
+
+__device__ __forceinline__ LaneSpan load_lane_masks(const Params& p, uint32_t b0, uint32_t nb, uint32_t* sw) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t a0 = b0 & ~15u;
+    const uint32_t nvec = (b0 + nb - a0 + 15) / 16;
+    const uint32_t vpl = (nvec + 31) / 32;
+    const uint32_t v0 = min(lane * vpl, nvec), v1 = min(v0 + vpl, nvec);
+    LaneSpan sp;
+    sp.a_first = a0 + 16 * v0;
+    sp.nwords = 4 * (v1 - v0);
+    const uint4* src = reinterpret_cast<const uint4*>(p.masks + a0);
+    uint4 v[kVecPerLane];
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; j++) v[j] = (v0 + j < v1) ? src[v0 + j] : make_uint4(0, 0, 0, 0);
+    const uint32_t lo = b0, hi = b0 + nb;  // the window's bytes
+#pragma unroll
+    for (int j = 0; j < kVecPerLane; j++) {
+        uint32_t vw[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        const uint32_t a = sp.a_first + 16 * j;
+        if (a < lo || a + 16 > hi) {  // an edge vector: clear bytes outside the window
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const uint32_t wa = a + 4 * k;
+                const uint32_t from = lo > wa ? min(lo - wa, 4u) : 0u;  // first kept byte
+                const uint32_t to = hi > wa ? min(hi - wa, 4u) : 0u;     // one past the last
+                const uint32_t upto = to >= 4 ? 0xFFFFFFFFu : (1u << (8 * to)) - 1;
+                const uint32_t below = from >= 4 ? 0xFFFFFFFFu : (1u << (8 * from)) - 1;
+                vw[k] &= upto & ~below;
+            }
         }
 #pragma unroll
-        for (int r = 0; r < kGroupsPerThread; r++) {
-            const uint32_t g = g0 + tid + r * kThreads;
-            if (g >= ugroups) continue;
-            const uint64_t e0 = ubase + 8ull * g;
-            uint32_t a_lo, a_hi, codes, mask;
-            encode_group(v[r], s_tab, a_lo, a_hi, codes, mask);
-            if (e0 + 8 > p.n) {  // ragged tail: codes and escapes of real values only
-                const uint32_t valid = (uint32_t)(p.n - e0);
-                mask &= (1u << valid) - 1;
-                codes &= (1u << (4 * valid)) - 1;
-            }
-            *reinterpret_cast<uint2*>(p.out + p.L.off_a + e0) = make_uint2(a_lo, a_hi);
-            *reinterpret_cast<uint32_t*>(p.out + p.L.off_b + e0 / 2) = codes;
-            s_mask[g] = (uint8_t)mask;
-        }
+        for (int k = 0; k < 4; k++) sw[(4 * j + k) * 32 + lane] = vw[k];
     }
-    __syncthreads();
+    return sp;
+}
 
-    // ---------------------------------------------------------------- count
-    const uint32_t run = (ugroups + kThreads - 1) / kThreads;
-    const uint32_t gbeg = min(tid * run, ugroups), gend = min(gbeg + run, ugroups);
-    uint32_t cnt = 0;
-    for (uint32_t g = gbeg; g < gend; g++) cnt += __popc(s_mask[g]);
-    uint32_t excl, total;
-    block_exclusive_scan(cnt, excl, total, s_warp);
+__global__ void __launch_bounds__(kThreads, 3) encode_escape_kernel(const Params p) {
+    extern __shared__ __align__(16) uint32_t s_dyn[];
+    __shared__ uint32_t s_warp[kWarps];
+    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // Layout: per-warp mask words | segment prefix (nseg + 1) | per-warp chunk tables.
+    uint32_t* sw = s_dyn + warp * (kLaneWords * 32);
+    uint32_t* s_segpref = s_dyn + kWarps * kLaneWords * 32;
+    uint32_t* s_cp = s_segpref + ((p.nseg + 1 + 3) & ~3u) + warp * (p.range_chunks + 1);
+
+    // Segment prefix, one block scan (kMaxSegments / kThreads = 8 totals per
+    // thread, loaded together).
     {
-        uint32_t running = excl;
-        for (uint32_t g = gbeg; g < gend; g++) {
-            const uint32_t el = 8 * g;
-            if (el % p.chunk == 0) s_cpref[el / p.chunk] = running;
-            running += __popc(s_mask[g]);
+        constexpr int kPer = kMaxSegments / kThreads;
+        uint32_t v[kPer];
+        uint32_t sum = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; i++) {
+            const uint32_t idx = tid * kPer + i;
+            v[i] = idx < p.nseg ? p.segs[idx] : 0;
         }
+#pragma unroll
+        for (int i = 0; i < kPer; i++) sum += v[i];
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        uint32_t run = incl - sum;
+        for (uint32_t w = 0; w < warp; w++) run += s_warp[w];
+#pragma unroll
+        for (int i = 0; i < kPer; i++) {
+            const uint32_t idx = tid * kPer + i;
+            if (idx <= p.nseg) s_segpref[idx] = run;
+            run += v[i];
+        }
+        __syncthreads();
     }
-    const uint32_t uchunks = (ulen + p.chunk - 1) / p.chunk;
-    if (tid == 0) s_cpref[uchunks] = total;
 
-    // ----------------------------------------------------------------- scan
-    if (tid < 32) {
-        const uint64_t prefix = lookback(p, u, total);
-        if (tid == 0) s_prefix = prefix;
-    }
-    __syncthreads();
-    const uint64_t prefix = s_prefix;
-
-    // ---------------------------------------------------------------- write
-    const uint64_t c0 = ubase / p.chunk;
-    uint8_t* offs = p.out + p.L.off_c;
-    for (uint32_t ci = tid; ci < uchunks; ci += kThreads)
-        *reinterpret_cast<uint32_t*>(offs + 4 * (c0 + ci)) = (uint32_t)(prefix + s_cpref[ci]);
-    const bool last_unit = (u == p.units - 1);
-    if (last_unit && tid == 0) {
-        const uint64_t m = prefix + total;
-        *reinterpret_cast<uint32_t*>(offs + 4 * p.L.nc) = (uint32_t)m;
-        zero_words(p.out, p.L.off_c + 4 * (p.L.nc + 1), p.L.off_d);
-        const uint64_t groups_all = (p.n + 7) / 8;
-        zero_words(p.out, p.L.off_a + 8 * groups_all, p.L.off_b);
-        zero_words(p.out, p.L.off_b + 4 * groups_all, p.L.off_c);
-        p.ws->m = m;
-    }
+    const uint32_t C = p.chunk;
     bool overflow = false;
-    if (total) {
-        uint32_t running = excl;
-        const uint64_t dbase = p.L.off_d + 3 * prefix;
-        for (uint32_t g = gbeg; g < gend; g++) {
-            uint32_t m8 = s_mask[g];
-            while (m8) {
-                const uint32_t b = __ffs(m8) - 1;
-                m8 &= m8 - 1;
-                const uint32_t el = 8 * g + b;
-                const uint32_t ci = el / p.chunk;
-                const uint32_t pos = el - ci * p.chunk;
-                const uint32_t cstart = s_cpref[ci];
-                const uint32_t k = s_cpref[ci + 1] - cstart;
-                const uint32_t rank = running - cstart;
-                const uint8_t e = (uint8_t)((p.in[ubase + el] >> 7) & 0xFF);
-                const uint64_t blk = dbase + 3ull * cstart;
-                put_byte(p, blk + 2ull * rank, (uint8_t)(pos & 0xFF), overflow);
-                put_byte(p, blk + 2ull * rank + 1, (uint8_t)(pos >> 8), overflow);
-                put_byte(p, blk + 2ull * k + rank, e, overflow);
-                running++;
+    const uint64_t stride = (uint64_t)gridDim.x * kWarps;
+    for (uint64_t r = (uint64_t)blockIdx.x * kWarps + warp; r < p.ranges; r += stride) {
+        const uint32_t c0 = (uint32_t)(r * p.range_chunks);
+        const uint32_t c1 = (uint32_t)min((uint64_t)c0 + p.range_chunks, p.L.nc);
+        const uint32_t nq = c1 - c0;
+        const uint32_t s = c0 * C;
+        const uint32_t e = (uint32_t)min((uint64_t)c1 * C, p.n);
+        const bool one_window = e - s <= kWinValues;
+        __syncwarp();  // the previous range's words are no longer read
+        // The first window's masks and the range's prefix are loaded together.
+        LaneSpan sp = load_lane_masks(p, s / 8, (min(s + kWinValues, e) - s + 7) / 8, sw);
+        const uint64_t pre = escapes_before(p, s_segpref, s);
+
+        // Pass 1: first escape rank (within the range) of every chunk. Chunk
+        // q starts at value s + q * C, a mask-byte boundary.
+        uint32_t base = 0, lexcl = 0;
+        for (uint32_t ws = s; ws < e; ws += kWinValues) {
+            const uint32_t we = min(ws + kWinValues, e);
+            if (ws != s) {
+                __syncwarp();  // the previous window's words are no longer read
+                sp = load_lane_masks(p, ws / 8, (we - ws + 7) / 8, sw);
             }
+            uint32_t cnt = 0;
+#pragma unroll
+            for (int k = 0; k < kLaneWords; k++) cnt += __popc(sw[k * 32 + lane]);
+            uint32_t incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            lexcl = incl - cnt;
+            // Chunk starts inside this lane's words, in value offsets from s
+            // (the lane's first word may begin up to 120 values before s).
+            const int32_t lv0 = 8 * (int32_t)sp.a_first - (int32_t)s;
+            const int32_t lv1 = lv0 + 32 * (int32_t)sp.nwords;
+            uint32_t q = lv0 <= 0 ? 0 : ((uint32_t)lv0 + C - 1) / C;
+            int32_t cs = (int32_t)(q * C);  // next chunk start
+            uint32_t running = base + lexcl;
+            for (int k = 0; k < (int)sp.nwords; k++) {
+                const uint32_t word = sw[k * 32 + lane];
+                const int32_t wv = lv0 + 32 * k;  // value offset of bit 0 of word k
+                while (q < nq && cs < wv + 32 && cs < lv1) {
+                    s_cp[q++] = running + __popc(word & ((1u << (cs - wv)) - 1));
+                    cs += (int32_t)C;
+                }
+                running += __popc(word);
+            }
+            base += __shfl_sync(0xffffffffu, incl, 31);
         }
+        const uint32_t rtotal = base;
+        if (lane == 0) s_cp[nq] = rtotal;
+        __syncwarp();
+
+        uint8_t* offs = p.out + p.L.off_c;
+        for (uint32_t q = lane; q < nq; q += 32)
+            *reinterpret_cast<uint32_t*>(offs + 4ull * (c0 + q)) = (uint32_t)(pre + s_cp[q]);
+        if (r == p.ranges - 1 && lane == 0) {
+            const uint64_t m = pre + rtotal;
+            *reinterpret_cast<uint32_t*>(offs + 4 * p.L.nc) = (uint32_t)m;
+            zero_words(p.out, p.L.off_c + 4 * (p.L.nc + 1), p.L.off_d);
+            const uint64_t groups_all = (p.n + 7) / 8;
+            zero_words(p.out, p.L.off_a + 8 * groups_all, p.L.off_b);
+            zero_words(p.out, p.L.off_b + 4 * groups_all, p.L.off_c);
+            p.ws->m = m;
+        }
+        if (rtotal == 0) {
+            __syncwarp();
+            continue;
+        }
+
+        // Pass 2: escapes, ascending, kBatch exponent re-reads in flight per
+        // lane. A single-window range still holds its masks in registers.
+        const uint64_t dbase = p.L.off_d + 3 * pre;
+        base = 0;
+        for (uint32_t ws = s; ws < e; ws += kWinValues) {
+            const uint32_t we = min(ws + kWinValues, e);
+            uint32_t wtotal = rtotal;
+            if (!one_window) {
+                __syncwarp();
+                sp = load_lane_masks(p, ws / 8, (we - ws + 7) / 8, sw);
+                uint32_t cnt = 0;
+#pragma unroll
+                for (int k = 0; k < kLaneWords; k++) cnt += __popc(sw[k * 32 + lane]);
+                uint32_t incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                lexcl = incl - cnt;
+                wtotal = __shfl_sync(0xffffffffu, incl, 31);
+            }
+            const int32_t lv0 = 8 * (int32_t)sp.a_first - (int32_t)s;
+            uint32_t running = base + lexcl;
+            uint32_t q = lv0 <= 0 ? 0 : (uint32_t)lv0 / C;  // chunk of the lane's first value
+            uint32_t next = (q + 1) * C;
+            const int kend = (int)sp.nwords;
+            int k = 0;
+            uint32_t bits = kend > 0 ? sw[lane] : 0;
+            for (;;) {
+                uint32_t el[kBatch], qq[kBatch], rk[kBatch];
+                int got = 0;
+                while (got < kBatch && k < kend) {
+                    if (bits == 0) {
+                        if (++k >= kend) break;
+                        bits = sw[k * 32 + lane];
+                        continue;
+                    }
+                    const uint32_t off = (uint32_t)(lv0 + 32 * k + (__ffs(bits) - 1));  // value offset in the range
+                    bits &= bits - 1;
+                    while (off >= next) {
+                        q++;
+                        next += C;
+                    }
+#pragma unroll
+                    for (int i = 0; i < kBatch; i++)
+                        if (i == got) {
+                            el[i] = s + off;
+                            qq[i] = q;
+                            rk[i] = running;
+                        }
+                    running++;
+                    got++;
+                }
+                if (got == 0) break;
+                uint32_t ex[kBatch];
+#pragma unroll
+                for (int i = 0; i < kBatch; i++) ex[i] = i < got ? (p.in[el[i]] >> 7) & 0xFF : 0;
+#pragma unroll
+                for (int i = 0; i < kBatch; i++) {
+                    if (i < got) {
+                        const uint32_t cstart = s_cp[qq[i]];
+                        const uint32_t kk = s_cp[qq[i] + 1] - cstart;
+                        const uint32_t rank = rk[i] - cstart;
+                        const uint32_t pos = el[i] - (c0 + qq[i]) * C;
+                        const uint64_t blk = dbase + 3ull * cstart;
+                        const uint64_t o_pos = blk + 2ull * rank, o_val = blk + 2ull * kk + rank;
+                        if (o_val < p.cap && o_pos + 1 < p.cap) {
+                            p.out[o_pos] = (uint8_t)(pos & 0xFF);
+                            p.out[o_pos + 1] = (uint8_t)(pos >> 8);
+                            p.out[o_val] = (uint8_t)ex[i];
+                        } else {
+                            overflow = true;
+                        }
+                    }
+                }
+            }
+            base += wtotal;
+        }
+        __syncwarp();  // s_cp is reused by this warp's next range
     }
     if (overflow) atomicOr(&p.ws->flags, UZIP_FLAG_CAPACITY);
 
-    // --------------------------------------------------------------- finish
+    // The last CTA to finish writes the header.
+    __threadfence();
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
         const unsigned prev = atomicAdd(&p.ws->done, 1u);
-        if (prev == (unsigned)(p.units - 1)) {
+        if (prev == gridDim.x - 1) {
             __threadfence();
             const uint64_t m = *reinterpret_cast<volatile unsigned long long*>(&p.ws->m);
             const uint32_t flags = *reinterpret_cast<volatile unsigned int*>(&p.ws->flags);
@@ -353,15 +515,14 @@ using namespace uzip;
 
 extern "C" UZIP_API size_t uzip_encode_workspace_bytes(size_t n, uint32_t chunk) {
     if (!chunk_valid(chunk) || n > UZIP_MAX_N) return 0;
-    const Geometry g = geometry_of(n, chunk);
-    return sizeof(Workspace) + 8 * (size_t)g.units;
+    return (size_t)geometry_of(n, chunk).bytes;
 }
 
 namespace uzip {
 
 int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_codebook, void* d_out,
                 size_t out_capacity, void* d_workspace, size_t workspace_bytes, size_t* h_out_bytes,
-                uzip_stream_t stream, uint64_t timeout_ns, uint32_t withhold_first) {
+                uzip_stream_t stream) {
     if (!chunk_valid(chunk)) return UZIP_ERR_CHUNK;
     if (n > UZIP_MAX_N || !d_out || !d_codebook || (n > 0 && !d_in_bf16) || !d_workspace) return UZIP_ERR_ARG;
     if (!aligned16(d_out) || !aligned16(d_codebook) || !aligned16(d_workspace) ||
@@ -369,33 +530,48 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         return UZIP_ERR_ALIGN;
     const Layout L = layout_of(n, chunk);
     if (out_capacity < L.off_d) return UZIP_ERR_CAPACITY;
-    const size_t ws_need = uzip_encode_workspace_bytes(n, chunk);
-    if (workspace_bytes < ws_need) return UZIP_ERR_CAPACITY;
+    const Geometry g = geometry_of(n, chunk);
+    if (workspace_bytes < g.bytes) return UZIP_ERR_CAPACITY;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const Geometry g = geometry_of(n, chunk);
+    uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     Params p;
     p.in = static_cast<const uint16_t*>(d_in_bf16);
     p.n = n;
     p.chunk = chunk;
-    p.unit_elems = g.unit_elems;
+    p.seg_units = g.seg_units;
+    p.nseg = g.nseg;
+    p.range_chunks = g.range_chunks;
     p.units = g.units;
+    p.ranges = g.ranges;
     p.cb = static_cast<const uint8_t*>(d_codebook);
     p.out = static_cast<uint8_t*>(d_out);
     p.cap = out_capacity;
     p.L = L;
-    p.ws = static_cast<Workspace*>(d_workspace);
-    p.desc = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(d_workspace) + sizeof(Workspace));
-    p.timeout_ns = timeout_ns;
-    p.withhold_first = withhold_first;
+    p.ws = reinterpret_cast<WsHeader*>(ws);
+    p.segs = reinterpret_cast<uint32_t*>(ws + g.off_segs);
+    p.counts = reinterpret_cast<uint32_t*>(ws + g.off_counts);
+    p.masks = ws + g.off_masks;
 
     if (n == 0) {
         encode_empty_kernel<<<1, 1, 0, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
     } else {
-        UZIP_CUDA_TRY(cudaMemsetAsync(d_workspace, 0, ws_need, s));
-        const size_t smem = pad16(g.unit_elems / 8) + 4 * (size_t)(g.chunks_per_unit + 1);
-        encode_kernel<<<(unsigned)g.units, kThreads, smem, s>>>(p);
+        int dev = 0, sms = 0, per_sm1 = 0, per_sm2 = 0;
+        UZIP_CUDA_TRY(cudaGetDevice(&dev));
+        UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        const size_t smem2 = 4 * ((size_t)kWarps * kLaneWords * 32 + ((size_t)g.nseg + 1 + 3) / 4 * 4 +
+                                  (size_t)kWarps * (g.range_chunks + 1));
+        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm1, encode_dense_kernel, kThreads, 0));
+        UZIP_CUDA_TRY(
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, encode_escape_kernel, kThreads, smem2));
+        if (per_sm1 < 1 || per_sm2 < 1) return UZIP_ERR_CUDA;
+        const uint64_t grid1 = std::min<uint64_t>((g.units + kWarps - 1) / kWarps, (uint64_t)sms * per_sm1);
+        const uint64_t grid2 = std::min<uint64_t>((g.ranges + kWarps - 1) / kWarps, (uint64_t)sms * per_sm2);
+        UZIP_CUDA_TRY(cudaMemsetAsync(ws, 0, g.off_counts, s));  // header + segment totals
+        encode_dense_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
+        UZIP_CUDA_TRY(cudaGetLastError());
+        encode_escape_kernel<<<(unsigned)grid2, kThreads, smem2, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
     }
     if (h_out_bytes) {
@@ -404,7 +580,6 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         UZIP_CUDA_TRY(cudaStreamSynchronize(s));
         *h_out_bytes = (size_t)hdr[12] | ((size_t)hdr[13] << 32);
         const uint32_t flags = hdr[1] >> 16;
-        if (flags & UZIP_FLAG_TIMEOUT) return UZIP_ERR_TIMEOUT;
         if (flags & UZIP_FLAG_CAPACITY) return UZIP_ERR_CAPACITY;
     }
     return UZIP_OK;
@@ -416,5 +591,5 @@ extern "C" UZIP_API int uzip_encode(const void* d_in_bf16, size_t n, uint32_t ch
                                     void* d_out, size_t out_capacity, void* d_workspace, size_t workspace_bytes,
                                     size_t* h_out_bytes, uzip_stream_t stream) {
     return encode_impl(d_in_bf16, n, chunk, d_codebook, d_out, out_capacity, d_workspace, workspace_bytes,
-                       h_out_bytes, stream, kDefaultTimeoutNs, 0);
+                       h_out_bytes, stream);
 }

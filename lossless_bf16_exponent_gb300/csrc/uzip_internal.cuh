@@ -82,10 +82,3 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
         if (_e != cudaSuccess) return UZIP_ERR_CUDA; \
     } while (0)
 
-namespace uzip {
-// Encoder entry shared by uzip_encode and uzip_encode_ex (encode.cu).
-int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_codebook, void* d_out,
-                size_t out_capacity, void* d_workspace, size_t workspace_bytes, size_t* h_out_bytes,
-                uzip_stream_t stream, uint64_t timeout_ns, uint32_t withhold_first);
-constexpr uint64_t kDefaultTimeoutNs = 1000000000ull;  // one second per look-back wait
-}  // namespace uzip

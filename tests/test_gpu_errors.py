@@ -1,7 +1,7 @@
 """Device-side error reporting, exercised without any GPU fault: every case
 below keeps all reads and writes inside the buffers (the kernels bound-check
-what a bad stream or a small buffer could push outside), every wait is
-bounded, and the CUDA context stays usable afterwards."""
+what a bad stream or a small buffer could push outside), no kernel waits on
+another block, and the CUDA context stays usable afterwards."""
 import numpy as np
 import pytest
 import torch
@@ -47,14 +47,17 @@ def test_capacity_overflow_is_flagged_and_bounded(uz):
     assert torch.all(y == 7)
 
 
-def test_lookback_timeout_is_reported_and_context_survives(uz):
-    x, s = _data(64 * 8192)
+def test_context_survives_a_flagged_encode(uz):
+    """After a device-side error the CUDA context stays usable."""
+    x, s = _data()
     cb = uz.calibrate(s)
-    with pytest.raises(_lib.UzipError) as e:
-        uz.encode(x, cb, 1024, timeout_ns=2_000_000, withhold_first_unit=True)
-    assert e.value.code == _lib.ERR_TIMEOUT
+    n = x.numel()
+    cap = uz.compressed_size(n, 0, 1024)
+    out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    with pytest.raises(_lib.UzipError):
+        uz.encode(x, cb, 1024, out=out)
     torch.cuda.synchronize()
-    assert uz.roundtrip_ok(x, cb, 1024)  # same process, same context: still fine
+    assert uz.roundtrip_ok(x, cb, 1024)
 
 
 def _good_stream(uz, n=200_000):
