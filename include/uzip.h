@@ -158,6 +158,26 @@ UZIP_API int uzip_encode(const void *d_in_bf16, size_t n, uint32_t chunk, const 
                          void *d_out, size_t out_capacity, void *d_workspace,
                          size_t workspace_bytes, size_t *h_out_bytes, uzip_stream_t stream);
 
+/* uzip_encode for callers that cannot allocate device memory for the
+ * workspace -- for example code that runs where a framework's caching
+ * allocator already holds the device memory, or latency-critical paths that
+ * must not call cudaMalloc, which can synchronise the device. The page has no
+ * counterpart: this is a library convenience, not part of the method.
+ *   The workspace is a device array built into the library, sized for at most
+ *   UZIP_NOALLOC_MAX_N values (about 8.1 MiB, held on every GPU that loads the
+ *   library until the process exits); n above that returns UZIP_ERR_CAPACITY
+ *   before any CUDA call. Nothing is allocated: the first call on a device
+ *   looks up the array's address with that device current (make that first
+ *   call before any stream capture). All calls share the one array; the call
+ *   clears what must start at zero, but calls that overlap on the GPU (other
+ *   streams, other host threads) race on it and corrupt each other's output,
+ *   so serialise them. Arguments, output and errors are otherwise those of
+ *   uzip_encode, and the stream is byte-identical to uzip_encode's. */
+#define UZIP_NOALLOC_MAX_N (1ull << 26)
+UZIP_API int uzip_encode_noalloc(const void *d_in_bf16, size_t n, uint32_t chunk, const void *d_codebook,
+                                 void *d_out, size_t out_capacity, size_t *h_out_bytes,
+                                 uzip_stream_t stream);
+
 /* Decode a stream produced by uzip_encode (§3.2): dense unpack and lookup,
  * then the escape fix-up, fused per tile so each output byte is written once.
  *   d_stream       stream_bytes bytes (at least the header's total).

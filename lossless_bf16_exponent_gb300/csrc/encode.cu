@@ -31,6 +31,7 @@
 //                  finish writes the 64-byte header.
 // The input is read from HBM once; the masks add N/8 bytes written and read.
 #include <algorithm>
+#include <atomic>
 
 #include "uzip_internal.cuh"
 
@@ -592,4 +593,61 @@ extern "C" UZIP_API int uzip_encode(const void* d_in_bf16, size_t n, uint32_t ch
                                     size_t* h_out_bytes, uzip_stream_t stream) {
     return encode_impl(d_in_bf16, n, chunk, d_codebook, d_out, out_capacity, d_workspace, workspace_bytes,
                        h_out_bytes, stream);
+}
+
+// ------------------------------------------------- encoding without allocation
+//
+// Some callers cannot allocate device memory for the encoder's workspace:
+// code running where a framework's caching allocator has already reserved the
+// device memory and hands out no raw buffers, or latency-critical paths that
+// must not call cudaMalloc (which can synchronise the device). For them the
+// workspace lives in a file-scope device array, fixed at load time: every GPU
+// that loads this library holds kNoAllocScratchBytes (about 8.1 MiB) of it
+// until the process exits. Host code cannot use the array's name as a device
+// address, so its address is looked up once per device with
+// cudaGetSymbolAddress (on the first call on that device, with the device
+// current) and passed to the same two kernels uzip_encode launches.
+
+namespace uzip {
+namespace {
+
+constexpr uint64_t cpad16(uint64_t v) { return (v + 15) / 16 * 16; }
+
+// Workspace bytes the encoder needs for n values (the geometry above, which
+// depends on n only).
+constexpr uint64_t workspace_bytes_for(uint64_t n) {
+    const uint64_t units = (n + kUnit - 1) / kUnit;
+    uint64_t seg_units = 64;
+    while ((units + seg_units - 1) / seg_units > kMaxSegments) seg_units *= 2;
+    const uint64_t nseg = (units + seg_units - 1) / seg_units;
+    return sizeof(WsHeader) + cpad16(4 * nseg) + cpad16(4 * units) + cpad16((n + 7) / 8);
+}
+
+constexpr uint64_t kNoAllocScratchBytes = workspace_bytes_for(UZIP_NOALLOC_MAX_N);
+
+constexpr int kMaxCachedDevices = 64;
+std::atomic<void*> g_scratch_addr[kMaxCachedDevices];
+
+}  // namespace
+}  // namespace uzip
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[uzip::kNoAllocScratchBytes];
+
+extern "C" UZIP_API int uzip_encode_noalloc(const void* d_in_bf16, size_t n, uint32_t chunk,
+                                            const void* d_codebook, void* d_out, size_t out_capacity,
+                                            size_t* h_out_bytes, uzip_stream_t stream) {
+    if (n > UZIP_NOALLOC_MAX_N) return UZIP_ERR_CAPACITY;  // beyond the built-in scratch
+    if (!chunk_valid(chunk)) return UZIP_ERR_CHUNK;
+    const uint64_t need = geometry_of(n, chunk).bytes;
+    if (need > kNoAllocScratchBytes) return UZIP_ERR_CAPACITY;
+    int dev = 0;
+    UZIP_CUDA_TRY(cudaGetDevice(&dev));
+    void* scratch = dev < kMaxCachedDevices ? g_scratch_addr[dev].load(std::memory_order_acquire) : nullptr;
+    if (!scratch) {
+        UZIP_CUDA_TRY(cudaGetSymbolAddress(&scratch, g_noalloc_scratch));
+        if (!scratch) return UZIP_ERR_CUDA;
+        if (dev < kMaxCachedDevices) g_scratch_addr[dev].store(scratch, std::memory_order_release);
+    }
+    return encode_impl(d_in_bf16, n, chunk, d_codebook, d_out, out_capacity, scratch, (size_t)need, h_out_bytes,
+                       stream);
 }

@@ -106,6 +106,12 @@ def test_encode_argument_validation(lib):
     assert enc(A16, 1000, 1024, A16, A16, cap, A16, ws - 1) == _lib.ERR_CAPACITY
 
 
+def test_noalloc_encode_rejects_oversize_before_any_cuda_call(lib):
+    n = _lib.NOALLOC_MAX_N
+    assert lib.uzip_encode_noalloc(A16, n + 1, 1024, A16, A16, 1 << 40, None, None) == _lib.ERR_CAPACITY
+    assert lib.uzip_encode_noalloc(A16, n, 12, A16, A16, 1 << 40, None, None) == _lib.ERR_CHUNK
+
+
 def test_decode_and_info_argument_validation(lib):
     assert lib.uzip_decode(None, 1000, A16, 10, None, None) == _lib.ERR_ARG
     assert lib.uzip_decode(A16, 1000, None, 10, None, None) == _lib.ERR_ARG
