@@ -173,7 +173,7 @@ UZIP_API int uzip_encode(const void *d_in_bf16, size_t n, uint32_t chunk, const 
  *   streams, other host threads) race on it and corrupt each other's output,
  *   so serialise them. Arguments, output and errors are otherwise those of
  *   uzip_encode, and the stream is byte-identical to uzip_encode's. */
-#define UZIP_NOALLOC_MAX_N (1ull << 26)
+#define UZIP_NOALLOC_MAX_N (1ull << 25)
 UZIP_API int uzip_encode_noalloc(const void *d_in_bf16, size_t n, uint32_t chunk, const void *d_codebook,
                                  void *d_out, size_t out_capacity, size_t *h_out_bytes,
                                  uzip_stream_t stream);

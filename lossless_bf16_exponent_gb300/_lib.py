@@ -22,7 +22,7 @@ EXPORTS = (
     "uzip_encode", "uzip_encode_noalloc", "uzip_decode", "uzip_stream_info", "uzip_status_string",
     "uzip_version",
 )
-NOALLOC_MAX_N = 1 << 26
+NOALLOC_MAX_N = 1 << 25
 
 
 class Info(ctypes.Structure):

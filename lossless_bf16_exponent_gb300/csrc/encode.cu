@@ -17,19 +17,21 @@
 //                  tickets, no barriers): 16-byte loads -> exponent and
 //                  sign-mantissa bytes with byte permutes -> code + escape bit
 //                  from a 256-byte shared table -> coalesced 8-byte
-//                  sign-mantissa and 4-byte code stores; one escape-mask byte
-//                  per group of eight values into the workspace (N/8 bytes),
-//                  the unit's escape count, and the count added to its
-//                  segment's total (64+ units per segment).
+//                  sign-mantissa and 4-byte code stores. Its escapes go, in
+//                  ascending order, into the unit's list of up to kListCap
+//                  (position, exponent) entries in the workspace; a unit with
+//                  more escapes stores its escape-mask bytes instead. It also
+//                  stores the unit's escape count and adds it to its segment's
+//                  total (64+ units per segment).
 //   escape kernel  every CTA scans the segment totals in shared memory; each
-//                  warp takes ranges of whole chunks, finds the range's first
-//                  escape rank from the segment prefix, unit counts and masks,
-//                  writes the chunk offsets, and writes each escape's
-//                  chunk-relative position and raw exponent (re-read from the
-//                  input, eight loads in flight per lane) in ascending element
-//                  order, bounds-checked against out_capacity. The last CTA to
-//                  finish writes the 64-byte header.
-// The input is read from HBM once; the masks add N/8 bytes written and read.
+//                  warp takes ranges of whole chunks (up to 32 units, one per
+//                  lane), finds the range's first escape rank from the segment
+//                  prefix and unit counts, writes the chunk offsets and then
+//                  each escape's chunk-relative position and raw exponent in
+//                  ascending element order, bounds-checked against
+//                  out_capacity. The last CTA to finish writes the header.
+// The input is read from HBM once; the escape lists cost about 4 bytes per
+// escape written and read.
 #include <algorithm>
 #include <atomic>
 
@@ -43,14 +45,19 @@ constexpr uint32_t kUnitGroups = kUnit / 8;   // its mask bytes
 constexpr int kThreads = 256;                 // both kernels
 constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kMaxSegments = 2048;       // segment totals one CTA scans
-constexpr uint32_t kRangeValues = 16384;      // target values per escape-kernel range
+constexpr uint32_t kListCap = 64;             // escape entries a unit keeps in its list
+constexpr uint32_t kMaxRangeUnits = 31;       // a range covers at most 31 units of values (32 overlapped)
+constexpr uint32_t kStageBytes = 4096;        // per-warp staging of a range's escape blocks
 constexpr uint32_t kMaxRangeChunks = 256;     // bounds the per-warp chunk table
-constexpr int kBatch = 8;                     // escape exponents re-read per lane at once
+constexpr int kBatch = 8;                     // escape exponents re-read at once (mask units)
 #ifndef UZIP_ENC_MIN_BLOCKS
 #define UZIP_ENC_MIN_BLOCKS 4
 #endif
 #ifndef UZIP_ENC_ITER_UNROLL
 #define UZIP_ENC_ITER_UNROLL 2
+#endif
+#ifndef UZIP_ESC_MIN_BLOCKS
+#define UZIP_ESC_MIN_BLOCKS 2
 #endif
 constexpr int kIterUnroll = UZIP_ENC_ITER_UNROLL;  // 2: both 4-load batches of a unit in flight per lane
 
@@ -67,9 +74,7 @@ struct Geometry {
     uint64_t units;         // counting units of kUnit values
     uint32_t seg_units;     // units per segment (power of two, >= 64)
     uint32_t nseg;          // segments
-    uint32_t range_chunks;  // chunks per escape-kernel range
-    uint64_t ranges;
-    uint64_t off_segs, off_counts, off_masks, bytes;  // workspace layout
+    uint64_t off_segs, off_counts, off_lists, off_masks, bytes;  // workspace layout
 };
 
 __host__ Geometry geometry_of(uint64_t n, uint32_t chunk) {
@@ -78,13 +83,11 @@ __host__ Geometry geometry_of(uint64_t n, uint32_t chunk) {
     g.seg_units = 64;
     while ((g.units + g.seg_units - 1) / g.seg_units > kMaxSegments) g.seg_units *= 2;
     g.nseg = (uint32_t)((g.units + g.seg_units - 1) / g.seg_units);
-    g.range_chunks = std::max<uint32_t>(1, std::min<uint32_t>(kRangeValues / chunk, kMaxRangeChunks));
-    const uint64_t nc = (n + chunk - 1) / chunk;
-    g.ranges = (nc + g.range_chunks - 1) / g.range_chunks;
     g.off_segs = sizeof(WsHeader);
     g.off_counts = g.off_segs + pad16(4ull * g.nseg);
-    g.off_masks = g.off_counts + pad16(4ull * g.units);
-    g.bytes = g.off_masks + pad16((n + 7) / 8);
+    g.off_lists = g.off_counts + pad16(4ull * g.units);
+    g.off_masks = g.off_lists + 4ull * kListCap * g.units;
+    g.bytes = g.off_masks + (uint64_t)kUnitGroups * g.units;
     return g;
 }
 
@@ -104,15 +107,17 @@ struct Params {
     WsHeader* ws;
     uint32_t* segs;
     uint32_t* counts;
-    uint8_t* masks;
+    uint32_t* lists;  // kListCap entries per unit: position | exponent << 16
+    uint8_t* masks;   // kUnitGroups bytes per unit, written only when a unit overflows its list
 };
 
 // Eight values -> 8 sign-mantissa bytes (a_lo, a_hi), 8 packed codes (one
-// word, value i in nibble i) and an 8-bit escape mask.
+// word, value i in nibble i), an 8-bit escape mask and the 8 exponents.
 __device__ __forceinline__ void encode_group(const uint4 v, const uint8_t* tab, uint32_t& a_lo,
-                                             uint32_t& a_hi, uint32_t& codes, uint32_t& mask) {
+                                             uint32_t& a_hi, uint32_t& codes, uint32_t& mask, uint32_t& e_lo,
+                                             uint32_t& e_hi) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t packed[2], esc[2], am[2];
+    uint32_t packed[2], esc[2], am[2], ex[2];
 #pragma unroll
     for (int h = 0; h < 2; h++) {
         // Bytes of four values: high bytes (sign + exponent bits 7..1) and
@@ -121,6 +126,7 @@ __device__ __forceinline__ void encode_group(const uint4 v, const uint8_t* tab, 
         const uint32_t lo = prmt(w[2 * h], w[2 * h + 1], 0x6420);
         const uint32_t e4 = ((hi << 1) & 0xFEFEFEFEu) | ((lo >> 7) & 0x01010101u);
         am[h] = (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
+        ex[h] = e4;
         // Table byte = code | escape << 7.
         const uint32_t t0 = tab[e4 & 0xFF];
         const uint32_t t1 = tab[(e4 >> 8) & 0xFF];
@@ -133,6 +139,8 @@ __device__ __forceinline__ void encode_group(const uint4 v, const uint8_t* tab, 
     }
     a_lo = am[0];
     a_hi = am[1];
+    e_lo = ex[0];
+    e_hi = ex[1];
     codes = prmt(packed[0], packed[1], 0x6420);
     // Bit 7 of byte i -> bit i (the four shifted copies never overlap).
     const uint32_t m_lo = (((esc[0] >> 7) * 0x204081u) >> 21) & 0xF;
@@ -173,8 +181,9 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
         const uint4* src = reinterpret_cast<const uint4*>(p.in + ubase);
         uint8_t* dst_a = p.out + p.L.off_a + ubase;
         uint8_t* dst_b = p.out + p.L.off_b + ubase / 2;
-        uint8_t* gmask = p.masks + u * kUnitGroups;
-        uint32_t cnt = 0;
+        uint32_t* list = p.lists + u * kListCap;
+        uint32_t cnt = 0;      // escapes so far in this unit (uniform across the warp)
+        uint32_t mbytes[2] = {0, 0};  // this lane's 8 mask bytes, in case the list overflows
 #pragma unroll kIterUnroll
         for (int it = 0; it < 2; it++) {
             uint4 v[4];
@@ -195,21 +204,47 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
 #pragma unroll
             for (int r = 0; r < 4; r++) {
                 const uint32_t g = it * 128 + r * 32 + lane;
-                if (8 * g >= ulen) continue;
-                uint32_t a_lo, a_hi, codes, mask;
-                encode_group(v[r], s_tab, a_lo, a_hi, codes, mask);
-                if (8 * g + 8 > ulen) {  // codes and escapes of real values only
-                    const uint32_t valid = ulen - 8 * g;
-                    mask &= (1u << valid) - 1;
-                    codes &= (1u << (4 * valid)) - 1;
+                uint32_t mask = 0, e_lo = 0, e_hi = 0;
+                if (8 * g < ulen) {
+                    uint32_t a_lo, a_hi, codes;
+                    encode_group(v[r], s_tab, a_lo, a_hi, codes, mask, e_lo, e_hi);
+                    if (8 * g + 8 > ulen) {  // codes and escapes of real values only
+                        const uint32_t valid = ulen - 8 * g;
+                        mask &= (1u << valid) - 1;
+                        codes &= (1u << (4 * valid)) - 1;
+                    }
+                    *reinterpret_cast<uint2*>(dst_a + 8 * g) = make_uint2(a_lo, a_hi);
+                    *reinterpret_cast<uint32_t*>(dst_b + 4 * g) = codes;
                 }
-                *reinterpret_cast<uint2*>(dst_a + 8 * g) = make_uint2(a_lo, a_hi);
-                *reinterpret_cast<uint32_t*>(dst_b + 4 * g) = codes;
-                gmask[g] = (uint8_t)mask;
-                cnt += __popc(mask);
+                // Groups g = it*128 + r*32 + lane come in ascending order per
+                // (it, r) row, so a warp scan ranks the row's escapes (the
+                // whole warp takes part, tail lanes with an empty mask).
+                if (__any_sync(0xffffffffu, mask != 0)) {
+                    const uint32_t c = __popc(mask);
+                    uint32_t incl = c;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    uint32_t j = cnt + incl - c;
+                    for (uint32_t bits = mask; bits; bits &= bits - 1, j++) {
+                        const uint32_t b = __ffs(bits) - 1;
+                        const uint32_t e = ((b < 4 ? e_lo : e_hi) >> (8 * (b & 3))) & 0xFF;
+                        if (j < kListCap) list[j] = (8 * g + b) | (e << 16);
+                    }
+                    cnt += __shfl_sync(0xffffffffu, incl, 31);
+                }
+                mbytes[it] |= mask << (8 * r);
             }
         }
-        cnt = warp_sum(cnt);
+        if (cnt > kListCap) {  // the list overflowed: keep the masks instead
+            uint8_t* gmask = p.masks + u * kUnitGroups;
+#pragma unroll
+            for (int it = 0; it < 2; it++)
+#pragma unroll
+                for (int r = 0; r < 4; r++) gmask[it * 128 + r * 32 + lane] = (uint8_t)(mbytes[it] >> (8 * r));
+        }
         if (lane == 0) {
             p.counts[u] = cnt;
             if (cnt) atomicAdd(&p.segs[u / p.seg_units], cnt);
@@ -219,86 +254,103 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
 
 // ----------------------------------------------------------- escape kernel
 
-// Escapes before value s (s a multiple of 8): the segment prefix, the counts
-// of the earlier units of its segment, the mask bytes of its own unit. A
-// segment holds at most 64 units at this size, so each lane loads at most two
-// counts and eight mask bytes, all at once.
-__device__ uint64_t escapes_before(const Params& p, const uint32_t* s_segpref, uint32_t s) {
-    const uint32_t lane = threadIdx.x & 31;
-    const uint32_t us = s / kUnit;
-    const uint32_t seg = us / p.seg_units;
-    uint32_t part = 0;
-    uint32_t i = seg * p.seg_units + lane;
-    for (; i + 32 < us; i += 64) part += p.counts[i] + p.counts[i + 32];
-    if (i < us) part += p.counts[i];
-    const uint32_t bend = s / 8;
-    uint32_t b = us * kUnitGroups + lane;
-    uint32_t m[8];
-#pragma unroll
-    for (int j = 0; j < 8; j++) m[j] = (b + 32 * j < bend) ? p.masks[b + 32 * j] : 0;
-#pragma unroll
-    for (int j = 0; j < 8; j++) part += __popc(m[j]);
-    return (uint64_t)s_segpref[seg] + warp_sum(part);
-}
-
-constexpr uint32_t kWinValues = 16384;  // values per mask window (2 KiB of mask bytes)
-constexpr int kVecPerLane = 5;           // 16-byte mask vectors per lane per window (128 + 2 slack)
-
-// One lane's share of a window of mask bytes: the 16-byte vectors [v0, v1) of
-// the aligned span around the window's bytes, bytes outside the window
-// cleared, kept in shared memory transposed (word k of lane l at
-// sw[k * 32 + l]) so a warp touching word k of every lane hits 32 different
-// banks. Bit i of word k stands for value 8 * (a_first + 4 * k) + i.
-constexpr int kLaneWords = kVecPerLane * 4;
-
-struct LaneSpan {
-    uint32_t a_first;  // byte address of the lane's word 0 in the mask section
-    uint32_t nwords;   // words the lane holds (<= kLaneWords)
+// One lane's view of unit u's escapes at unit positions [plo, phi): from the
+// unit's sorted list, or (a unit that overflowed its list) from its mask bytes
+// with exponents re-read from the input.
+struct UnitPart {
+    uint64_t ubase;  // first value of the unit
+    uint32_t cnt;    // all escapes of the unit
+    uint32_t plo, phi;
+    bool list;
+    const uint32_t* entries;
+    const uint32_t* mwords;  // 64 mask words: bit i of word w = unit position 32 w + i
 };
 
-__device__ __forceinline__ LaneSpan load_lane_masks(const Params& p, uint32_t b0, uint32_t nb, uint32_t* sw) {
-    const uint32_t lane = threadIdx.x & 31;
-    const uint32_t a0 = b0 & ~15u;
-    const uint32_t nvec = (b0 + nb - a0 + 15) / 16;
-    const uint32_t vpl = (nvec + 31) / 32;
-    const uint32_t v0 = min(lane * vpl, nvec), v1 = min(v0 + vpl, nvec);
-    LaneSpan sp;
-    sp.a_first = a0 + 16 * v0;
-    sp.nwords = 4 * (v1 - v0);
-    const uint4* src = reinterpret_cast<const uint4*>(p.masks + a0);
-    uint4 v[kVecPerLane];
-#pragma unroll
-    for (int j = 0; j < kVecPerLane; j++) v[j] = (v0 + j < v1) ? src[v0 + j] : make_uint4(0, 0, 0, 0);
-    const uint32_t lo = b0, hi = b0 + nb;  // the window's bytes
-#pragma unroll
-    for (int j = 0; j < kVecPerLane; j++) {
-        uint32_t vw[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-        const uint32_t a = sp.a_first + 16 * j;
-        if (a < lo || a + 16 > hi) {  // an edge vector: clear bytes outside the window
-#pragma unroll
-            for (int k = 0; k < 4; k++) {
-                const uint32_t wa = a + 4 * k;
-                const uint32_t from = lo > wa ? min(lo - wa, 4u) : 0u;  // first kept byte
-                const uint32_t to = hi > wa ? min(hi - wa, 4u) : 0u;     // one past the last
-                const uint32_t upto = to >= 4 ? 0xFFFFFFFFu : (1u << (8 * to)) - 1;
-                const uint32_t below = from >= 4 ? 0xFFFFFFFFu : (1u << (8 * from)) - 1;
-                vw[k] &= upto & ~below;
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 4; k++) sw[(4 * j + k) * 32 + lane] = vw[k];
-    }
-    return sp;
+// Bits of mask word w (unit positions 32 w ..) that lie in [lo, hi).
+__device__ __forceinline__ uint32_t bits_in(uint32_t word, uint32_t w, uint32_t lo, uint32_t hi) {
+    const uint32_t b0 = 32 * w;
+    const uint32_t keep_hi = hi >= b0 + 32 ? 0xFFFFFFFFu : (hi <= b0 ? 0u : (1u << (hi - b0)) - 1);
+    const uint32_t drop_lo = lo >= b0 + 32 ? 0xFFFFFFFFu : (lo <= b0 ? 0u : (1u << (lo - b0)) - 1);
+    return word & keep_hi & ~drop_lo;
 }
 
-__global__ void __launch_bounds__(kThreads, 3) encode_escape_kernel(const Params p) {
+// Escapes of a list unit below plo and inside [plo, phi), from its sorted
+// list (head = its first four entries, already loaded).
+__device__ __forceinline__ void count_part(const UnitPart& up, const uint4 head, uint32_t& n_lo, uint32_t& n_in) {
+    n_lo = 0;
+    n_in = 0;
+    for (uint32_t i = 0; i < up.cnt; i += 4) {
+        const uint4 q4 = i == 0 ? head : __ldg(reinterpret_cast<const uint4*>(up.entries + i));
+        const uint32_t qs[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+        for (int t = 0; t < 4; t++) {
+            if (i + t < up.cnt) {
+                const uint32_t pos = qs[t] & 0xFFFF;
+                n_lo += pos < up.plo;
+                n_in += pos >= up.plo && pos < up.phi;
+            }
+        }
+    }
+}
+
+// A range's loads, issued together before any of them is used: the counts
+// and first four list entries of its units (two rounds of one unit per lane)
+// and the counts of the earlier units of its first unit's segment.
+constexpr int kPreLoads = 8;   // earlier-unit counts per lane (segments of up to 256 units)
+
+// kRounds = 1 when every range overlaps at most 32 units (one per lane); 2 for
+// the chunk sizes whose single chunk can overlap 33 units (longer than
+// 32 * 2048 - 2040 values and not a multiple of 2048).
+template <int kRounds>
+struct RangeLoads {
+    uint32_t c0, nq, s, e, u0, nu, seg;
+    uint32_t cnt[kRounds];
+    uint4 head[kRounds];
+    uint32_t pre_cnt[kPreLoads];
+};
+
+template <int kRounds>
+__device__ __forceinline__ void load_range(const Params& p, uint64_t r, RangeLoads<kRounds>& rl) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t C = p.chunk;
+    rl.c0 = (uint32_t)(r * p.range_chunks);
+    const uint32_t c1 = (uint32_t)min((uint64_t)rl.c0 + p.range_chunks, p.L.nc);
+    rl.nq = c1 - rl.c0;
+    rl.s = rl.c0 * C;  // n < 2^32
+    rl.e = (uint32_t)min((uint64_t)c1 * C, p.n);
+    rl.u0 = rl.s / kUnit;
+    rl.nu = (rl.e - 1) / kUnit - rl.u0 + 1;
+    rl.seg = rl.u0 / p.seg_units;
+#pragma unroll
+    for (int rr = 0; rr < kRounds; rr++) {
+        const uint32_t u = rl.u0 + 32 * rr + lane;
+        const bool on = 32 * rr + lane < rl.nu;
+        rl.cnt[rr] = on ? __ldg(p.counts + u) : 0;
+        rl.head[rr] = on ? __ldg(reinterpret_cast<const uint4*>(p.lists + (uint64_t)u * kListCap))
+                         : make_uint4(0, 0, 0, 0);
+    }
+    const uint32_t first = rl.seg * p.seg_units;
+#pragma unroll
+    for (int j = 0; j < kPreLoads; j++) {
+        const uint32_t i = first + 32 * j + lane;
+        rl.pre_cnt[j] = i < rl.u0 ? __ldg(p.counts + i) : 0;
+    }
+}
+
+template <int kRounds>
+__global__ void __launch_bounds__(kThreads, UZIP_ESC_MIN_BLOCKS) encode_escape_kernel(const Params p) {
     extern __shared__ __align__(16) uint32_t s_dyn[];
     __shared__ uint32_t s_warp[kWarps];
     const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // Layout: per-warp mask words | segment prefix (nseg + 1) | per-warp chunk tables.
-    uint32_t* sw = s_dyn + warp * (kLaneWords * 32);
-    uint32_t* s_segpref = s_dyn + kWarps * kLaneWords * 32;
+    // Layout: per-warp escape staging | segment prefixes (nseg + 1) | per-warp chunk tables.
+    uint8_t* stage = reinterpret_cast<uint8_t*>(s_dyn) + warp * kStageBytes;
+    uint32_t* s_segpref = s_dyn + kWarps * kStageBytes / 4;
     uint32_t* s_cp = s_segpref + ((p.nseg + 1 + 3) & ~3u) + warp * (p.range_chunks + 1);
+
+    const uint64_t stride = (uint64_t)gridDim.x * kWarps;
+    uint64_t r = (uint64_t)blockIdx.x * kWarps + warp;
+    RangeLoads<kRounds> rl;
+    if (r < p.ranges) load_range(p, r, rl);  // in flight during the segment scan below
 
     // Segment prefix, one block scan (kMaxSegments / kThreads = 8 totals per
     // thread, loaded together).
@@ -334,57 +386,122 @@ __global__ void __launch_bounds__(kThreads, 3) encode_escape_kernel(const Params
 
     const uint32_t C = p.chunk;
     bool overflow = false;
-    const uint64_t stride = (uint64_t)gridDim.x * kWarps;
-    for (uint64_t r = (uint64_t)blockIdx.x * kWarps + warp; r < p.ranges; r += stride) {
-        const uint32_t c0 = (uint32_t)(r * p.range_chunks);
-        const uint32_t c1 = (uint32_t)min((uint64_t)c0 + p.range_chunks, p.L.nc);
-        const uint32_t nq = c1 - c0;
-        const uint32_t s = c0 * C;
-        const uint32_t e = (uint32_t)min((uint64_t)c1 * C, p.n);
-        const bool one_window = e - s <= kWinValues;
-        __syncwarp();  // the previous range's words are no longer read
-        // The first window's masks and the range's prefix are loaded together.
-        LaneSpan sp = load_lane_masks(p, s / 8, (min(s + kWinValues, e) - s + 7) / 8, sw);
-        const uint64_t pre = escapes_before(p, s_segpref, s);
-
-        // Pass 1: first escape rank (within the range) of every chunk. Chunk
-        // q starts at value s + q * C, a mask-byte boundary.
-        uint32_t base = 0, lexcl = 0;
-        for (uint32_t ws = s; ws < e; ws += kWinValues) {
-            const uint32_t we = min(ws + kWinValues, e);
-            if (ws != s) {
-                __syncwarp();  // the previous window's words are no longer read
-                sp = load_lane_masks(p, ws / 8, (we - ws + 7) / 8, sw);
-            }
-            uint32_t cnt = 0;
+    for (; r < p.ranges; r += stride) {
+        const uint32_t c0 = rl.c0, nq = rl.nq, s = rl.s, e = rl.e, u0 = rl.u0, nu = rl.nu, seg = rl.seg;
+        UnitPart up[kRounds];
+        uint32_t n_lo[kRounds], n_in[kRounds];
 #pragma unroll
-            for (int k = 0; k < kLaneWords; k++) cnt += __popc(sw[k * 32 + lane]);
-            uint32_t incl = cnt;
+        for (int rr = 0; rr < kRounds; rr++) {
+            n_lo[rr] = n_in[rr] = 0;
+            up[rr].list = true;
+            if (32 * rr + lane < nu) {
+                UnitPart& u = up[rr];
+                u.ubase = (uint64_t)(u0 + 32 * rr + lane) * kUnit;
+                u.cnt = rl.cnt[rr];
+                u.plo = s > u.ubase ? (uint32_t)(s - u.ubase) : 0u;
+                u.phi = (uint32_t)min((uint64_t)kUnit, (uint64_t)e - u.ubase);
+                u.list = u.cnt <= kListCap;
+                u.entries = p.lists + (u.ubase / kUnit) * kListCap;
+                u.mwords = reinterpret_cast<const uint32_t*>(p.masks + (u.ubase / kUnit) * kUnitGroups);
+                if (u.list) count_part(u, rl.head[rr], n_lo[rr], n_in[rr]);
+            }
+        }
+        // Units that overflowed their list are handled by the whole warp: lane
+        // l takes mask words 2l and 2l+1 (unit positions 64l .. 64l+63).
+        auto coop = [&](int rr, int o, uint64_t& ub, uint32_t& plo, uint32_t& phi, uint32_t& b0, uint32_t& b1) {
+            ub = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(up[rr].ubase >> 32), o) << 32) |
+                 __shfl_sync(0xffffffffu, (uint32_t)up[rr].ubase, o);
+            plo = __shfl_sync(0xffffffffu, up[rr].plo, o);
+            phi = __shfl_sync(0xffffffffu, up[rr].phi, o);
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.masks + (ub / kUnit) * kUnitGroups) + lane);
+            b0 = bits_in(w.x, 2 * lane, plo, phi);
+            b1 = bits_in(w.y, 2 * lane + 1, plo, phi);
+            return w;
+        };
+#pragma unroll
+        for (int rr = 0; rr < kRounds; rr++) {
+            for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
+                const int o = __ffs(ovf) - 1;
+                uint64_t ub;
+                uint32_t plo, phi, b0, b1;
+                const uint2 w = coop(rr, o, ub, plo, phi, b0, b1);
+                const uint32_t lo = warp_sum(__popc(bits_in(w.x, 2 * lane, 0, plo)) +
+                                             __popc(bits_in(w.y, 2 * lane + 1, 0, plo)));
+                const uint32_t in = warp_sum(__popc(b0) + __popc(b1));
+                if (lane == (uint32_t)o) {
+                    n_lo[rr] = lo;
+                    n_in[rr] = in;
+                }
+            }
+        }
+        // Escapes before s: segment prefix + earlier units of the segment +
+        // unit u0's escapes before s.
+        uint32_t part = 0;
+#pragma unroll
+        for (int j = 0; j < kPreLoads; j++) part += rl.pre_cnt[j];
+        for (uint32_t i = seg * p.seg_units + 32 * kPreLoads + lane; i < u0; i += 32) part += __ldg(p.counts + i);
+        uint64_t pre = (uint64_t)s_segpref[seg] + warp_sum(part) + __shfl_sync(0xffffffffu, n_lo[0], 0);
+
+        // Pass 1: running rank of each unit's first in-range escape, and every
+        // chunk's first rank. Chunk q starts at value s + q * C.
+        __syncwarp();  // the previous range's chunk table is no longer read
+        uint32_t first[kRounds];
+        uint32_t carry = 0;
+#pragma unroll
+        for (int rr = 0; rr < kRounds; rr++) {
+            uint32_t incl = n_in[rr];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += t;
             }
-            lexcl = incl - cnt;
-            // Chunk starts inside this lane's words, in value offsets from s
-            // (the lane's first word may begin up to 120 values before s).
-            const int32_t lv0 = 8 * (int32_t)sp.a_first - (int32_t)s;
-            const int32_t lv1 = lv0 + 32 * (int32_t)sp.nwords;
-            uint32_t q = lv0 <= 0 ? 0 : ((uint32_t)lv0 + C - 1) / C;
-            int32_t cs = (int32_t)(q * C);  // next chunk start
-            uint32_t running = base + lexcl;
-            for (int k = 0; k < (int)sp.nwords; k++) {
-                const uint32_t word = sw[k * 32 + lane];
-                const int32_t wv = lv0 + 32 * k;  // value offset of bit 0 of word k
-                while (q < nq && cs < wv + 32 && cs < lv1) {
-                    s_cp[q++] = running + __popc(word & ((1u << (cs - wv)) - 1));
-                    cs += (int32_t)C;
+            first[rr] = carry + incl - n_in[rr];
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+            if (32 * rr + lane < nu && up[rr].list) {
+                const UnitPart& u = up[rr];
+                const uint32_t v_lo = (uint32_t)(u.ubase + u.plo) - s;  // range offset of plo
+                uint32_t q = (v_lo + C - 1) / C;
+                uint32_t x = (uint32_t)(s + q * C - u.ubase);  // unit position of chunk q's start
+                uint32_t i = n_lo[rr];
+                const uint32_t iend = n_lo[rr] + n_in[rr];
+                while (q < nq && x < u.phi) {
+                    while (i < iend && (__ldg(u.entries + i) & 0xFFFF) < x) i++;
+                    s_cp[q] = first[rr] + (i - n_lo[rr]);
+                    q++;
+                    x += C;
                 }
-                running += __popc(word);
             }
-            base += __shfl_sync(0xffffffffu, incl, 31);
+            for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
+                const int o = __ffs(ovf) - 1;
+                uint64_t ub;
+                uint32_t plo, phi, b0, b1;
+                coop(rr, o, ub, plo, phi, b0, b1);
+                const uint32_t f = __shfl_sync(0xffffffffu, first[rr], o);
+                const uint32_t c = __popc(b0) + __popc(b1);
+                uint32_t ic = c;
+#pragma unroll
+                for (int k = 1; k < 32; k <<= 1) {
+                    const uint32_t t = __shfl_up_sync(0xffffffffu, ic, k);
+                    if (lane >= k) ic += t;
+                }
+                const uint32_t before = f + ic - c;  // rank of this lane's first escape
+                const uint32_t lo = max(64 * lane, plo), hi = min(64 * lane + 64, phi);
+                if (lo < hi) {
+                    const uint32_t v_lo = (uint32_t)(ub + lo) - s;
+                    uint32_t q = (v_lo + C - 1) / C;
+                    uint32_t x = (uint32_t)(s + q * C - ub);
+                    while (q < nq && x < hi) {
+                        const uint32_t d = x - 64 * lane;  // 0..63
+                        const uint32_t below = d < 32 ? __popc(b0 & ((1u << d) - 1))
+                                                      : __popc(b0) + __popc(b1 & ((1u << (d - 32)) - 1));
+                        s_cp[q] = before + below;
+                        q++;
+                        x += C;
+                    }
+                }
+            }
         }
-        const uint32_t rtotal = base;
+        const uint32_t rtotal = carry;
         if (lane == 0) s_cp[nq] = rtotal;
         __syncwarp();
 
@@ -400,91 +517,98 @@ __global__ void __launch_bounds__(kThreads, 3) encode_escape_kernel(const Params
             zero_words(p.out, p.L.off_b + 4 * groups_all, p.L.off_c);
             p.ws->m = m;
         }
-        if (rtotal == 0) {
-            __syncwarp();
-            continue;
-        }
-
-        // Pass 2: escapes, ascending, kBatch exponent re-reads in flight per
-        // lane. A single-window range still holds its masks in registers.
-        const uint64_t dbase = p.L.off_d + 3 * pre;
-        base = 0;
-        for (uint32_t ws = s; ws < e; ws += kWinValues) {
-            const uint32_t we = min(ws + kWinValues, e);
-            uint32_t wtotal = rtotal;
-            if (!one_window) {
+        if (rtotal != 0) {
+            // Pass 2: each escape's chunk-relative position and raw exponent.
+            // The range's escape blocks are contiguous in the stream: assemble
+            // them in this warp's stage and copy them out with coalesced
+            // stores, unless there are too many, then store them directly.
+            const uint64_t dbase = p.L.off_d + 3 * pre;
+            const uint32_t dbytes = 3 * rtotal;
+            const bool staged = dbytes <= kStageBytes;
+            auto put = [&](uint32_t off, uint32_t rank_in_range, uint32_t q, uint32_t expo) {
+                const uint32_t cstart = s_cp[q];
+                const uint32_t k = s_cp[q + 1] - cstart;
+                const uint32_t rank = rank_in_range - cstart;
+                const uint32_t pos = off - q * C;
+                const uint32_t rel_pos = 3 * cstart + 2 * rank, rel_val = 3 * cstart + 2 * k + rank;
+                if (staged) {
+                    stage[rel_pos] = (uint8_t)(pos & 0xFF);
+                    stage[rel_pos + 1] = (uint8_t)(pos >> 8);
+                    stage[rel_val] = (uint8_t)expo;
+                } else if (dbase + rel_val < p.cap && dbase + rel_pos + 1 < p.cap) {
+                    p.out[dbase + rel_pos] = (uint8_t)(pos & 0xFF);
+                    p.out[dbase + rel_pos + 1] = (uint8_t)(pos >> 8);
+                    p.out[dbase + rel_val] = (uint8_t)expo;
+                } else {
+                    overflow = true;
+                }
+            };
+#pragma unroll
+            for (int rr = 0; rr < kRounds; rr++) {
+                if (32 * rr + lane < nu && up[rr].list && n_in[rr]) {
+                    const UnitPart& u = up[rr];
+                    uint32_t running = first[rr];
+                    uint32_t q = ((uint32_t)(u.ubase + u.plo) - s) / C;  // chunk of the part's first value
+                    uint32_t next = (q + 1) * C;
+                    for (uint32_t i = n_lo[rr]; i < n_lo[rr] + n_in[rr]; i++) {
+                        const uint32_t ent = __ldg(u.entries + i);
+                        const uint32_t off = (uint32_t)(u.ubase + (ent & 0xFFFF)) - s;
+                        while (off >= next) {
+                            q++;
+                            next += C;
+                        }
+                        put(off, running++, q, ent >> 16);
+                    }
+                }
+                for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
+                    const int o = __ffs(ovf) - 1;
+                    uint64_t ub;
+                    uint32_t plo, phi, b0, b1;
+                    coop(rr, o, ub, plo, phi, b0, b1);
+                    const uint32_t f = __shfl_sync(0xffffffffu, first[rr], o);
+                    const uint32_t c = __popc(b0) + __popc(b1);
+                    uint32_t ic = c;
+#pragma unroll
+                    for (int k = 1; k < 32; k <<= 1) {
+                        const uint32_t t = __shfl_up_sync(0xffffffffu, ic, k);
+                        if (lane >= k) ic += t;
+                    }
+                    uint32_t running = f + ic - c;
+                    // this lane's escapes, exponents re-read kBatch at a time
+                    while (b0 | b1) {
+                        uint32_t offs_b[kBatch], ex[kBatch];
+                        int got = 0;
+#pragma unroll
+                        for (int t = 0; t < kBatch; t++) {
+                            offs_b[t] = 0;
+                            if (b0 | b1) {
+                                const bool lo_word = b0 != 0;
+                                const uint32_t bits = lo_word ? b0 : b1;
+                                const uint32_t pos = 64 * lane + (lo_word ? 0 : 32) + (__ffs(bits) - 1);
+                                if (lo_word) b0 &= b0 - 1;
+                                else b1 &= b1 - 1;
+                                offs_b[t] = (uint32_t)(ub + pos) - s;
+                                got = t + 1;
+                            }
+                        }
+#pragma unroll
+                        for (int t = 0; t < kBatch; t++) ex[t] = t < got ? (__ldg(p.in + s + offs_b[t]) >> 7) & 0xFF : 0;
+#pragma unroll
+                        for (int t = 0; t < kBatch; t++)
+                            if (t < got) put(offs_b[t], running++, offs_b[t] / C, ex[t]);
+                    }
+                }
+            }
+            if (staged) {
                 __syncwarp();
-                sp = load_lane_masks(p, ws / 8, (we - ws + 7) / 8, sw);
-                uint32_t cnt = 0;
-#pragma unroll
-                for (int k = 0; k < kLaneWords; k++) cnt += __popc(sw[k * 32 + lane]);
-                uint32_t incl = cnt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += t;
+                for (uint32_t b = lane; b < dbytes; b += 32) {
+                    if (dbase + b < p.cap) p.out[dbase + b] = stage[b];
+                    else overflow = true;
                 }
-                lexcl = incl - cnt;
-                wtotal = __shfl_sync(0xffffffffu, incl, 31);
+                __syncwarp();  // the stage is reused by the next range
             }
-            const int32_t lv0 = 8 * (int32_t)sp.a_first - (int32_t)s;
-            uint32_t running = base + lexcl;
-            uint32_t q = lv0 <= 0 ? 0 : (uint32_t)lv0 / C;  // chunk of the lane's first value
-            uint32_t next = (q + 1) * C;
-            const int kend = (int)sp.nwords;
-            int k = 0;
-            uint32_t bits = kend > 0 ? sw[lane] : 0;
-            for (;;) {
-                uint32_t el[kBatch], qq[kBatch], rk[kBatch];
-                int got = 0;
-                while (got < kBatch && k < kend) {
-                    if (bits == 0) {
-                        if (++k >= kend) break;
-                        bits = sw[k * 32 + lane];
-                        continue;
-                    }
-                    const uint32_t off = (uint32_t)(lv0 + 32 * k + (__ffs(bits) - 1));  // value offset in the range
-                    bits &= bits - 1;
-                    while (off >= next) {
-                        q++;
-                        next += C;
-                    }
-#pragma unroll
-                    for (int i = 0; i < kBatch; i++)
-                        if (i == got) {
-                            el[i] = s + off;
-                            qq[i] = q;
-                            rk[i] = running;
-                        }
-                    running++;
-                    got++;
-                }
-                if (got == 0) break;
-                uint32_t ex[kBatch];
-#pragma unroll
-                for (int i = 0; i < kBatch; i++) ex[i] = i < got ? (p.in[el[i]] >> 7) & 0xFF : 0;
-#pragma unroll
-                for (int i = 0; i < kBatch; i++) {
-                    if (i < got) {
-                        const uint32_t cstart = s_cp[qq[i]];
-                        const uint32_t kk = s_cp[qq[i] + 1] - cstart;
-                        const uint32_t rank = rk[i] - cstart;
-                        const uint32_t pos = el[i] - (c0 + qq[i]) * C;
-                        const uint64_t blk = dbase + 3ull * cstart;
-                        const uint64_t o_pos = blk + 2ull * rank, o_val = blk + 2ull * kk + rank;
-                        if (o_val < p.cap && o_pos + 1 < p.cap) {
-                            p.out[o_pos] = (uint8_t)(pos & 0xFF);
-                            p.out[o_pos + 1] = (uint8_t)(pos >> 8);
-                            p.out[o_val] = (uint8_t)ex[i];
-                        } else {
-                            overflow = true;
-                        }
-                    }
-                }
-            }
-            base += wtotal;
         }
-        __syncwarp();  // s_cp is reused by this warp's next range
+        if (r + stride < p.ranges) load_range(p, r + stride, rl);
     }
     if (overflow) atomicOr(&p.ws->flags, UZIP_FLAG_CAPACITY);
 
@@ -542,9 +666,7 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
     p.chunk = chunk;
     p.seg_units = g.seg_units;
     p.nseg = g.nseg;
-    p.range_chunks = g.range_chunks;
     p.units = g.units;
-    p.ranges = g.ranges;
     p.cb = static_cast<const uint8_t*>(d_codebook);
     p.out = static_cast<uint8_t*>(d_out);
     p.cap = out_capacity;
@@ -552,6 +674,7 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
     p.ws = reinterpret_cast<WsHeader*>(ws);
     p.segs = reinterpret_cast<uint32_t*>(ws + g.off_segs);
     p.counts = reinterpret_cast<uint32_t*>(ws + g.off_counts);
+    p.lists = reinterpret_cast<uint32_t*>(ws + g.off_lists);
     p.masks = ws + g.off_masks;
 
     if (n == 0) {
@@ -561,18 +684,30 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         int dev = 0, sms = 0, per_sm1 = 0, per_sm2 = 0;
         UZIP_CUDA_TRY(cudaGetDevice(&dev));
         UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        const size_t smem2 = 4 * ((size_t)kWarps * kLaneWords * 32 + ((size_t)g.nseg + 1 + 3) / 4 * 4 +
-                                  (size_t)kWarps * (g.range_chunks + 1));
+        const size_t smem2_max = (size_t)kWarps * kStageBytes +
+                                 4 * (((size_t)g.nseg + 1 + 3) / 4 * 4 + (size_t)kWarps * (kMaxRangeChunks + 1));
         UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm1, encode_dense_kernel, kThreads, 0));
-        UZIP_CUDA_TRY(
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, encode_escape_kernel, kThreads, smem2));
+        const bool two_rounds = chunk > 32 * kUnit - 2040 && chunk % kUnit != 0;
+        auto* esc_kernel = two_rounds ? encode_escape_kernel<2> : encode_escape_kernel<1>;
+        if (smem2_max > 48 * 1024)
+            UZIP_CUDA_TRY(cudaFuncSetAttribute(esc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2_max));
+        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, esc_kernel, kThreads, smem2_max));
         if (per_sm1 < 1 || per_sm2 < 1) return UZIP_ERR_CUDA;
+        // Escape-kernel ranges: whole chunks, sized so every resident warp
+        // gets at most one (the per-range cost is mostly load latency).
+        const uint64_t warps2 = (uint64_t)sms * per_sm2 * kWarps;
+        const uint32_t rc_max =
+            std::max<uint32_t>(1, std::min<uint32_t>(kMaxRangeChunks, kMaxRangeUnits * kUnit / chunk));
+        p.range_chunks = (uint32_t)std::min<uint64_t>(rc_max, std::max<uint64_t>(1, (L.nc + warps2 - 1) / warps2));
+        p.ranges = (L.nc + p.range_chunks - 1) / p.range_chunks;
+        const size_t smem2 = (size_t)kWarps * kStageBytes +
+                             4 * (((size_t)g.nseg + 1 + 3) / 4 * 4 + (size_t)kWarps * (p.range_chunks + 1));
         const uint64_t grid1 = std::min<uint64_t>((g.units + kWarps - 1) / kWarps, (uint64_t)sms * per_sm1);
-        const uint64_t grid2 = std::min<uint64_t>((g.ranges + kWarps - 1) / kWarps, (uint64_t)sms * per_sm2);
+        const uint64_t grid2 = std::min<uint64_t>((p.ranges + kWarps - 1) / kWarps, (uint64_t)sms * per_sm2);
         UZIP_CUDA_TRY(cudaMemsetAsync(ws, 0, g.off_counts, s));  // header + segment totals
         encode_dense_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
-        encode_escape_kernel<<<(unsigned)grid2, kThreads, smem2, s>>>(p);
+        esc_kernel<<<(unsigned)grid2, kThreads, smem2, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
     }
     if (h_out_bytes) {
@@ -620,7 +755,8 @@ constexpr uint64_t workspace_bytes_for(uint64_t n) {
     uint64_t seg_units = 64;
     while ((units + seg_units - 1) / seg_units > kMaxSegments) seg_units *= 2;
     const uint64_t nseg = (units + seg_units - 1) / seg_units;
-    return sizeof(WsHeader) + cpad16(4 * nseg) + cpad16(4 * units) + cpad16((n + 7) / 8);
+    return sizeof(WsHeader) + cpad16(4 * nseg) + cpad16(4 * units) + 4ull * kListCap * units +
+           (uint64_t)kUnitGroups * units;
 }
 
 constexpr uint64_t kNoAllocScratchBytes = workspace_bytes_for(UZIP_NOALLOC_MAX_N);

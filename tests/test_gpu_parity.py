@@ -81,7 +81,7 @@ def test_sweep_small(uz, orc, chunk):
 
 # ----------------------------------------------------------------- edge sizes
 
-EDGE_CHUNKS = [8, 24, 256, 1000, 1024, 4096, 8192, 8200, 16384, 65536]
+EDGE_CHUNKS = [8, 24, 256, 1000, 1024, 4096, 8192, 8200, 16384, 63496, 64008, 65528, 65536]
 
 
 @pytest.mark.parametrize("chunk", EDGE_CHUNKS)
