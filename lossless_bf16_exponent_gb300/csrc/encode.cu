@@ -112,10 +112,11 @@ struct Params {
 };
 
 // Eight values -> 8 sign-mantissa bytes (a_lo, a_hi), 8 packed codes (one
-// word, value i in nibble i), an 8-bit escape mask and the 8 exponents.
+// word, value i in nibble i), the escape flags (bit 7 of byte i of esc_lo /
+// esc_hi for value i / i + 4) and the 8 exponents.
 __device__ __forceinline__ void encode_group(const uint4 v, const uint8_t* tab, uint32_t& a_lo,
-                                             uint32_t& a_hi, uint32_t& codes, uint32_t& mask, uint32_t& e_lo,
-                                             uint32_t& e_hi) {
+                                             uint32_t& a_hi, uint32_t& codes, uint32_t& esc_lo, uint32_t& esc_hi,
+                                             uint32_t& e_lo, uint32_t& e_hi) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t packed[2], esc[2], am[2], ex[2];
 #pragma unroll
@@ -129,8 +130,8 @@ __device__ __forceinline__ void encode_group(const uint4 v, const uint8_t* tab, 
         ex[h] = e4;
         // Table byte = code | escape << 7.
         const uint32_t t0 = tab[e4 & 0xFF];
-        const uint32_t t1 = tab[(e4 >> 8) & 0xFF];
-        const uint32_t t2 = tab[(e4 >> 16) & 0xFF];
+        const uint32_t t1 = tab[prmt(e4, 0, 0x4441)];
+        const uint32_t t2 = tab[prmt(e4, 0, 0x4442)];
         const uint32_t t3 = tab[e4 >> 24];
         const uint32_t t4 = prmt(prmt(t0, t1, 0x0040), prmt(t2, t3, 0x0040), 0x5410);
         const uint32_t c = t4 & 0x0F0F0F0Fu;
@@ -141,11 +142,17 @@ __device__ __forceinline__ void encode_group(const uint4 v, const uint8_t* tab, 
     a_hi = am[1];
     e_lo = ex[0];
     e_hi = ex[1];
+    esc_lo = esc[0];
+    esc_hi = esc[1];
     codes = prmt(packed[0], packed[1], 0x6420);
-    // Bit 7 of byte i -> bit i (the four shifted copies never overlap).
-    const uint32_t m_lo = (((esc[0] >> 7) * 0x204081u) >> 21) & 0xF;
-    const uint32_t m_hi = (((esc[1] >> 7) * 0x204081u) >> 21) & 0xF;
-    mask = m_lo | (m_hi << 4);
+}
+
+// Escape flags (bit 7 of each byte) -> 8-bit mask, value i at bit i (the four
+// shifted copies of the multiply never overlap).
+__device__ __forceinline__ uint32_t escape_mask(uint32_t esc_lo, uint32_t esc_hi) {
+    const uint32_t m_lo = (((esc_lo >> 7) * 0x204081u) >> 21) & 0xF;
+    const uint32_t m_hi = (((esc_hi >> 7) * 0x204081u) >> 21) & 0xF;
+    return m_lo | (m_hi << 4);
 }
 
 __device__ void write_header(const Params& p, uint64_t m, uint32_t flags) {
@@ -182,8 +189,9 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
         uint8_t* dst_a = p.out + p.L.off_a + ubase;
         uint8_t* dst_b = p.out + p.L.off_b + ubase / 2;
         uint32_t* list = p.lists + u * kListCap;
-        uint32_t cnt = 0;      // escapes so far in this unit (uniform across the warp)
-        uint32_t mbytes[2] = {0, 0};  // this lane's 8 mask bytes, in case the list overflows
+        const bool full = ulen == kUnit;  // every unit but the tensor's last
+        uint32_t cnt = 0;                 // escapes so far in this unit (uniform across the warp)
+        uint32_t mbytes[2] = {0, 0};      // this lane's 8 mask bytes, in case the list overflows
 #pragma unroll kIterUnroll
         for (int it = 0; it < 2; it++) {
             uint4 v[4];
@@ -191,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
             for (int r = 0; r < 4; r++) {
                 const uint32_t g = it * 128 + r * 32 + lane;
                 v[r] = make_uint4(0, 0, 0, 0);
-                if (8 * g + 8 <= ulen) {
+                if (full || 8 * g + 8 <= ulen) {
                     v[r] = ld_stream_v4(src + g);
                 } else if (8 * g < ulen) {  // ragged tail of the tensor (< 8 values)
                     uint32_t w[4] = {0, 0, 0, 0};
@@ -204,38 +212,51 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
 #pragma unroll
             for (int r = 0; r < 4; r++) {
                 const uint32_t g = it * 128 + r * 32 + lane;
-                uint32_t mask = 0, e_lo = 0, e_hi = 0;
-                if (8 * g < ulen) {
+                uint32_t esc_lo = 0, esc_hi = 0, e_lo = 0, e_hi = 0;
+                if (full || 8 * g < ulen) {
                     uint32_t a_lo, a_hi, codes;
-                    encode_group(v[r], s_tab, a_lo, a_hi, codes, mask, e_lo, e_hi);
-                    if (8 * g + 8 > ulen) {  // codes and escapes of real values only
+                    encode_group(v[r], s_tab, a_lo, a_hi, codes, esc_lo, esc_hi, e_lo, e_hi);
+                    if (!full && 8 * g + 8 > ulen) {  // codes and escapes of real values only
                         const uint32_t valid = ulen - 8 * g;
-                        mask &= (1u << valid) - 1;
+                        const uint64_t keep = (1ull << (8 * valid)) - 1;
+                        esc_lo &= (uint32_t)keep;
+                        esc_hi &= (uint32_t)(keep >> 32);
                         codes &= (1u << (4 * valid)) - 1;
                     }
                     *reinterpret_cast<uint2*>(dst_a + 8 * g) = make_uint2(a_lo, a_hi);
                     *reinterpret_cast<uint32_t*>(dst_b + 4 * g) = codes;
                 }
-                // Groups g = it*128 + r*32 + lane come in ascending order per
-                // (it, r) row, so a warp scan ranks the row's escapes (the
-                // whole warp takes part, tail lanes with an empty mask).
-                if (__any_sync(0xffffffffu, mask != 0)) {
+                // Escapes are rare: the mask and the ranking run only for rows
+                // holding one. Groups g = it*128 + r*32 + lane come in
+                // ascending order per (it, r) row, so a warp scan ranks the
+                // row's escapes (the whole warp takes part).
+                if (__any_sync(0xffffffffu, (esc_lo | esc_hi) != 0)) {
+                    const uint32_t mask = escape_mask(esc_lo, esc_hi);
                     const uint32_t c = __popc(mask);
-                    uint32_t incl = c;
+                    uint32_t excl, total;
+                    if (!__any_sync(0xffffffffu, c > 1)) {  // sparse row: one ballot ranks it
+                        const uint32_t b = __ballot_sync(0xffffffffu, c != 0);
+                        excl = __popc(b & ((1u << lane) - 1));
+                        total = __popc(b);
+                    } else {
+                        uint32_t incl = c;
 #pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                        if (lane >= o) incl += t;
+                        for (int o = 1; o < 32; o <<= 1) {
+                            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                            if (lane >= o) incl += t;
+                        }
+                        excl = incl - c;
+                        total = __shfl_sync(0xffffffffu, incl, 31);
                     }
-                    uint32_t j = cnt + incl - c;
+                    uint32_t j = cnt + excl;
                     for (uint32_t bits = mask; bits; bits &= bits - 1, j++) {
                         const uint32_t b = __ffs(bits) - 1;
                         const uint32_t e = ((b < 4 ? e_lo : e_hi) >> (8 * (b & 3))) & 0xFF;
                         if (j < kListCap) list[j] = (8 * g + b) | (e << 16);
                     }
-                    cnt += __shfl_sync(0xffffffffu, incl, 31);
+                    cnt += total;
+                    mbytes[it] |= mask << (8 * r);
                 }
-                mbytes[it] |= mask << (8 * r);
             }
         }
         if (cnt > kListCap) {  // the list overflowed: keep the masks instead
