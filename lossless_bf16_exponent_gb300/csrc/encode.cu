@@ -13,23 +13,27 @@
 // chain of inclusive prefixes; on GB300 that chain, not HBM, set the pace
 // (one window of predecessors per loaded-L2 round trip). So the prefix is
 // resolved by the kernel boundary instead:
-//   dense kernel   each warp owns fixed units of 2048 values (grid-stride, no
-//                  tickets, no barriers): 16-byte loads -> exponent and
-//                  sign-mantissa bytes with byte permutes -> code + escape bit
-//                  from a 256-byte shared table -> coalesced 8-byte
-//                  sign-mantissa and 4-byte code stores. Its escapes go, in
-//                  ascending order, into the unit's list of up to kListCap
-//                  (position, exponent) entries in the workspace; a unit with
-//                  more escapes stores its escape-mask bytes instead. It also
-//                  stores the unit's escape count and adds it to its segment's
-//                  total (64+ units per segment).
-//   escape kernel  every CTA scans the segment totals in shared memory; each
-//                  warp takes ranges of whole chunks (up to 32 units, one per
-//                  lane), finds the range's first escape rank from the segment
-//                  prefix and unit counts, writes the chunk offsets and then
-//                  each escape's chunk-relative position and raw exponent in
-//                  ascending element order, bounds-checked against
-//                  out_capacity. The last CTA to finish writes the header.
+//   dense kernel   warps take units of 2048 values in grid-stride order (all
+//                  warps stream one compact window of the input, which keeps
+//                  HBM rows open; contiguous per-warp spans measured 8 % slower):
+//                  16-byte loads -> exponent and sign-mantissa bytes with byte
+//                  permutes -> code + escape bit from a 256-byte shared table ->
+//                  coalesced 8-byte sign-mantissa and 4-byte code stores. Its
+//                  escapes go, in ascending order, into the unit's list of up to
+//                  kListCap (position, exponent) entries in the workspace; a
+//                  unit with more escapes stores its escape-mask bytes instead.
+//                  It stores the unit's escape count and adds it to its
+//                  segment's total (64 or more units per segment; the totals
+//                  are cleared before the launch).
+//   escape kernel  launched as a programmatic dependent of the dense kernel (its
+//                  launch overlaps the dense tail; it waits for the dense
+//                  results before touching them). Each warp takes a range of
+//                  whole chunks (up to 32 units, one per lane), adds the
+//                  segment and unit totals before it into the range's first
+//                  escape rank, writes the chunk offsets and then each escape's
+//                  chunk-relative position and raw exponent in ascending
+//                  element order, bounds-checked against out_capacity. The warp
+//                  that owns the last range writes the tail and the header.
 // The input is read from HBM once; the escape lists cost about 4 bytes per
 // escape written and read.
 #include <algorithm>
@@ -44,8 +48,9 @@ constexpr uint32_t kUnit = 2048;              // values per counting unit (one w
 constexpr uint32_t kUnitGroups = kUnit / 8;   // its mask bytes
 constexpr int kThreads = 256;                 // both kernels
 constexpr int kWarps = kThreads / 32;
-constexpr uint32_t kMaxSegments = 2048;       // segment totals one CTA scans
+constexpr uint32_t kMaxSegments = 2048;       // segment totals (a block sums up to all of them)
 constexpr uint32_t kListCap = 64;             // escape entries a unit keeps in its list
+constexpr uint32_t kHeadEntries = 8;          // list entries in the first 32-byte sector
 constexpr uint32_t kMaxRangeUnits = 31;       // a range covers at most 31 units of values (32 overlapped)
 constexpr uint32_t kStageBytes = 4096;        // per-warp staging of a range's escape blocks
 constexpr uint32_t kMaxRangeChunks = 256;     // bounds the per-warp chunk table
@@ -57,35 +62,31 @@ constexpr int kBatch = 8;                     // escape exponents re-read at onc
 #define UZIP_ENC_ITER_UNROLL 2
 #endif
 #ifndef UZIP_ESC_MIN_BLOCKS
-#define UZIP_ESC_MIN_BLOCKS 2
+#define UZIP_ESC_MIN_BLOCKS 4
 #endif
 constexpr int kIterUnroll = UZIP_ENC_ITER_UNROLL;  // 2: both 4-load batches of a unit in flight per lane
 
-// Start of the caller's workspace.
-struct WsHeader {
-    unsigned int done;
-    unsigned int flags;
-    unsigned long long m;
-    unsigned long long pad[6];
-};
-static_assert(sizeof(WsHeader) == 64, "workspace header is 64 bytes");
-
+// Workspace layout, a function of n only: segment totals (cleared by each
+// call) | unit counts | unit lists | unit mask bytes. Every other word the
+// escape kernel reads is written by the dense kernel of the same call.
 struct Geometry {
-    uint64_t units;         // counting units of kUnit values
-    uint32_t seg_units;     // units per segment (power of two, >= 64)
-    uint32_t nseg;          // segments
-    uint64_t off_segs, off_counts, off_lists, off_masks, bytes;  // workspace layout
+    uint64_t units;      // counting units of kUnit values
+    uint32_t seg_units;  // units per segment (power of two, >= 64)
+    uint32_t nseg;       // segments
+    uint64_t off_segs, off_counts, off_lists, off_masks, bytes;
 };
 
-__host__ Geometry geometry_of(uint64_t n, uint32_t chunk) {
-    Geometry g;
+__host__ __device__ constexpr uint64_t pad16c(uint64_t v) { return (v + 15) / 16 * 16; }
+
+__host__ __device__ constexpr Geometry geometry_of(uint64_t n) {
+    Geometry g{};
     g.units = (n + kUnit - 1) / kUnit;
     g.seg_units = 64;
     while ((g.units + g.seg_units - 1) / g.seg_units > kMaxSegments) g.seg_units *= 2;
     g.nseg = (uint32_t)((g.units + g.seg_units - 1) / g.seg_units);
-    g.off_segs = sizeof(WsHeader);
-    g.off_counts = g.off_segs + pad16(4ull * g.nseg);
-    g.off_lists = g.off_counts + pad16(4ull * g.units);
+    g.off_segs = 0;
+    g.off_counts = g.off_segs + pad16c(4ull * g.nseg);
+    g.off_lists = g.off_counts + pad16c(4ull * g.units);
     g.off_masks = g.off_lists + 4ull * kListCap * g.units;
     g.bytes = g.off_masks + (uint64_t)kUnitGroups * g.units;
     return g;
@@ -95,8 +96,8 @@ struct Params {
     const uint16_t* in;
     uint64_t n;
     uint32_t chunk;
-    uint32_t seg_units;
-    uint32_t nseg;
+    uint32_t seg_units;   // units per segment
+    uint32_t nseg;        // segments
     uint32_t range_chunks;
     uint64_t units;
     uint64_t ranges;
@@ -104,12 +105,17 @@ struct Params {
     uint8_t* out;
     uint64_t cap;
     Layout L;
-    WsHeader* ws;
-    uint32_t* segs;
-    uint32_t* counts;
-    uint32_t* lists;  // kListCap entries per unit: position | exponent << 16
-    uint8_t* masks;   // kUnitGroups bytes per unit, written only when a unit overflows its list
+    uint32_t* segs;    // escapes per segment
+    uint32_t* counts;  // escapes per unit
+    uint32_t* lists;   // kListCap entries per unit: position | exponent << 16
+    uint8_t* masks;    // kUnitGroups bytes per unit, written only when a unit overflows its list
 };
+
+// Programmatic dependent launch (PTX griddepcontrol): the dense kernel lets
+// the escape kernel be scheduled early; the escape kernel waits until the
+// dense grid has completed and its writes are visible.
+__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_for_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Eight values -> 8 sign-mantissa bytes (a_lo, a_hi), 8 packed codes (one
 // word, value i in nibble i), the escape flags (bit 7 of byte i of esc_lo /
@@ -179,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
     uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_tab_words);
     s_tab[threadIdx.x] = p.cb[UZIP_CB_ENC + threadIdx.x] | (p.cb[UZIP_CB_ESC + threadIdx.x] ? 0x80 : 0);
     __syncthreads();
+    allow_dependent_launch();
 
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t stride = (uint64_t)gridDim.x * kWarps;
@@ -284,7 +291,6 @@ struct UnitPart {
     uint32_t plo, phi;
     bool list;
     const uint32_t* entries;
-    const uint32_t* mwords;  // 64 mask words: bit i of word w = unit position 32 w + i
 };
 
 // Bits of mask word w (unit positions 32 w ..) that lie in [lo, hi).
@@ -295,29 +301,11 @@ __device__ __forceinline__ uint32_t bits_in(uint32_t word, uint32_t w, uint32_t 
     return word & keep_hi & ~drop_lo;
 }
 
-// Escapes of a list unit below plo and inside [plo, phi), from its sorted
-// list (head = its first four entries, already loaded).
-__device__ __forceinline__ void count_part(const UnitPart& up, const uint4 head, uint32_t& n_lo, uint32_t& n_in) {
-    n_lo = 0;
-    n_in = 0;
-    for (uint32_t i = 0; i < up.cnt; i += 4) {
-        const uint4 q4 = i == 0 ? head : __ldg(reinterpret_cast<const uint4*>(up.entries + i));
-        const uint32_t qs[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-        for (int t = 0; t < 4; t++) {
-            if (i + t < up.cnt) {
-                const uint32_t pos = qs[t] & 0xFFFF;
-                n_lo += pos < up.plo;
-                n_in += pos >= up.plo && pos < up.phi;
-            }
-        }
-    }
-}
-
-// A range's loads, issued together before any of them is used: the counts
-// and first four list entries of its units (two rounds of one unit per lane)
-// and the counts of the earlier units of its first unit's segment.
-constexpr int kPreLoads = 8;   // earlier-unit counts per lane (segments of up to 256 units)
+// A range's loads, issued together before any of them is used: per unit (one
+// per lane and round) its count and first kHeadEntries list entries; the
+// counts of the earlier units of u0's segment; the segment totals between the
+// block's base segment and u0's segment.
+constexpr int kPreLoads = 8;  // earlier-unit counts per lane, loaded up front (segments up to 256 units)
 
 // kRounds = 1 when every range overlaps at most 32 units (one per lane); 2 for
 // the chunk sizes whose single chunk can overlap 33 units (longer than
@@ -326,18 +314,19 @@ template <int kRounds>
 struct RangeLoads {
     uint32_t c0, nq, s, e, u0, nu, seg;
     uint32_t cnt[kRounds];
-    uint4 head[kRounds];
+    uint4 h0[kRounds], h1[kRounds];
     uint32_t pre_cnt[kPreLoads];
+    uint32_t mid;
 };
 
 template <int kRounds>
-__device__ __forceinline__ void load_range(const Params& p, uint64_t r, RangeLoads<kRounds>& rl) {
+__device__ __forceinline__ void load_range(const Params& p, uint64_t r, uint32_t seg_first, RangeLoads<kRounds>& rl) {
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t C = p.chunk;
     rl.c0 = (uint32_t)(r * p.range_chunks);
     const uint32_t c1 = (uint32_t)min((uint64_t)rl.c0 + p.range_chunks, p.L.nc);
     rl.nq = c1 - rl.c0;
-    rl.s = rl.c0 * C;  // n < 2^32
+    rl.s = rl.c0 * C;  // < n < 2^32
     rl.e = (uint32_t)min((uint64_t)c1 * C, p.n);
     rl.u0 = rl.s / kUnit;
     rl.nu = (rl.e - 1) / kUnit - rl.u0 + 1;
@@ -346,9 +335,10 @@ __device__ __forceinline__ void load_range(const Params& p, uint64_t r, RangeLoa
     for (int rr = 0; rr < kRounds; rr++) {
         const uint32_t u = rl.u0 + 32 * rr + lane;
         const bool on = 32 * rr + lane < rl.nu;
+        const uint4* head = reinterpret_cast<const uint4*>(p.lists + (uint64_t)u * kListCap);
         rl.cnt[rr] = on ? __ldg(p.counts + u) : 0;
-        rl.head[rr] = on ? __ldg(reinterpret_cast<const uint4*>(p.lists + (uint64_t)u * kListCap))
-                         : make_uint4(0, 0, 0, 0);
+        rl.h0[rr] = on ? __ldg(head) : make_uint4(0, 0, 0, 0);
+        rl.h1[rr] = on ? __ldg(head + 1) : make_uint4(0, 0, 0, 0);
     }
     const uint32_t first = rl.seg * p.seg_units;
 #pragma unroll
@@ -356,294 +346,302 @@ __device__ __forceinline__ void load_range(const Params& p, uint64_t r, RangeLoa
         const uint32_t i = first + 32 * j + lane;
         rl.pre_cnt[j] = i < rl.u0 ? __ldg(p.counts + i) : 0;
     }
+    uint32_t mid = 0;
+    for (uint32_t i = seg_first + lane; i < rl.seg; i += 32) mid += __ldg(p.segs + i);
+    rl.mid = mid;
 }
 
+// One range: the chunk offsets c0 .. c0 + nq - 1 and the range's escape blocks
+// (and, for the last range, offsets[nc], the padding and the header). base =
+// escapes before the block's base segment.
 template <int kRounds>
-__global__ void __launch_bounds__(kThreads, UZIP_ESC_MIN_BLOCKS) encode_escape_kernel(const Params p) {
-    extern __shared__ __align__(16) uint32_t s_dyn[];
-    __shared__ uint32_t s_warp[kWarps];
-    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // Layout: per-warp escape staging | segment prefixes (nseg + 1) | per-warp chunk tables.
-    uint8_t* stage = reinterpret_cast<uint8_t*>(s_dyn) + warp * kStageBytes;
-    uint32_t* s_segpref = s_dyn + kWarps * kStageBytes / 4;
-    uint32_t* s_cp = s_segpref + ((p.nseg + 1 + 3) & ~3u) + warp * (p.range_chunks + 1);
+__device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<kRounds>& rl, uint32_t base,
+                                             uint8_t* stage, uint32_t* s_head, uint32_t* s_cp) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t C = p.chunk;
+    const uint32_t c0 = rl.c0, nq = rl.nq, s = rl.s, e = rl.e, u0 = rl.u0, nu = rl.nu, seg = rl.seg;
 
-    const uint64_t stride = (uint64_t)gridDim.x * kWarps;
-    uint64_t r = (uint64_t)blockIdx.x * kWarps + warp;
-    RangeLoads<kRounds> rl;
-    if (r < p.ranges) load_range(p, r, rl);  // in flight during the segment scan below
-
-    // Segment prefix, one block scan (kMaxSegments / kThreads = 8 totals per
-    // thread, loaded together).
-    {
-        constexpr int kPer = kMaxSegments / kThreads;
-        uint32_t v[kPer];
-        uint32_t sum = 0;
+    // Each lane keeps its units' first list entries in shared memory,
+    // [round][entry][lane] (a lane only reads its own column).
 #pragma unroll
-        for (int i = 0; i < kPer; i++) {
-            const uint32_t idx = tid * kPer + i;
-            v[i] = idx < p.nseg ? p.segs[idx] : 0;
+    for (int rr = 0; rr < kRounds; rr++) {
+        const uint32_t q[kHeadEntries] = {rl.h0[rr].x, rl.h0[rr].y, rl.h0[rr].z, rl.h0[rr].w,
+                                          rl.h1[rr].x, rl.h1[rr].y, rl.h1[rr].z, rl.h1[rr].w};
+#pragma unroll
+        for (int j = 0; j < (int)kHeadEntries; j++) s_head[(rr * kHeadEntries + j) * 32 + lane] = q[j];
+    }
+    auto entry = [&](int rr, const uint32_t* entries, uint32_t j) -> uint32_t {
+        return j < kHeadEntries ? s_head[(rr * kHeadEntries + j) * 32 + lane] : __ldg(entries + j);
+    };
+
+    UnitPart up[kRounds];
+    uint32_t n_lo[kRounds], n_in[kRounds];
+#pragma unroll
+    for (int rr = 0; rr < kRounds; rr++) {
+        n_lo[rr] = n_in[rr] = 0;
+        up[rr].list = true;
+        if (32 * rr + lane < nu) {
+            UnitPart& u = up[rr];
+            const uint32_t uidx = u0 + 32 * rr + lane;
+            u.ubase = (uint64_t)uidx * kUnit;
+            u.cnt = rl.cnt[rr];
+            u.plo = s > u.ubase ? (uint32_t)(s - u.ubase) : 0u;
+            u.phi = (uint32_t)min((uint64_t)kUnit, (uint64_t)e - u.ubase);
+            u.list = u.cnt <= kListCap;
+            u.entries = p.lists + (uint64_t)uidx * kListCap;
+            if (u.list) {
+                const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - u.ubase);
+                if (u.plo == 0 && u.phi >= ulen) {
+                    n_in[rr] = u.cnt;  // the whole unit lies in the range
+                } else {
+                    for (uint32_t j = 0; j < u.cnt; j++) {
+                        const uint32_t pos = entry(rr, u.entries, j) & 0xFFFF;
+                        n_lo[rr] += pos < u.plo;
+                        n_in[rr] += pos >= u.plo && pos < u.phi;
+                    }
+                }
+            }
         }
+    }
+    // Units that overflowed their list are handled by the whole warp: lane
+    // l takes mask words 2l and 2l+1 (unit positions 64l .. 64l+63).
+    auto coop = [&](int rr, int o, uint64_t& ub, uint32_t& plo, uint32_t& phi, uint32_t& b0, uint32_t& b1) {
+        ub = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(up[rr].ubase >> 32), o) << 32) |
+             __shfl_sync(0xffffffffu, (uint32_t)up[rr].ubase, o);
+        plo = __shfl_sync(0xffffffffu, up[rr].plo, o);
+        phi = __shfl_sync(0xffffffffu, up[rr].phi, o);
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.masks + (ub / kUnit) * kUnitGroups) + lane);
+        b0 = bits_in(w.x, 2 * lane, plo, phi);
+        b1 = bits_in(w.y, 2 * lane + 1, plo, phi);
+        return w;
+    };
 #pragma unroll
-        for (int i = 0; i < kPer; i++) sum += v[i];
-        uint32_t incl = sum;
+    for (int rr = 0; rr < kRounds; rr++) {
+        for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
+            const int o = __ffs(ovf) - 1;
+            uint64_t ub;
+            uint32_t plo, phi, b0, b1;
+            const uint2 w = coop(rr, o, ub, plo, phi, b0, b1);
+            const uint32_t lo = warp_sum(__popc(bits_in(w.x, 2 * lane, 0, plo)) +
+                                         __popc(bits_in(w.y, 2 * lane + 1, 0, plo)));
+            const uint32_t in = warp_sum(__popc(b0) + __popc(b1));
+            if (lane == (uint32_t)o) {
+                n_lo[rr] = lo;
+                n_in[rr] = in;
+            }
+        }
+    }
+    // Escapes before s: the block base, the segment totals up to u0's
+    // segment, the earlier units of that segment, and unit u0's escapes
+    // before s.
+    uint32_t part = rl.mid;
+#pragma unroll
+    for (int j = 0; j < kPreLoads; j++) part += rl.pre_cnt[j];
+    for (uint32_t i = seg * p.seg_units + 32 * kPreLoads + lane; i < u0; i += 32) part += __ldg(p.counts + i);
+    const uint32_t pre = base + warp_sum(part) + __shfl_sync(0xffffffffu, n_lo[0], 0);
+
+    // Pass 1: running rank of each unit's first in-range escape, and every
+    // chunk's first rank. Chunk q starts at value s + q * C.
+    __syncwarp();  // the previous range's chunk table is no longer read
+    uint32_t first[kRounds];
+    uint32_t carry = 0;
+#pragma unroll
+    for (int rr = 0; rr < kRounds; rr++) {
+        uint32_t incl = n_in[rr];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += t;
         }
-        if (lane == 31) s_warp[warp] = incl;
-        __syncthreads();
-        uint32_t run = incl - sum;
-        for (uint32_t w = 0; w < warp; w++) run += s_warp[w];
-#pragma unroll
-        for (int i = 0; i < kPer; i++) {
-            const uint32_t idx = tid * kPer + i;
-            if (idx <= p.nseg) s_segpref[idx] = run;
-            run += v[i];
-        }
-        __syncthreads();
-    }
-
-    const uint32_t C = p.chunk;
-    bool overflow = false;
-    for (; r < p.ranges; r += stride) {
-        const uint32_t c0 = rl.c0, nq = rl.nq, s = rl.s, e = rl.e, u0 = rl.u0, nu = rl.nu, seg = rl.seg;
-        UnitPart up[kRounds];
-        uint32_t n_lo[kRounds], n_in[kRounds];
-#pragma unroll
-        for (int rr = 0; rr < kRounds; rr++) {
-            n_lo[rr] = n_in[rr] = 0;
-            up[rr].list = true;
-            if (32 * rr + lane < nu) {
-                UnitPart& u = up[rr];
-                u.ubase = (uint64_t)(u0 + 32 * rr + lane) * kUnit;
-                u.cnt = rl.cnt[rr];
-                u.plo = s > u.ubase ? (uint32_t)(s - u.ubase) : 0u;
-                u.phi = (uint32_t)min((uint64_t)kUnit, (uint64_t)e - u.ubase);
-                u.list = u.cnt <= kListCap;
-                u.entries = p.lists + (u.ubase / kUnit) * kListCap;
-                u.mwords = reinterpret_cast<const uint32_t*>(p.masks + (u.ubase / kUnit) * kUnitGroups);
-                if (u.list) count_part(u, rl.head[rr], n_lo[rr], n_in[rr]);
+        first[rr] = carry + incl - n_in[rr];
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+        if (32 * rr + lane < nu && up[rr].list) {
+            const UnitPart& u = up[rr];
+            const uint32_t v_lo = (uint32_t)(u.ubase + u.plo) - s;  // range offset of plo
+            uint32_t q = (v_lo + C - 1) / C;
+            uint32_t x = (uint32_t)(s + q * C - u.ubase);  // unit position of chunk q's start
+            uint32_t i = n_lo[rr];
+            const uint32_t iend = n_lo[rr] + n_in[rr];
+            while (q < nq && x < u.phi) {
+                while (i < iend && (entry(rr, u.entries, i) & 0xFFFF) < x) i++;
+                s_cp[q] = first[rr] + (i - n_lo[rr]);
+                q++;
+                x += C;
             }
         }
-        // Units that overflowed their list are handled by the whole warp: lane
-        // l takes mask words 2l and 2l+1 (unit positions 64l .. 64l+63).
-        auto coop = [&](int rr, int o, uint64_t& ub, uint32_t& plo, uint32_t& phi, uint32_t& b0, uint32_t& b1) {
-            ub = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(up[rr].ubase >> 32), o) << 32) |
-                 __shfl_sync(0xffffffffu, (uint32_t)up[rr].ubase, o);
-            plo = __shfl_sync(0xffffffffu, up[rr].plo, o);
-            phi = __shfl_sync(0xffffffffu, up[rr].phi, o);
-            const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.masks + (ub / kUnit) * kUnitGroups) + lane);
-            b0 = bits_in(w.x, 2 * lane, plo, phi);
-            b1 = bits_in(w.y, 2 * lane + 1, plo, phi);
-            return w;
-        };
+        for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
+            const int o = __ffs(ovf) - 1;
+            uint64_t ub;
+            uint32_t plo, phi, b0, b1;
+            coop(rr, o, ub, plo, phi, b0, b1);
+            const uint32_t f = __shfl_sync(0xffffffffu, first[rr], o);
+            const uint32_t c = __popc(b0) + __popc(b1);
+            uint32_t ic = c;
 #pragma unroll
-        for (int rr = 0; rr < kRounds; rr++) {
-            for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
-                const int o = __ffs(ovf) - 1;
-                uint64_t ub;
-                uint32_t plo, phi, b0, b1;
-                const uint2 w = coop(rr, o, ub, plo, phi, b0, b1);
-                const uint32_t lo = warp_sum(__popc(bits_in(w.x, 2 * lane, 0, plo)) +
-                                             __popc(bits_in(w.y, 2 * lane + 1, 0, plo)));
-                const uint32_t in = warp_sum(__popc(b0) + __popc(b1));
-                if (lane == (uint32_t)o) {
-                    n_lo[rr] = lo;
-                    n_in[rr] = in;
-                }
+            for (int k = 1; k < 32; k <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, ic, k);
+                if (lane >= k) ic += t;
             }
-        }
-        // Escapes before s: segment prefix + earlier units of the segment +
-        // unit u0's escapes before s.
-        uint32_t part = 0;
-#pragma unroll
-        for (int j = 0; j < kPreLoads; j++) part += rl.pre_cnt[j];
-        for (uint32_t i = seg * p.seg_units + 32 * kPreLoads + lane; i < u0; i += 32) part += __ldg(p.counts + i);
-        uint64_t pre = (uint64_t)s_segpref[seg] + warp_sum(part) + __shfl_sync(0xffffffffu, n_lo[0], 0);
-
-        // Pass 1: running rank of each unit's first in-range escape, and every
-        // chunk's first rank. Chunk q starts at value s + q * C.
-        __syncwarp();  // the previous range's chunk table is no longer read
-        uint32_t first[kRounds];
-        uint32_t carry = 0;
-#pragma unroll
-        for (int rr = 0; rr < kRounds; rr++) {
-            uint32_t incl = n_in[rr];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            first[rr] = carry + incl - n_in[rr];
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-            if (32 * rr + lane < nu && up[rr].list) {
-                const UnitPart& u = up[rr];
-                const uint32_t v_lo = (uint32_t)(u.ubase + u.plo) - s;  // range offset of plo
+            const uint32_t before = f + ic - c;  // rank of this lane's first escape
+            const uint32_t lo = max(64 * lane, plo), hi = min(64 * lane + 64, phi);
+            if (lo < hi) {
+                const uint32_t v_lo = (uint32_t)(ub + lo) - s;
                 uint32_t q = (v_lo + C - 1) / C;
-                uint32_t x = (uint32_t)(s + q * C - u.ubase);  // unit position of chunk q's start
-                uint32_t i = n_lo[rr];
-                const uint32_t iend = n_lo[rr] + n_in[rr];
-                while (q < nq && x < u.phi) {
-                    while (i < iend && (__ldg(u.entries + i) & 0xFFFF) < x) i++;
-                    s_cp[q] = first[rr] + (i - n_lo[rr]);
+                uint32_t x = (uint32_t)(s + q * C - ub);
+                while (q < nq && x < hi) {
+                    const uint32_t d = x - 64 * lane;  // 0..63
+                    const uint32_t below = d < 32 ? __popc(b0 & ((1u << d) - 1))
+                                                  : __popc(b0) + __popc(b1 & ((1u << (d - 32)) - 1));
+                    s_cp[q] = before + below;
                     q++;
                     x += C;
                 }
             }
-            for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
-                const int o = __ffs(ovf) - 1;
-                uint64_t ub;
-                uint32_t plo, phi, b0, b1;
-                coop(rr, o, ub, plo, phi, b0, b1);
-                const uint32_t f = __shfl_sync(0xffffffffu, first[rr], o);
-                const uint32_t c = __popc(b0) + __popc(b1);
-                uint32_t ic = c;
-#pragma unroll
-                for (int k = 1; k < 32; k <<= 1) {
-                    const uint32_t t = __shfl_up_sync(0xffffffffu, ic, k);
-                    if (lane >= k) ic += t;
-                }
-                const uint32_t before = f + ic - c;  // rank of this lane's first escape
-                const uint32_t lo = max(64 * lane, plo), hi = min(64 * lane + 64, phi);
-                if (lo < hi) {
-                    const uint32_t v_lo = (uint32_t)(ub + lo) - s;
-                    uint32_t q = (v_lo + C - 1) / C;
-                    uint32_t x = (uint32_t)(s + q * C - ub);
-                    while (q < nq && x < hi) {
-                        const uint32_t d = x - 64 * lane;  // 0..63
-                        const uint32_t below = d < 32 ? __popc(b0 & ((1u << d) - 1))
-                                                      : __popc(b0) + __popc(b1 & ((1u << (d - 32)) - 1));
-                        s_cp[q] = before + below;
-                        q++;
-                        x += C;
-                    }
-                }
-            }
         }
-        const uint32_t rtotal = carry;
-        if (lane == 0) s_cp[nq] = rtotal;
-        __syncwarp();
-
-        uint8_t* offs = p.out + p.L.off_c;
-        for (uint32_t q = lane; q < nq; q += 32)
-            *reinterpret_cast<uint32_t*>(offs + 4ull * (c0 + q)) = (uint32_t)(pre + s_cp[q]);
-        if (r == p.ranges - 1 && lane == 0) {
-            const uint64_t m = pre + rtotal;
-            *reinterpret_cast<uint32_t*>(offs + 4 * p.L.nc) = (uint32_t)m;
-            zero_words(p.out, p.L.off_c + 4 * (p.L.nc + 1), p.L.off_d);
-            const uint64_t groups_all = (p.n + 7) / 8;
-            zero_words(p.out, p.L.off_a + 8 * groups_all, p.L.off_b);
-            zero_words(p.out, p.L.off_b + 4 * groups_all, p.L.off_c);
-            p.ws->m = m;
-        }
-        if (rtotal != 0) {
-            // Pass 2: each escape's chunk-relative position and raw exponent.
-            // The range's escape blocks are contiguous in the stream: assemble
-            // them in this warp's stage and copy them out with coalesced
-            // stores, unless there are too many, then store them directly.
-            const uint64_t dbase = p.L.off_d + 3 * pre;
-            const uint32_t dbytes = 3 * rtotal;
-            const bool staged = dbytes <= kStageBytes;
-            auto put = [&](uint32_t off, uint32_t rank_in_range, uint32_t q, uint32_t expo) {
-                const uint32_t cstart = s_cp[q];
-                const uint32_t k = s_cp[q + 1] - cstart;
-                const uint32_t rank = rank_in_range - cstart;
-                const uint32_t pos = off - q * C;
-                const uint32_t rel_pos = 3 * cstart + 2 * rank, rel_val = 3 * cstart + 2 * k + rank;
-                if (staged) {
-                    stage[rel_pos] = (uint8_t)(pos & 0xFF);
-                    stage[rel_pos + 1] = (uint8_t)(pos >> 8);
-                    stage[rel_val] = (uint8_t)expo;
-                } else if (dbase + rel_val < p.cap && dbase + rel_pos + 1 < p.cap) {
-                    p.out[dbase + rel_pos] = (uint8_t)(pos & 0xFF);
-                    p.out[dbase + rel_pos + 1] = (uint8_t)(pos >> 8);
-                    p.out[dbase + rel_val] = (uint8_t)expo;
-                } else {
-                    overflow = true;
-                }
-            };
-#pragma unroll
-            for (int rr = 0; rr < kRounds; rr++) {
-                if (32 * rr + lane < nu && up[rr].list && n_in[rr]) {
-                    const UnitPart& u = up[rr];
-                    uint32_t running = first[rr];
-                    uint32_t q = ((uint32_t)(u.ubase + u.plo) - s) / C;  // chunk of the part's first value
-                    uint32_t next = (q + 1) * C;
-                    for (uint32_t i = n_lo[rr]; i < n_lo[rr] + n_in[rr]; i++) {
-                        const uint32_t ent = __ldg(u.entries + i);
-                        const uint32_t off = (uint32_t)(u.ubase + (ent & 0xFFFF)) - s;
-                        while (off >= next) {
-                            q++;
-                            next += C;
-                        }
-                        put(off, running++, q, ent >> 16);
-                    }
-                }
-                for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
-                    const int o = __ffs(ovf) - 1;
-                    uint64_t ub;
-                    uint32_t plo, phi, b0, b1;
-                    coop(rr, o, ub, plo, phi, b0, b1);
-                    const uint32_t f = __shfl_sync(0xffffffffu, first[rr], o);
-                    const uint32_t c = __popc(b0) + __popc(b1);
-                    uint32_t ic = c;
-#pragma unroll
-                    for (int k = 1; k < 32; k <<= 1) {
-                        const uint32_t t = __shfl_up_sync(0xffffffffu, ic, k);
-                        if (lane >= k) ic += t;
-                    }
-                    uint32_t running = f + ic - c;
-                    // this lane's escapes, exponents re-read kBatch at a time
-                    while (b0 | b1) {
-                        uint32_t offs_b[kBatch], ex[kBatch];
-                        int got = 0;
-#pragma unroll
-                        for (int t = 0; t < kBatch; t++) {
-                            offs_b[t] = 0;
-                            if (b0 | b1) {
-                                const bool lo_word = b0 != 0;
-                                const uint32_t bits = lo_word ? b0 : b1;
-                                const uint32_t pos = 64 * lane + (lo_word ? 0 : 32) + (__ffs(bits) - 1);
-                                if (lo_word) b0 &= b0 - 1;
-                                else b1 &= b1 - 1;
-                                offs_b[t] = (uint32_t)(ub + pos) - s;
-                                got = t + 1;
-                            }
-                        }
-#pragma unroll
-                        for (int t = 0; t < kBatch; t++) ex[t] = t < got ? (__ldg(p.in + s + offs_b[t]) >> 7) & 0xFF : 0;
-#pragma unroll
-                        for (int t = 0; t < kBatch; t++)
-                            if (t < got) put(offs_b[t], running++, offs_b[t] / C, ex[t]);
-                    }
-                }
-            }
-            if (staged) {
-                __syncwarp();
-                for (uint32_t b = lane; b < dbytes; b += 32) {
-                    if (dbase + b < p.cap) p.out[dbase + b] = stage[b];
-                    else overflow = true;
-                }
-                __syncwarp();  // the stage is reused by the next range
-            }
-        }
-        if (r + stride < p.ranges) load_range(p, r + stride, rl);
     }
-    if (overflow) atomicOr(&p.ws->flags, UZIP_FLAG_CAPACITY);
+    const uint32_t rtotal = carry;
+    if (lane == 0) s_cp[nq] = rtotal;
+    __syncwarp();
 
-    // The last CTA to finish writes the header.
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const unsigned prev = atomicAdd(&p.ws->done, 1u);
-        if (prev == gridDim.x - 1) {
-            __threadfence();
-            const uint64_t m = *reinterpret_cast<volatile unsigned long long*>(&p.ws->m);
-            const uint32_t flags = *reinterpret_cast<volatile unsigned int*>(&p.ws->flags);
-            write_header(p, m, flags);
+    uint8_t* offs = p.out + p.L.off_c;
+    for (uint32_t q = lane; q < nq; q += 32)
+        *reinterpret_cast<uint32_t*>(offs + 4ull * (c0 + q)) = pre + s_cp[q];
+    if (c0 + nq == p.L.nc && lane == 0) {  // the last range: tail, padding, header
+        const uint64_t m = (uint64_t)pre + rtotal;
+        *reinterpret_cast<uint32_t*>(offs + 4 * p.L.nc) = (uint32_t)m;
+        zero_words(p.out, p.L.off_c + 4 * (p.L.nc + 1), p.L.off_d);
+        const uint64_t groups_all = (p.n + 7) / 8;
+        zero_words(p.out, p.L.off_a + 8 * groups_all, p.L.off_b);
+        zero_words(p.out, p.L.off_b + 4 * groups_all, p.L.off_c);
+        // Escape bytes are written only below out_capacity; the stream is
+        // complete exactly when its total fits.
+        write_header(p, m, p.L.off_d + 3 * m > p.cap ? UZIP_FLAG_CAPACITY : 0u);
+    }
+    if (rtotal == 0) return;
+
+    // Pass 2: each escape's chunk-relative position and raw exponent. The
+    // range's escape blocks are contiguous in the stream: assemble them in
+    // this warp's stage and copy them out with coalesced stores, unless there
+    // are too many, then store them directly.
+    const uint64_t dbase = p.L.off_d + 3ull * pre;
+    const uint32_t dbytes = 3 * rtotal;
+    const bool staged = dbytes <= kStageBytes;
+    auto put = [&](uint32_t off, uint32_t rank_in_range, uint32_t q, uint32_t expo) {
+        const uint32_t cstart = s_cp[q];
+        const uint32_t k = s_cp[q + 1] - cstart;
+        const uint32_t rank = rank_in_range - cstart;
+        const uint32_t pos = off - q * C;
+        const uint32_t rel_pos = 3 * cstart + 2 * rank, rel_val = 3 * cstart + 2 * k + rank;
+        if (staged) {
+            stage[rel_pos] = (uint8_t)(pos & 0xFF);
+            stage[rel_pos + 1] = (uint8_t)(pos >> 8);
+            stage[rel_val] = (uint8_t)expo;
+        } else if (dbase + rel_val < p.cap && dbase + rel_pos + 1 < p.cap) {
+            p.out[dbase + rel_pos] = (uint8_t)(pos & 0xFF);
+            p.out[dbase + rel_pos + 1] = (uint8_t)(pos >> 8);
+            p.out[dbase + rel_val] = (uint8_t)expo;
         }
+    };
+#pragma unroll
+    for (int rr = 0; rr < kRounds; rr++) {
+        if (32 * rr + lane < nu && up[rr].list && n_in[rr]) {
+            const UnitPart& u = up[rr];
+            uint32_t running = first[rr];
+            uint32_t q = ((uint32_t)(u.ubase + u.plo) - s) / C;  // chunk of the part's first value
+            uint32_t next = (q + 1) * C;
+            for (uint32_t i = n_lo[rr]; i < n_lo[rr] + n_in[rr]; i++) {
+                const uint32_t ent = entry(rr, u.entries, i);
+                const uint32_t off = (uint32_t)(u.ubase + (ent & 0xFFFF)) - s;
+                while (off >= next) {
+                    q++;
+                    next += C;
+                }
+                put(off, running++, q, ent >> 16);
+            }
+        }
+        for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
+            const int o = __ffs(ovf) - 1;
+            uint64_t ub;
+            uint32_t plo, phi, b0, b1;
+            coop(rr, o, ub, plo, phi, b0, b1);
+            const uint32_t f = __shfl_sync(0xffffffffu, first[rr], o);
+            const uint32_t c = __popc(b0) + __popc(b1);
+            uint32_t ic = c;
+#pragma unroll
+            for (int k = 1; k < 32; k <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, ic, k);
+                if (lane >= k) ic += t;
+            }
+            uint32_t running = f + ic - c;
+            // this lane's escapes, exponents re-read kBatch at a time
+            while (b0 | b1) {
+                uint32_t offs_b[kBatch], ex[kBatch];
+                int got = 0;
+#pragma unroll
+                for (int t = 0; t < kBatch; t++) {
+                    offs_b[t] = 0;
+                    if (b0 | b1) {
+                        const bool lo_word = b0 != 0;
+                        const uint32_t bits = lo_word ? b0 : b1;
+                        const uint32_t pos = 64 * lane + (lo_word ? 0 : 32) + (__ffs(bits) - 1);
+                        if (lo_word) b0 &= b0 - 1;
+                        else b1 &= b1 - 1;
+                        offs_b[t] = (uint32_t)(ub + pos) - s;
+                        got = t + 1;
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < kBatch; t++) ex[t] = t < got ? (__ldg(p.in + s + offs_b[t]) >> 7) & 0xFF : 0;
+#pragma unroll
+                for (int t = 0; t < kBatch; t++)
+                    if (t < got) put(offs_b[t], running++, offs_b[t] / C, ex[t]);
+            }
+        }
+    }
+    if (staged) {
+        __syncwarp();
+        for (uint32_t b = lane; b < dbytes; b += 32)
+            if (dbase + b < p.cap) p.out[dbase + b] = stage[b];
+        __syncwarp();  // the stage is reused by the next range
+    }
+}
+
+template <int kRounds>
+__global__ void __launch_bounds__(kThreads, UZIP_ESC_MIN_BLOCKS) encode_escape_kernel(const Params p) {
+    extern __shared__ __align__(16) uint32_t s_dyn[];
+    __shared__ uint32_t s_red[kWarps];
+    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // Layout: per-warp escape staging | per-warp list heads | per-warp chunk tables.
+    uint8_t* stage = reinterpret_cast<uint8_t*>(s_dyn) + warp * kStageBytes;
+    uint32_t* s_head = s_dyn + kWarps * kStageBytes / 4 + warp * (kRounds * kHeadEntries * 32);
+    uint32_t* s_cp = s_dyn + kWarps * (kStageBytes / 4 + kRounds * kHeadEntries * 32) + warp * (p.range_chunks + 1);
+
+    wait_for_prerequisite();  // the dense kernel's stream and workspace are complete past this point
+
+    const uint64_t stride = (uint64_t)gridDim.x * kWarps;
+    for (uint64_t rb = (uint64_t)blockIdx.x * kWarps; rb < p.ranges; rb += stride) {
+        // Ranges rb .. rb + 7, one per warp, in ascending order. The block's
+        // base: escapes of the segments before the one holding range rb's
+        // first unit (a block-wide sum of at most kMaxSegments totals).
+        const uint64_t r = rb + warp;
+        const bool active = r < p.ranges;
+        const uint32_t seg_first = (uint32_t)(rb * p.range_chunks * p.chunk / kUnit) / p.seg_units;
+        RangeLoads<kRounds> rl;
+        if (active) load_range(p, r, seg_first, rl);
+        uint32_t v = 0;
+#pragma unroll
+        for (int k = 0; k < (int)(kMaxSegments / kThreads); k++) {
+            const uint32_t i = tid + k * kThreads;
+            if (i < seg_first) v += __ldg(p.segs + i);
+        }
+        v = warp_sum(v);
+        __syncthreads();  // the previous round's totals are read
+        if (lane == 0) s_red[warp] = v;
+        __syncthreads();
+        uint32_t base = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; w++) base += s_red[w];
+        if (active) escape_range<kRounds>(p, rl, base, stage, s_head, s_cp);
     }
 }
 
@@ -661,10 +659,50 @@ using namespace uzip;
 
 extern "C" UZIP_API size_t uzip_encode_workspace_bytes(size_t n, uint32_t chunk) {
     if (!chunk_valid(chunk) || n > UZIP_MAX_N) return 0;
-    return (size_t)geometry_of(n, chunk).bytes;
+    return (size_t)geometry_of(n).bytes;
 }
 
 namespace uzip {
+namespace {
+
+// Per-device launch facts, looked up on the first call on each device (the
+// results are the same whichever thread gets there first).
+struct DeviceFacts {
+    int sms, per_sm1, per_sm2[2];
+};
+constexpr int kMaxFactDevices = 64;
+std::atomic<int> g_facts_ready[kMaxFactDevices];
+DeviceFacts g_facts[kMaxFactDevices];
+
+size_t escape_smem(uint32_t range_chunks, int rounds) {
+    return (size_t)kWarps * (kStageBytes + 4ull * rounds * kHeadEntries * 32 + 4ull * (range_chunks + 1));
+}
+
+int device_facts(DeviceFacts& f) {
+    int dev = 0;
+    UZIP_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < kMaxFactDevices && g_facts_ready[dev].load(std::memory_order_acquire)) {
+        f = g_facts[dev];
+        return UZIP_OK;
+    }
+    UZIP_CUDA_TRY(cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev));
+    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm1, encode_dense_kernel, kThreads, 0));
+    void (*esc[2])(Params) = {encode_escape_kernel<1>, encode_escape_kernel<2>};
+    for (int k = 0; k < 2; k++) {
+        const size_t smem_max = escape_smem(kMaxRangeChunks, k + 1);
+        if (smem_max > 48 * 1024)
+            UZIP_CUDA_TRY(cudaFuncSetAttribute(esc[k], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max));
+        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm2[k], esc[k], kThreads, smem_max));
+    }
+    if (f.sms < 1 || f.per_sm1 < 1 || f.per_sm2[0] < 1 || f.per_sm2[1] < 1) return UZIP_ERR_CUDA;
+    if (dev < kMaxFactDevices) {
+        g_facts[dev] = f;
+        g_facts_ready[dev].store(1, std::memory_order_release);
+    }
+    return UZIP_OK;
+}
+
+}  // namespace
 
 int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_codebook, void* d_out,
                 size_t out_capacity, void* d_workspace, size_t workspace_bytes, size_t* h_out_bytes,
@@ -676,7 +714,7 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         return UZIP_ERR_ALIGN;
     const Layout L = layout_of(n, chunk);
     if (out_capacity < L.off_d) return UZIP_ERR_CAPACITY;
-    const Geometry g = geometry_of(n, chunk);
+    const Geometry g = geometry_of(n);
     if (workspace_bytes < g.bytes) return UZIP_ERR_CAPACITY;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -685,14 +723,13 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
     p.in = static_cast<const uint16_t*>(d_in_bf16);
     p.n = n;
     p.chunk = chunk;
-    p.seg_units = g.seg_units;
-    p.nseg = g.nseg;
     p.units = g.units;
     p.cb = static_cast<const uint8_t*>(d_codebook);
     p.out = static_cast<uint8_t*>(d_out);
     p.cap = out_capacity;
     p.L = L;
-    p.ws = reinterpret_cast<WsHeader*>(ws);
+    p.seg_units = g.seg_units;
+    p.nseg = g.nseg;
     p.segs = reinterpret_cast<uint32_t*>(ws + g.off_segs);
     p.counts = reinterpret_cast<uint32_t*>(ws + g.off_counts);
     p.lists = reinterpret_cast<uint32_t*>(ws + g.off_lists);
@@ -702,34 +739,36 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         encode_empty_kernel<<<1, 1, 0, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
     } else {
-        int dev = 0, sms = 0, per_sm1 = 0, per_sm2 = 0;
-        UZIP_CUDA_TRY(cudaGetDevice(&dev));
-        UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        const size_t smem2_max = (size_t)kWarps * kStageBytes +
-                                 4 * (((size_t)g.nseg + 1 + 3) / 4 * 4 + (size_t)kWarps * (kMaxRangeChunks + 1));
-        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm1, encode_dense_kernel, kThreads, 0));
-        const bool two_rounds = chunk > 32 * kUnit - 2040 && chunk % kUnit != 0;
-        auto* esc_kernel = two_rounds ? encode_escape_kernel<2> : encode_escape_kernel<1>;
-        if (smem2_max > 48 * 1024)
-            UZIP_CUDA_TRY(cudaFuncSetAttribute(esc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2_max));
-        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm2, esc_kernel, kThreads, smem2_max));
-        if (per_sm1 < 1 || per_sm2 < 1) return UZIP_ERR_CUDA;
-        // Escape-kernel ranges: whole chunks, sized so every resident warp
+        DeviceFacts f;
+        const int rc = device_facts(f);
+        if (rc != UZIP_OK) return rc;
+        // Dense kernel: one resident wave.
+        const uint64_t grid1 = std::min<uint64_t>((g.units + kWarps - 1) / kWarps, (uint64_t)f.sms * f.per_sm1);
+        // Escape kernel: ranges of whole chunks, sized so every resident warp
         // gets at most one (the per-range cost is mostly load latency).
-        const uint64_t warps2 = (uint64_t)sms * per_sm2 * kWarps;
+        const int two_rounds = chunk > 32 * kUnit - 2040 && chunk % kUnit != 0;
+        const uint64_t warps2 = (uint64_t)f.sms * f.per_sm2[two_rounds] * kWarps;
         const uint32_t rc_max =
             std::max<uint32_t>(1, std::min<uint32_t>(kMaxRangeChunks, kMaxRangeUnits * kUnit / chunk));
         p.range_chunks = (uint32_t)std::min<uint64_t>(rc_max, std::max<uint64_t>(1, (L.nc + warps2 - 1) / warps2));
         p.ranges = (L.nc + p.range_chunks - 1) / p.range_chunks;
-        const size_t smem2 = (size_t)kWarps * kStageBytes +
-                             4 * (((size_t)g.nseg + 1 + 3) / 4 * 4 + (size_t)kWarps * (p.range_chunks + 1));
-        const uint64_t grid1 = std::min<uint64_t>((g.units + kWarps - 1) / kWarps, (uint64_t)sms * per_sm1);
-        const uint64_t grid2 = std::min<uint64_t>((p.ranges + kWarps - 1) / kWarps, (uint64_t)sms * per_sm2);
-        UZIP_CUDA_TRY(cudaMemsetAsync(ws, 0, g.off_counts, s));  // header + segment totals
+        const uint64_t grid2 = std::min<uint64_t>((p.ranges + kWarps - 1) / kWarps, (uint64_t)f.sms * f.per_sm2[two_rounds]);
+
+        UZIP_CUDA_TRY(cudaMemsetAsync(p.segs, 0, 4ull * g.nseg, s));  // segment totals
         encode_dense_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
-        esc_kernel<<<(unsigned)grid2, kThreads, smem2, s>>>(p);
-        UZIP_CUDA_TRY(cudaGetLastError());
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid2);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = escape_smem(p.range_chunks, two_rounds + 1);
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        UZIP_CUDA_TRY(two_rounds ? cudaLaunchKernelEx(&cfg, encode_escape_kernel<2>, p)
+                                 : cudaLaunchKernelEx(&cfg, encode_escape_kernel<1>, p));
     }
     if (h_out_bytes) {
         uint32_t hdr[16];
@@ -767,18 +806,9 @@ extern "C" UZIP_API int uzip_encode(const void* d_in_bf16, size_t n, uint32_t ch
 namespace uzip {
 namespace {
 
-constexpr uint64_t cpad16(uint64_t v) { return (v + 15) / 16 * 16; }
-
 // Workspace bytes the encoder needs for n values (the geometry above, which
 // depends on n only).
-constexpr uint64_t workspace_bytes_for(uint64_t n) {
-    const uint64_t units = (n + kUnit - 1) / kUnit;
-    uint64_t seg_units = 64;
-    while ((units + seg_units - 1) / seg_units > kMaxSegments) seg_units *= 2;
-    const uint64_t nseg = (units + seg_units - 1) / seg_units;
-    return sizeof(WsHeader) + cpad16(4 * nseg) + cpad16(4 * units) + 4ull * kListCap * units +
-           (uint64_t)kUnitGroups * units;
-}
+constexpr uint64_t workspace_bytes_for(uint64_t n) { return geometry_of(n).bytes; }
 
 constexpr uint64_t kNoAllocScratchBytes = workspace_bytes_for(UZIP_NOALLOC_MAX_N);
 
@@ -795,7 +825,7 @@ extern "C" UZIP_API int uzip_encode_noalloc(const void* d_in_bf16, size_t n, uin
                                             size_t* h_out_bytes, uzip_stream_t stream) {
     if (n > UZIP_NOALLOC_MAX_N) return UZIP_ERR_CAPACITY;  // beyond the built-in scratch
     if (!chunk_valid(chunk)) return UZIP_ERR_CHUNK;
-    const uint64_t need = geometry_of(n, chunk).bytes;
+    const uint64_t need = geometry_of(n).bytes;
     if (need > kNoAllocScratchBytes) return UZIP_ERR_CAPACITY;
     int dev = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
