@@ -36,6 +36,10 @@ METRIC = "encode/decode GB/s (raw BF16 bytes) @256M elems; ratio; % of HBM peak"
 WORKLOAD = "kv_cache [64,2,8,2048,128] bf16 = 268,435,456 values, chunk 1024, calibration sample 1 Mi values"
 CHUNK = 1024
 FALLBACK_HBM_GBS = 6800.0
+# Kernels one step launches: calibrate (histogram, Top-16 selection), encode
+# (dense pass, escape pass), decode (one kernel). The two clears of small
+# device arrays (histogram bins, segment totals) are driver memsets.
+KERNELS_PER_STEP = 5
 
 
 # ------------------------------------------------------------- distributed
@@ -341,7 +345,7 @@ def report(args, ws, rank, n, raw, nbytes, m, max_ms, total_raw, cal_ms, enc_ms,
                      "algorithmic_bytes": enc_bytes if dominant == "encode" else dec_bytes},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
         "clocks": clocks,
     }
     return line
