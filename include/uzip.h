@@ -129,15 +129,17 @@ UZIP_API int uzip_codebook_from_exps(const uint8_t *h_exps16, void *d_codebook,
  * chunk, n > UZIP_MAX_N or n_escapes > n. Host only. */
 UZIP_API size_t uzip_compressed_size(size_t n, size_t n_escapes, uint32_t chunk);
 
-/* Device workspace bytes uzip_encode needs for (n, chunk): about n/8 + 64
- * (escape masks, per-2048-value escape counts, segment totals); 0 for an
- * invalid chunk or n. Host only. */
+/* Device workspace bytes uzip_encode needs for (n, chunk): about n/4 bytes
+ * (per 2048 values: an escape count, a list of up to 64 escape entries and
+ * 256 escape-mask bytes; plus one total per segment of 64 or more such units);
+ * 0 for an invalid chunk or n. Host only. */
 UZIP_API size_t uzip_encode_workspace_bytes(size_t n, uint32_t chunk);
 
 /* Encode n BF16 values (§3.2), reading the input from HBM once: a dense kernel
- * (sign-mantissa bytes, packed codes, escape masks and counts) and an escape
- * kernel (chunk offsets from the escape-count prefix, escape blocks in
- * ascending element order).
+ * (sign-mantissa bytes, packed codes, per-unit escape lists and counts) and an
+ * escape kernel (chunk offsets from the escape-count prefix, escape blocks in
+ * ascending element order, header). Each call launches a small memset and the
+ * two kernels on `stream`.
  *   d_in_bf16      n BF16 values (may be NULL when n == 0).
  *   chunk          escape-position chunk, a multiple of 8 in [8, 65536].
  *   d_codebook     from uzip_calibrate / uzip_codebook_from_exps.
@@ -147,8 +149,10 @@ UZIP_API size_t uzip_encode_workspace_bytes(size_t n, uint32_t chunk);
  *                  never overflow. If the escapes do not fit, the kernel writes
  *                  none past out_capacity and sets UZIP_FLAG_CAPACITY in the
  *                  header.
- *   d_workspace    at least uzip_encode_workspace_bytes(n, chunk) bytes; cleared
- *                  by the call; must not be shared with a concurrent call.
+ *   d_workspace    at least uzip_encode_workspace_bytes(n, chunk) bytes, 16-byte
+ *                  aligned, any contents (the call clears what it accumulates
+ *                  into and writes everything else before reading it); must not
+ *                  be shared with a call that may overlap on the GPU.
  *   h_out_bytes    NULL: fully asynchronous; read the total from the header.
  *                  Non-NULL: the call synchronises `stream`, stores the exact
  *                  stream size and returns UZIP_ERR_CAPACITY if the kernels
