@@ -99,7 +99,8 @@ enum uzip_status {
  *   (code -> exponent, equal to exps) | [48,304) u8 encode table
  *   (exponent -> code, 0 for an escape) | [304,560) u8 escape table
  *   (exponent -> 1 if not in the Top-16) | [1024,3072) u64 histogram[256] of
- *   the calibration sample (zero for uzip_codebook_from_exps). */
+ *   the calibration sample (zero for uzip_codebook_from_exps) | [3072,3088)
+ *   working space of uzip_calibrate, zero when it has finished. */
 #define UZIP_CB_EXPS 16
 #define UZIP_CB_DEC 32
 #define UZIP_CB_ENC 48

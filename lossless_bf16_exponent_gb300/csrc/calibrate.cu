@@ -6,15 +6,18 @@
 // §3.4: all 16 codes are real exponents; an escape gets a dummy code (0 here).
 //
 // Kernels:
-//   hist256_kernel  grid-stride over the sample with 16-byte loads; one
-//                   256-bin shared-memory histogram per warp; equal exponents
-//                   inside a warp are merged with __match_any_sync so a
-//                   concentrated distribution does not serialise on one bin;
-//                   per-block totals go to the blob's u64 histogram.
-//   top16_kernel    one CTA: thread j ranks bin j against all 256 counts
-//                   (count descending, exponent ascending) and the 16 lowest
-//                   ranks become the codebook; then the three tables.
-//   luts_kernel     same tables from 16 caller-given exponents.
+//   calibrate_kernel  one CTA per SM at most: every thread issues its 16-byte
+//                     loads of the sample first, then counts; one 256-bin
+//                     shared-memory histogram per warp, where equal exponents
+//                     inside a warp are merged with __match_any_sync so a
+//                     concentrated distribution does not serialise on one bin;
+//                     per-block totals are added to the blob's u64 histogram.
+//                     The last block to finish (a fence and a counter, no
+//                     waiting) ranks the 256 bins -- thread j ranks bin j
+//                     against all counts (count descending, exponent
+//                     ascending) -- and the 16 lowest ranks become the
+//                     codebook; then it writes the three tables.
+//   luts_kernel       the same tables from 16 caller-given exponents.
 #include "uzip_internal.cuh"
 
 namespace uzip {
@@ -30,27 +33,47 @@ __device__ __forceinline__ void warp_hist_add(uint32_t* h, uint32_t e, bool vali
     if (valid && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&h[e], __popc(peers));
 }
 
-__global__ void __launch_bounds__(kHistThreads) hist256_kernel(const uint16_t* __restrict__ x, uint64_t n,
-                                                               unsigned long long* __restrict__ hist) {
+constexpr int kLoadsPerThread = 4;  // 16-byte loads in flight per thread
+
+// Block-done counter of calibrate_kernel, in the blob's reserved bytes after
+// the histogram; cleared with the histogram before each launch.
+constexpr uint32_t kCbCounter = UZIP_CB_HIST + 256 * 8;
+
+__device__ void rank_and_write(uint8_t* cb, uint64_t n_sample);
+
+__global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const uint16_t* __restrict__ x, uint64_t n,
+                                                                 uint8_t* __restrict__ cb) {
     __shared__ uint32_t sh[kHistWarps][256];
+    __shared__ bool s_last;
+    unsigned long long* hist = reinterpret_cast<unsigned long long*>(cb + UZIP_CB_HIST);
+    unsigned int* counter = reinterpret_cast<unsigned int*>(cb + kCbCounter);
     for (int i = threadIdx.x; i < kHistWarps * 256; i += kHistThreads) (&sh[0][0])[i] = 0;
     __syncthreads();
     uint32_t* h = sh[threadIdx.x / 32];
 
     const uint64_t groups = n / 8;
-    const uint64_t stride = (uint64_t)gridDim.x * kHistThreads;
-    // Warp-uniform trip count so __match_any_sync always sees the full warp.
-    const uint64_t warp_first = (uint64_t)blockIdx.x * kHistThreads + (threadIdx.x & ~31u);
-    for (uint64_t wg = warp_first; wg < groups; wg += stride) {
-        const uint64_t g = wg + (threadIdx.x & 31);
-        const bool valid = g < groups;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (valid) v = ld_stream_v4(x + 8 * g);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const uint64_t stride = (uint64_t)gridDim.x * kHistThreads * kLoadsPerThread;
+    // Group g of a round is lane + 32 * (warp + kHistWarps * (j + kLoadsPerThread * block)); the
+    // trip count is warp-uniform so __match_any_sync always sees the full warp.
+    const uint64_t first =
+        ((uint64_t)blockIdx.x * kLoadsPerThread * kHistWarps + threadIdx.x / 32) * 32 + (threadIdx.x & 31);
+    for (uint64_t base = 0; base < groups; base += stride) {
+        uint4 v[kLoadsPerThread];
+        bool valid[kLoadsPerThread];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            warp_hist_add(h, (w[q] >> 7) & 0xFF, valid);
-            warp_hist_add(h, (w[q] >> 23) & 0xFF, valid);
+        for (int j = 0; j < kLoadsPerThread; j++) {
+            const uint64_t g = base + first + (uint64_t)j * kHistThreads;
+            valid[j] = g < groups;
+            v[j] = valid[j] ? ld_stream_v4(x + 8 * g) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < kLoadsPerThread; j++) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                warp_hist_add(h, (w[q] >> 7) & 0xFF, valid[j]);
+                warp_hist_add(h, (w[q] >> 23) & 0xFF, valid[j]);
+            }
         }
     }
     // Ragged tail (< 8 values): block 0's first warp.
@@ -66,6 +89,15 @@ __global__ void __launch_bounds__(kHistThreads) hist256_kernel(const uint16_t* _
         for (int w = 0; w < kHistWarps; w++) s += sh[w][b];
         if (s) atomicAdd(&hist[b], (unsigned long long)s);
     }
+    // The last block ranks the totals.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(counter, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    rank_and_write(cb, n);
+    if (threadIdx.x == 0) *counter = 0;
 }
 
 // Tables from exps[16] (shared memory), written by a 256-thread CTA.
@@ -91,15 +123,18 @@ __device__ void write_tables(const uint8_t* exps, uint8_t* cb, uint64_t n_sample
     }
 }
 
-__global__ void __launch_bounds__(256) top16_kernel(uint8_t* __restrict__ cb, uint64_t n_sample) {
+// Rank the blob's 256 totals (count descending, exponent ascending) and write
+// the codebook; one 256-thread CTA, totals read from L2.
+__device__ void rank_and_write(uint8_t* cb, uint64_t n_sample) {
     __shared__ unsigned long long cnt[256];
     __shared__ uint8_t exps[16];
     const int t = threadIdx.x;
     const unsigned long long* hist = reinterpret_cast<const unsigned long long*>(cb + UZIP_CB_HIST);
-    cnt[t] = hist[t];
+    cnt[t] = __ldcg(hist + t);
     __syncthreads();
     const unsigned long long mine = cnt[t];
     int rank = 0;
+#pragma unroll 8
     for (int i = 0; i < 256; i++) {
         const unsigned long long c = cnt[i];
         rank += (c > mine) || (c == mine && i < t);
@@ -133,22 +168,17 @@ extern "C" UZIP_API int uzip_calibrate(const void* d_sample_bf16, size_t n_sampl
     if (!aligned16(d_codebook) || (n_sample > 0 && !aligned16(d_sample_bf16))) return UZIP_ERR_ALIGN;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* cb = static_cast<uint8_t*>(d_codebook);
-    UZIP_CUDA_TRY(cudaMemsetAsync(cb + UZIP_CB_HIST, 0, 256 * sizeof(unsigned long long), s));
-    if (n_sample > 0) {
-        int dev = 0, sms = 0;
-        UZIP_CUDA_TRY(cudaGetDevice(&dev));
-        UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        const uint64_t groups = n_sample / 8;
-        uint64_t blocks = (groups + kHistThreads - 1) / kHistThreads;
-        const uint64_t cap = (uint64_t)sms * 4;
-        if (blocks > cap) blocks = cap;
-        if (blocks == 0) blocks = 1;
-        hist256_kernel<<<(unsigned)blocks, kHistThreads, 0, s>>>(
-            static_cast<const uint16_t*>(d_sample_bf16), n_sample,
-            reinterpret_cast<unsigned long long*>(cb + UZIP_CB_HIST));
-        UZIP_CUDA_TRY(cudaGetLastError());
-    }
-    top16_kernel<<<1, 256, 0, s>>>(cb, n_sample);
+    // Histogram totals and the block counter start at zero.
+    UZIP_CUDA_TRY(cudaMemsetAsync(cb + UZIP_CB_HIST, 0, kCbCounter + 16 - UZIP_CB_HIST, s));
+    int dev = 0, sms = 0;
+    UZIP_CUDA_TRY(cudaGetDevice(&dev));
+    UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const uint64_t per_block = (uint64_t)kHistThreads * kLoadsPerThread;
+    uint64_t blocks = (n_sample / 8 + per_block - 1) / per_block;
+    if (blocks > (uint64_t)sms) blocks = sms;
+    if (blocks == 0) blocks = 1;
+    calibrate_kernel<<<(unsigned)blocks, kHistThreads, 0, s>>>(static_cast<const uint16_t*>(d_sample_bf16),
+                                                                n_sample, cb);
     UZIP_CUDA_TRY(cudaGetLastError());
     return UZIP_OK;
 }
