@@ -189,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
 
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t stride = (uint64_t)gridDim.x * kWarps;
+    const uint64_t keep = l2_policy_evict_last();  // counts, lists, masks: read by the escape kernel
     for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride) {
         const uint64_t ubase = u * kUnit;
         const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
                     for (uint32_t bits = mask; bits; bits &= bits - 1, j++) {
                         const uint32_t b = __ffs(bits) - 1;
                         const uint32_t e = ((b < 4 ? e_lo : e_hi) >> (8 * (b & 3))) & 0xFF;
-                        if (j < kListCap) list[j] = (8 * g + b) | (e << 16);
+                        if (j < kListCap) st_u32_keep(list + j, (8 * g + b) | (e << 16), keep);
                     }
                     cnt += total;
                     mbytes[it] |= mask << (8 * r);
@@ -271,10 +272,10 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
 #pragma unroll
             for (int it = 0; it < 2; it++)
 #pragma unroll
-                for (int r = 0; r < 4; r++) gmask[it * 128 + r * 32 + lane] = (uint8_t)(mbytes[it] >> (8 * r));
+                for (int r = 0; r < 4; r++) st_u8_keep(gmask + it * 128 + r * 32 + lane, (mbytes[it] >> (8 * r)) & 0xFF, keep);
         }
         if (lane == 0) {
-            p.counts[u] = cnt;
+            st_u32_keep(p.counts + u, cnt, keep);
             if (cnt) atomicAdd(&p.segs[u / p.seg_units], cnt);
         }
     }

@@ -74,6 +74,21 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return v;
 }
 
+// L2 eviction priority (PTX createpolicy): data a later kernel of the same
+// call reads back is stored with evict_last so the streamed tensor does not
+// push it out of L2 first.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_u32_keep(void* p, uint32_t v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_u8_keep(void* p, uint32_t v, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.u8 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+
 }  // namespace uzip
 
 #define UZIP_CUDA_TRY(expr)                          \
