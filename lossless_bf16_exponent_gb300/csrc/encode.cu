@@ -55,6 +55,8 @@ constexpr uint32_t kMaxRangeUnits = 31;       // a range covers at most 31 units
 constexpr uint32_t kStageBytes = 4096;        // per-warp staging of a range's escape blocks
 constexpr uint32_t kMaxRangeChunks = 256;     // bounds the per-warp chunk table
 constexpr int kBatch = 8;                     // escape exponents re-read at once (mask units)
+constexpr uint32_t kParallelAbove = 32;       // pass 2 goes escape-parallel when a unit has more escapes
+                                              // (below, one lane per unit walking its list measured faster)
 #ifndef UZIP_ENC_MIN_BLOCKS
 #define UZIP_ENC_MIN_BLOCKS 4
 #endif
@@ -99,6 +101,7 @@ struct Params {
     uint32_t seg_units;   // units per segment
     uint32_t nseg;        // segments
     uint32_t range_chunks;
+    uint32_t chunk_shift;  // log2(chunk) when chunk is a power of two, else 32
     uint64_t units;
     uint64_t ranges;
     const uint8_t* cb;
@@ -177,6 +180,11 @@ __device__ void zero_words(uint8_t* out, uint64_t from, uint64_t to) {
 }
 
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) { return __reduce_add_sync(0xffffffffu, v); }
+
+// x / chunk (a shift for the power-of-two chunk sizes).
+__device__ __forceinline__ uint32_t div_chunk(const Params& p, uint32_t x) {
+    return p.chunk_shift < 32 ? x >> p.chunk_shift : x / p.chunk;
+}
 
 // ------------------------------------------------------------ dense kernel
 
@@ -287,11 +295,10 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
 // unit's sorted list, or (a unit that overflowed its list) from its mask bytes
 // with exponents re-read from the input.
 struct UnitPart {
-    uint64_t ubase;  // first value of the unit
+    uint32_t ubase;  // first value of the unit (n < 2^32)
     uint32_t cnt;    // all escapes of the unit
     uint32_t plo, phi;
     bool list;
-    const uint32_t* entries;
 };
 
 // Bits of mask word w (unit positions 32 w ..) that lie in [lo, hi).
@@ -306,7 +313,7 @@ __device__ __forceinline__ uint32_t bits_in(uint32_t word, uint32_t w, uint32_t 
 // per lane and round) its count and first kHeadEntries list entries; the
 // counts of the earlier units of u0's segment; the segment totals between the
 // block's base segment and u0's segment.
-constexpr int kPreLoads = 8;  // earlier-unit counts per lane, loaded up front (segments up to 256 units)
+constexpr int kPreLoads = 2;  // earlier-unit counts per lane, loaded up front (segments of 64 units)
 
 // kRounds = 1 when every range overlaps at most 32 units (one per lane); 2 for
 // the chunk sizes whose single chunk can overlap 33 units (longer than
@@ -315,13 +322,16 @@ template <int kRounds>
 struct RangeLoads {
     uint32_t c0, nq, s, e, u0, nu, seg;
     uint32_t cnt[kRounds];
-    uint4 h0[kRounds], h1[kRounds];
     uint32_t pre_cnt[kPreLoads];
     uint32_t mid;
 };
 
+// Non-binding prefetch of a global line into L1.
+__device__ __forceinline__ void prefetch_l1(const void* ptr) { asm volatile("prefetch.global.L1 [%0];" ::"l"(ptr)); }
+
 template <int kRounds>
-__device__ __forceinline__ void load_range(const Params& p, uint64_t r, uint32_t seg_first, RangeLoads<kRounds>& rl) {
+__device__ __forceinline__ void load_range(const Params& p, uint64_t r, uint32_t seg_first, RangeLoads<kRounds>& rl,
+                                           uint32_t* s_head) {
     const uint32_t lane = threadIdx.x & 31;
     const uint32_t C = p.chunk;
     rl.c0 = (uint32_t)(r * p.range_chunks);
@@ -336,10 +346,14 @@ __device__ __forceinline__ void load_range(const Params& p, uint64_t r, uint32_t
     for (int rr = 0; rr < kRounds; rr++) {
         const uint32_t u = rl.u0 + 32 * rr + lane;
         const bool on = 32 * rr + lane < rl.nu;
-        const uint4* head = reinterpret_cast<const uint4*>(p.lists + (uint64_t)u * kListCap);
         rl.cnt[rr] = on ? __ldg(p.counts + u) : 0;
-        rl.h0[rr] = on ? __ldg(head) : make_uint4(0, 0, 0, 0);
-        rl.h1[rr] = on ? __ldg(head + 1) : make_uint4(0, 0, 0, 0);
+        if (on) {  // the unit's first list entries -> shared memory, [round][entry][lane]
+            const uint4* head = reinterpret_cast<const uint4*>(p.lists + (uint64_t)u * kListCap);
+            const uint4 h0 = __ldg(head), h1 = __ldg(head + 1);
+            const uint32_t q[kHeadEntries] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+            for (int j = 0; j < (int)kHeadEntries; j++) s_head[(rr * kHeadEntries + j) * 32 + lane] = q[j];
+        }
     }
     const uint32_t first = rl.seg * p.seg_units;
 #pragma unroll
@@ -362,17 +376,18 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
     const uint32_t C = p.chunk;
     const uint32_t c0 = rl.c0, nq = rl.nq, s = rl.s, e = rl.e, u0 = rl.u0, nu = rl.nu, seg = rl.seg;
 
-    // Each lane keeps its units' first list entries in shared memory,
-    // [round][entry][lane] (a lane only reads its own column).
+    // The units' first list entries are in s_head, [round][entry][lane]; the
+    // rest of a longer list is prefetched into L1 now, ahead of its use.
+    __syncwarp();
 #pragma unroll
     for (int rr = 0; rr < kRounds; rr++) {
-        const uint32_t q[kHeadEntries] = {rl.h0[rr].x, rl.h0[rr].y, rl.h0[rr].z, rl.h0[rr].w,
-                                          rl.h1[rr].x, rl.h1[rr].y, rl.h1[rr].z, rl.h1[rr].w};
-#pragma unroll
-        for (int j = 0; j < (int)kHeadEntries; j++) s_head[(rr * kHeadEntries + j) * 32 + lane] = q[j];
+        const uint32_t c = min(rl.cnt[rr], kListCap);
+        const uint32_t* list = p.lists + (uint64_t)(u0 + 32 * rr + lane) * kListCap;
+        for (uint32_t j = kHeadEntries; j < c; j += 32) prefetch_l1(list + j);  // 128-byte lines
     }
-    auto entry = [&](int rr, const uint32_t* entries, uint32_t j) -> uint32_t {
-        return j < kHeadEntries ? s_head[(rr * kHeadEntries + j) * 32 + lane] : __ldg(entries + j);
+    auto entry = [&](int rr, uint32_t ubase, uint32_t j) -> uint32_t {
+        return j < kHeadEntries ? s_head[(rr * kHeadEntries + j) * 32 + lane]
+                                : __ldg(p.lists + (uint64_t)(ubase / kUnit) * kListCap + j);
     };
 
     UnitPart up[kRounds];
@@ -384,19 +399,18 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
         if (32 * rr + lane < nu) {
             UnitPart& u = up[rr];
             const uint32_t uidx = u0 + 32 * rr + lane;
-            u.ubase = (uint64_t)uidx * kUnit;
+            u.ubase = uidx * kUnit;
             u.cnt = rl.cnt[rr];
-            u.plo = s > u.ubase ? (uint32_t)(s - u.ubase) : 0u;
-            u.phi = (uint32_t)min((uint64_t)kUnit, (uint64_t)e - u.ubase);
+            u.plo = s > u.ubase ? s - u.ubase : 0u;
+            u.phi = min(kUnit, e - u.ubase);
             u.list = u.cnt <= kListCap;
-            u.entries = p.lists + (uint64_t)uidx * kListCap;
             if (u.list) {
                 const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - u.ubase);
                 if (u.plo == 0 && u.phi >= ulen) {
                     n_in[rr] = u.cnt;  // the whole unit lies in the range
                 } else {
                     for (uint32_t j = 0; j < u.cnt; j++) {
-                        const uint32_t pos = entry(rr, u.entries, j) & 0xFFFF;
+                        const uint32_t pos = entry(rr, u.ubase, j) & 0xFFFF;
                         n_lo[rr] += pos < u.plo;
                         n_in[rr] += pos >= u.plo && pos < u.phi;
                     }
@@ -407,8 +421,7 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
     // Units that overflowed their list are handled by the whole warp: lane
     // l takes mask words 2l and 2l+1 (unit positions 64l .. 64l+63).
     auto coop = [&](int rr, int o, uint64_t& ub, uint32_t& plo, uint32_t& phi, uint32_t& b0, uint32_t& b1) {
-        ub = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(up[rr].ubase >> 32), o) << 32) |
-             __shfl_sync(0xffffffffu, (uint32_t)up[rr].ubase, o);
+        ub = __shfl_sync(0xffffffffu, up[rr].ubase, o);
         plo = __shfl_sync(0xffffffffu, up[rr].plo, o);
         phi = __shfl_sync(0xffffffffu, up[rr].phi, o);
         const uint2 w = __ldg(reinterpret_cast<const uint2*>(p.masks + (ub / kUnit) * kUnitGroups) + lane);
@@ -458,13 +471,13 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
         carry += __shfl_sync(0xffffffffu, incl, 31);
         if (32 * rr + lane < nu && up[rr].list) {
             const UnitPart& u = up[rr];
-            const uint32_t v_lo = (uint32_t)(u.ubase + u.plo) - s;  // range offset of plo
-            uint32_t q = (v_lo + C - 1) / C;
-            uint32_t x = (uint32_t)(s + q * C - u.ubase);  // unit position of chunk q's start
+            const uint32_t v_lo = u.ubase + u.plo - s;  // range offset of plo
+            uint32_t q = div_chunk(p, v_lo + C - 1);
+            uint32_t x = s + q * C - u.ubase;  // unit position of chunk q's start
             uint32_t i = n_lo[rr];
             const uint32_t iend = n_lo[rr] + n_in[rr];
             while (q < nq && x < u.phi) {
-                while (i < iend && (entry(rr, u.entries, i) & 0xFFFF) < x) i++;
+                while (i < iend && (entry(rr, u.ubase, i) & 0xFFFF) < x) i++;
                 s_cp[q] = first[rr] + (i - n_lo[rr]);
                 q++;
                 x += C;
@@ -487,7 +500,7 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
             const uint32_t lo = max(64 * lane, plo), hi = min(64 * lane + 64, phi);
             if (lo < hi) {
                 const uint32_t v_lo = (uint32_t)(ub + lo) - s;
-                uint32_t q = (v_lo + C - 1) / C;
+                uint32_t q = div_chunk(p, v_lo + C - 1);
                 uint32_t x = (uint32_t)(s + q * C - ub);
                 while (q < nq && x < hi) {
                     const uint32_t d = x - 64 * lane;  // 0..63
@@ -522,11 +535,14 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
 
     // Pass 2: each escape's chunk-relative position and raw exponent. The
     // range's escape blocks are contiguous in the stream: assemble them in
-    // this warp's stage and copy them out with coalesced stores, unless there
-    // are too many, then store them directly.
+    // this warp's stage -- shifted by the destination's offset within a
+    // 4-byte word, so whole words can be copied out -- and store them with
+    // coalesced word stores, unless there are too many, then store them
+    // directly.
     const uint64_t dbase = p.L.off_d + 3ull * pre;
     const uint32_t dbytes = 3 * rtotal;
-    const bool staged = dbytes <= kStageBytes;
+    const uint32_t lead = (uint32_t)(dbase & 3);
+    const bool staged = lead + dbytes <= kStageBytes;
     auto put = [&](uint32_t off, uint32_t rank_in_range, uint32_t q, uint32_t expo) {
         const uint32_t cstart = s_cp[q];
         const uint32_t k = s_cp[q + 1] - cstart;
@@ -534,32 +550,63 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
         const uint32_t pos = off - q * C;
         const uint32_t rel_pos = 3 * cstart + 2 * rank, rel_val = 3 * cstart + 2 * k + rank;
         if (staged) {
-            stage[rel_pos] = (uint8_t)(pos & 0xFF);
-            stage[rel_pos + 1] = (uint8_t)(pos >> 8);
-            stage[rel_val] = (uint8_t)expo;
+            stage[lead + rel_pos] = (uint8_t)(pos & 0xFF);
+            stage[lead + rel_pos + 1] = (uint8_t)(pos >> 8);
+            stage[lead + rel_val] = (uint8_t)expo;
         } else if (dbase + rel_val < p.cap && dbase + rel_pos + 1 < p.cap) {
             p.out[dbase + rel_pos] = (uint8_t)(pos & 0xFF);
             p.out[dbase + rel_pos + 1] = (uint8_t)(pos >> 8);
             p.out[dbase + rel_val] = (uint8_t)expo;
         }
     };
+    if (kRounds == 1 && __any_sync(0xffffffffu, n_in[0] > kParallelAbove)) {
+        // Some unit has many escapes: go escape-parallel. Lane l takes range
+        // ranks l, l + 32, ...; the unit
+        // holding rank r is the last lane whose first rank is <= r (lanes
+        // past the range's units never match).
+        const uint32_t key = lane < nu ? first[0] : 0xFFFFFFFFu;
+        const uint32_t nlo = n_lo[0], is_list = up[0].list ? 1u : 0u;
+        for (uint32_t r0 = 0; r0 < rtotal; r0 += 32) {
+            const uint32_t r = r0 + lane;
+            uint32_t L = 0;
 #pragma unroll
-    for (int rr = 0; rr < kRounds; rr++) {
-        if (32 * rr + lane < nu && up[rr].list && n_in[rr]) {
-            const UnitPart& u = up[rr];
-            uint32_t running = first[rr];
-            uint32_t q = ((uint32_t)(u.ubase + u.plo) - s) / C;  // chunk of the part's first value
-            uint32_t next = (q + 1) * C;
-            for (uint32_t i = n_lo[rr]; i < n_lo[rr] + n_in[rr]; i++) {
-                const uint32_t ent = entry(rr, u.entries, i);
-                const uint32_t off = (uint32_t)(u.ubase + (ent & 0xFFFF)) - s;
-                while (off >= next) {
-                    q++;
-                    next += C;
-                }
-                put(off, running++, q, ent >> 16);
+            for (uint32_t st = 16; st; st >>= 1) {
+                const uint32_t kc = __shfl_sync(0xffffffffu, key, L + st);
+                if (kc <= r) L += st;
+            }
+            const uint32_t fL = __shfl_sync(0xffffffffu, key, L);
+            const uint32_t nloL = __shfl_sync(0xffffffffu, nlo, L);
+            const uint32_t listL = __shfl_sync(0xffffffffu, is_list, L);
+            if (r < rtotal && listL) {
+                const uint32_t j = r - fL + nloL;  // index in unit L's list
+                const uint32_t ent = j < kHeadEntries ? s_head[j * 32 + L]
+                                                      : __ldg(p.lists + (uint64_t)(u0 + L) * kListCap + j);
+                const uint32_t off = (u0 + L) * kUnit + (ent & 0xFFFF) - s;
+                put(off, r, div_chunk(p, off), ent >> 16);
             }
         }
+    } else {
+#pragma unroll
+        for (int rr = 0; rr < kRounds; rr++) {
+            if (32 * rr + lane < nu && up[rr].list && n_in[rr]) {
+                const UnitPart& u = up[rr];
+                uint32_t running = first[rr];
+                uint32_t q = div_chunk(p, (uint32_t)(u.ubase + u.plo) - s);  // chunk of the part's first value
+                uint32_t next = (q + 1) * C;
+                for (uint32_t i = n_lo[rr]; i < n_lo[rr] + n_in[rr]; i++) {
+                    const uint32_t ent = entry(rr, u.ubase, i);
+                    const uint32_t off = (uint32_t)(u.ubase + (ent & 0xFFFF)) - s;
+                    while (off >= next) {
+                        q++;
+                        next += C;
+                    }
+                    put(off, running++, q, ent >> 16);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < kRounds; rr++) {
         for (uint32_t ovf = __ballot_sync(0xffffffffu, !up[rr].list); ovf; ovf &= ovf - 1) {
             const int o = __ffs(ovf) - 1;
             uint64_t ub;
@@ -595,14 +642,25 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
                 for (int t = 0; t < kBatch; t++) ex[t] = t < got ? (__ldg(p.in + s + offs_b[t]) >> 7) & 0xFF : 0;
 #pragma unroll
                 for (int t = 0; t < kBatch; t++)
-                    if (t < got) put(offs_b[t], running++, offs_b[t] / C, ex[t]);
+                    if (t < got) put(offs_b[t], running++, div_chunk(p, offs_b[t]), ex[t]);
             }
         }
     }
     if (staged) {
+        // Stage bytes [lead, lead + dbytes) go to the 4-byte aligned global
+        // address gbase + the same index.
         __syncwarp();
-        for (uint32_t b = lane; b < dbytes; b += 32)
-            if (dbase + b < p.cap) p.out[dbase + b] = stage[b];
+        const uint32_t end = lead + dbytes;
+        const uint64_t gbase = dbase - lead;
+        const bool fits = dbase + dbytes <= p.cap;
+        for (uint32_t b0 = 4 * lane; b0 < end; b0 += 128) {
+            if (fits && b0 >= lead && b0 + 4 <= end) {
+                *reinterpret_cast<uint32_t*>(p.out + gbase + b0) = *reinterpret_cast<const uint32_t*>(stage + b0);
+            } else {
+                for (uint32_t i = max(b0, lead); i < min(b0 + 4, end); i++)
+                    if (gbase + i < p.cap) p.out[gbase + i] = stage[i];
+            }
+        }
         __syncwarp();  // the stage is reused by the next range
     }
 }
@@ -628,7 +686,8 @@ __global__ void __launch_bounds__(kThreads, UZIP_ESC_MIN_BLOCKS) encode_escape_k
         const bool active = r < p.ranges;
         const uint32_t seg_first = (uint32_t)(rb * p.range_chunks * p.chunk / kUnit) / p.seg_units;
         RangeLoads<kRounds> rl;
-        if (active) load_range(p, r, seg_first, rl);
+        __syncwarp();  // the previous range's list entries are no longer read
+        if (active) load_range(p, r, seg_first, rl, s_head);
         uint32_t v = 0;
 #pragma unroll
         for (int k = 0; k < (int)(kMaxSegments / kThreads); k++) {
@@ -724,6 +783,7 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
     p.in = static_cast<const uint16_t*>(d_in_bf16);
     p.n = n;
     p.chunk = chunk;
+    p.chunk_shift = (chunk & (chunk - 1)) == 0 ? (uint32_t)__builtin_ctz(chunk) : 32u;
     p.units = g.units;
     p.cb = static_cast<const uint8_t*>(d_codebook);
     p.out = static_cast<uint8_t*>(d_out);
