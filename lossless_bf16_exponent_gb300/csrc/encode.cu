@@ -50,11 +50,11 @@ constexpr int kThreads = 256;                 // both kernels
 constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kMaxSegments = 2048;       // segment totals (a block sums up to all of them)
 constexpr uint32_t kListCap = 64;             // escape entries a unit keeps in its list
-constexpr uint32_t kHeadEntries = 8;          // list entries in the first 32-byte sector
+constexpr uint32_t kHeadEntries = 32;         // list entries a unit keeps in shared memory during the escape pass
 constexpr uint32_t kMaxRangeUnits = 31;       // a range covers at most 31 units of values (32 overlapped)
-constexpr uint32_t kStageBytes = 4096;        // per-warp staging of a range's escape blocks
+constexpr uint32_t kStageBytes = 2560;        // per-warp staging of a range's escape blocks (853 escapes)
 constexpr uint32_t kMaxRangeChunks = 256;     // bounds the per-warp chunk table
-constexpr int kBatch = 8;                     // escape exponents re-read at once (mask units)
+constexpr int kBatch = 4;                     // escape exponents re-read at once (mask units)
 constexpr uint32_t kParallelAbove = 32;       // pass 2 goes escape-parallel when a unit has more escapes
                                               // (below, one lane per unit walking its list measured faster)
 #ifndef UZIP_ENC_MIN_BLOCKS
@@ -180,6 +180,21 @@ __device__ void zero_words(uint8_t* out, uint64_t from, uint64_t to) {
 }
 
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) { return __reduce_add_sync(0xffffffffu, v); }
+
+// Shared-memory slot of list entry j of lane L's unit (round rr): each lane
+// owns a 128-byte row of eight 16-byte chunks, chunk c stored at c ^ (L & 7)
+// so that lanes reading the same entry spread over the banks.
+__device__ __forceinline__ uint32_t head_slot(int rr, uint32_t L, uint32_t j) {
+    return (uint32_t)rr * (kHeadEntries * 32) + L * kHeadEntries + ((((j >> 2) ^ (L & 7)) << 2) | (j & 3));
+}
+
+// 16-byte asynchronous global -> shared copy (cp.async) and its wait.
+__device__ __forceinline__ void cp_async16(uint32_t* dst, const uint32_t* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // x / chunk (a shift for the power-of-two chunk sizes).
 __device__ __forceinline__ uint32_t div_chunk(const Params& p, uint32_t x) {
@@ -347,14 +362,13 @@ __device__ __forceinline__ void load_range(const Params& p, uint64_t r, uint32_t
         const uint32_t u = rl.u0 + 32 * rr + lane;
         const bool on = 32 * rr + lane < rl.nu;
         rl.cnt[rr] = on ? __ldg(p.counts + u) : 0;
-        if (on) {  // the unit's first list entries -> shared memory, [round][entry][lane]
-            const uint4* head = reinterpret_cast<const uint4*>(p.lists + (uint64_t)u * kListCap);
-            const uint4 h0 = __ldg(head), h1 = __ldg(head + 1);
-            const uint32_t q[kHeadEntries] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-#pragma unroll
-            for (int j = 0; j < (int)kHeadEntries; j++) s_head[(rr * kHeadEntries + j) * 32 + lane] = q[j];
+        if (on) {  // the list's first 32-byte sector -> shared memory (the rest once the count is known)
+            const uint32_t* list = p.lists + (uint64_t)u * kListCap;
+            cp_async16(s_head + head_slot(rr, lane, 0), list);
+            cp_async16(s_head + head_slot(rr, lane, 4), list + 4);
         }
     }
+    cp_async_commit();
     const uint32_t first = rl.seg * p.seg_units;
 #pragma unroll
     for (int j = 0; j < kPreLoads; j++) {
@@ -376,17 +390,23 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
     const uint32_t C = p.chunk;
     const uint32_t c0 = rl.c0, nq = rl.nq, s = rl.s, e = rl.e, u0 = rl.u0, nu = rl.nu, seg = rl.seg;
 
-    // The units' first list entries are in s_head, [round][entry][lane]; the
-    // rest of a longer list is prefetched into L1 now, ahead of its use.
-    __syncwarp();
+    // Longer lists: their entries 8 .. kHeadEntries - 1 follow into shared
+    // memory (entries past that are read from global memory, prefetched into
+    // L1 here).
 #pragma unroll
     for (int rr = 0; rr < kRounds; rr++) {
-        const uint32_t c = min(rl.cnt[rr], kListCap);
-        const uint32_t* list = p.lists + (uint64_t)(u0 + 32 * rr + lane) * kListCap;
-        for (uint32_t j = kHeadEntries; j < c; j += 32) prefetch_l1(list + j);  // 128-byte lines
+        if (32 * rr + lane < nu && rl.cnt[rr] > 8) {
+            const uint32_t c = min(rl.cnt[rr], kListCap);
+            const uint32_t* list = p.lists + (uint64_t)(u0 + 32 * rr + lane) * kListCap;
+            for (uint32_t j = 8; j < min(c, kHeadEntries); j += 4) cp_async16(s_head + head_slot(rr, lane, j), list + j);
+            for (uint32_t j = kHeadEntries; j < c; j += 8) prefetch_l1(list + j);  // one 32-byte sector each
+        }
     }
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncwarp();
     auto entry = [&](int rr, uint32_t ubase, uint32_t j) -> uint32_t {
-        return j < kHeadEntries ? s_head[(rr * kHeadEntries + j) * 32 + lane]
+        return j < kHeadEntries ? s_head[head_slot(rr, lane, j)]
                                 : __ldg(p.lists + (uint64_t)(ubase / kUnit) * kListCap + j);
     };
 
@@ -477,7 +497,12 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
             uint32_t i = n_lo[rr];
             const uint32_t iend = n_lo[rr] + n_in[rr];
             while (q < nq && x < u.phi) {
-                while (i < iend && (entry(rr, u.ubase, i) & 0xFFFF) < x) i++;
+                uint32_t hi = iend;  // first entry at or past x: binary search (the list is ascending)
+                while (i < hi) {
+                    const uint32_t mid = (i + hi) >> 1;
+                    if ((entry(rr, u.ubase, mid) & 0xFFFF) < x) i = mid + 1;
+                    else hi = mid;
+                }
                 s_cp[q] = first[rr] + (i - n_lo[rr]);
                 q++;
                 x += C;
@@ -543,12 +568,8 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
     const uint32_t dbytes = 3 * rtotal;
     const uint32_t lead = (uint32_t)(dbase & 3);
     const bool staged = lead + dbytes <= kStageBytes;
-    auto put = [&](uint32_t off, uint32_t rank_in_range, uint32_t q, uint32_t expo) {
-        const uint32_t cstart = s_cp[q];
-        const uint32_t k = s_cp[q + 1] - cstart;
-        const uint32_t rank = rank_in_range - cstart;
-        const uint32_t pos = off - q * C;
-        const uint32_t rel_pos = 3 * cstart + 2 * rank, rel_val = 3 * cstart + 2 * k + rank;
+    // One escape: its position bytes at block offset rel_pos, its value at rel_val.
+    auto emit = [&](uint32_t rel_pos, uint32_t rel_val, uint32_t pos, uint32_t expo) {
         if (staged) {
             stage[lead + rel_pos] = (uint8_t)(pos & 0xFF);
             stage[lead + rel_pos + 1] = (uint8_t)(pos >> 8);
@@ -558,6 +579,12 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
             p.out[dbase + rel_pos + 1] = (uint8_t)(pos >> 8);
             p.out[dbase + rel_val] = (uint8_t)expo;
         }
+    };
+    auto put = [&](uint32_t off, uint32_t rank_in_range, uint32_t q, uint32_t expo) {
+        const uint32_t cstart = s_cp[q];
+        const uint32_t k = s_cp[q + 1] - cstart;
+        const uint32_t rank = rank_in_range - cstart;
+        emit(3 * cstart + 2 * rank, 3 * cstart + 2 * k + rank, off - q * C, expo);
     };
     if (kRounds == 1 && __any_sync(0xffffffffu, n_in[0] > kParallelAbove)) {
         // Some unit has many escapes: go escape-parallel. Lane l takes range
@@ -579,7 +606,7 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
             const uint32_t listL = __shfl_sync(0xffffffffu, is_list, L);
             if (r < rtotal && listL) {
                 const uint32_t j = r - fL + nloL;  // index in unit L's list
-                const uint32_t ent = j < kHeadEntries ? s_head[j * 32 + L]
+                const uint32_t ent = j < kHeadEntries ? s_head[head_slot(0, L, j)]
                                                       : __ldg(p.lists + (uint64_t)(u0 + L) * kListCap + j);
                 const uint32_t off = (u0 + L) * kUnit + (ent & 0xFFFF) - s;
                 put(off, r, div_chunk(p, off), ent >> 16);
@@ -590,17 +617,37 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
         for (int rr = 0; rr < kRounds; rr++) {
             if (32 * rr + lane < nu && up[rr].list && n_in[rr]) {
                 const UnitPart& u = up[rr];
-                uint32_t running = first[rr];
-                uint32_t q = div_chunk(p, (uint32_t)(u.ubase + u.plo) - s);  // chunk of the part's first value
-                uint32_t next = (q + 1) * C;
-                for (uint32_t i = n_lo[rr]; i < n_lo[rr] + n_in[rr]; i++) {
-                    const uint32_t ent = entry(rr, u.ubase, i);
-                    const uint32_t off = (uint32_t)(u.ubase + (ent & 0xFFFF)) - s;
-                    while (off >= next) {
-                        q++;
-                        next += C;
+                // Walk the unit's list chunk by chunk: one chunk-table lookup
+                // per chunk, then each escape's bytes follow the previous
+                // one's (positions 2 bytes on, values 1 byte on); the next
+                // entry is read before the current escape is stored.
+                uint32_t i = n_lo[rr];
+                const uint32_t iend = i + n_in[rr];
+                uint32_t rank = first[rr];
+                uint32_t ent = entry(rr, u.ubase, i);
+                uint32_t off = u.ubase + (ent & 0xFFFF) - s;
+                for (;;) {
+                    const uint32_t q = div_chunk(p, off);
+                    const uint32_t qbeg = q * C;
+                    const uint32_t cstart = s_cp[q];
+                    const uint32_t k = s_cp[q + 1] - cstart;
+                    uint32_t rel_pos = 3 * cstart + 2 * (rank - cstart);
+                    uint32_t rel_val = 3 * cstart + 2 * k + (rank - cstart);
+                    bool more;
+                    for (;;) {
+                        const uint32_t pos = off - qbeg, expo = ent >> 16;
+                        i++;
+                        rank++;
+                        more = i < iend;
+                        if (more) ent = entry(rr, u.ubase, i);
+                        emit(rel_pos, rel_val, pos, expo);
+                        rel_pos += 2;
+                        rel_val += 1;
+                        if (!more) break;
+                        off = u.ubase + (ent & 0xFFFF) - s;
+                        if (off >= qbeg + C) break;  // the next escape opens another chunk
                     }
-                    put(off, running++, q, ent >> 16);
+                    if (!more) break;
                 }
             }
         }
@@ -728,7 +775,7 @@ namespace {
 // Per-device launch facts, looked up on the first call on each device (the
 // results are the same whichever thread gets there first).
 struct DeviceFacts {
-    int sms, per_sm1, per_sm2[2];
+    int sms, per_sm1;
 };
 constexpr int kMaxFactDevices = 64;
 std::atomic<int> g_facts_ready[kMaxFactDevices];
@@ -752,9 +799,8 @@ int device_facts(DeviceFacts& f) {
         const size_t smem_max = escape_smem(kMaxRangeChunks, k + 1);
         if (smem_max > 48 * 1024)
             UZIP_CUDA_TRY(cudaFuncSetAttribute(esc[k], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max));
-        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm2[k], esc[k], kThreads, smem_max));
     }
-    if (f.sms < 1 || f.per_sm1 < 1 || f.per_sm2[0] < 1 || f.per_sm2[1] < 1) return UZIP_ERR_CUDA;
+    if (f.sms < 1 || f.per_sm1 < 1) return UZIP_ERR_CUDA;
     if (dev < kMaxFactDevices) {
         g_facts[dev] = f;
         g_facts_ready[dev].store(1, std::memory_order_release);
@@ -808,12 +854,18 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         // Escape kernel: ranges of whole chunks, sized so every resident warp
         // gets at most one (the per-range cost is mostly load latency).
         const int two_rounds = chunk > 32 * kUnit - 2040 && chunk % kUnit != 0;
-        const uint64_t warps2 = (uint64_t)f.sms * f.per_sm2[two_rounds] * kWarps;
         const uint32_t rc_max =
             std::max<uint32_t>(1, std::min<uint32_t>(kMaxRangeChunks, kMaxRangeUnits * kUnit / chunk));
+        // Residency at the largest chunk table this chunk size can need.
+        int per_sm2 = 0;
+        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm2, two_rounds ? encode_escape_kernel<2> : encode_escape_kernel<1>, kThreads,
+            escape_smem(rc_max, two_rounds + 1)));
+        if (per_sm2 < 1) return UZIP_ERR_CUDA;
+        const uint64_t warps2 = (uint64_t)f.sms * per_sm2 * kWarps;
         p.range_chunks = (uint32_t)std::min<uint64_t>(rc_max, std::max<uint64_t>(1, (L.nc + warps2 - 1) / warps2));
         p.ranges = (L.nc + p.range_chunks - 1) / p.range_chunks;
-        const uint64_t grid2 = std::min<uint64_t>((p.ranges + kWarps - 1) / kWarps, (uint64_t)f.sms * f.per_sm2[two_rounds]);
+        const uint64_t grid2 = std::min<uint64_t>((p.ranges + kWarps - 1) / kWarps, (uint64_t)f.sms * per_sm2);
 
         UZIP_CUDA_TRY(cudaMemsetAsync(p.segs, 0, 4ull * g.nseg, s));  // segment totals
         encode_dense_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
