@@ -561,12 +561,12 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
     // Pass 2: each escape's chunk-relative position and raw exponent. The
     // range's escape blocks are contiguous in the stream: assemble them in
     // this warp's stage -- shifted by the destination's offset within a
-    // 4-byte word, so whole words can be copied out -- and store them with
-    // coalesced word stores, unless there are too many, then store them
+    // 16-byte piece, so whole pieces can be copied out -- and store them with
+    // coalesced 16-byte stores, unless there are too many, then store them
     // directly.
     const uint64_t dbase = p.L.off_d + 3ull * pre;
     const uint32_t dbytes = 3 * rtotal;
-    const uint32_t lead = (uint32_t)(dbase & 3);
+    const uint32_t lead = (uint32_t)(dbase & 15);
     const bool staged = lead + dbytes <= kStageBytes;
     // One escape: its position bytes at block offset rel_pos, its value at rel_val.
     auto emit = [&](uint32_t rel_pos, uint32_t rel_val, uint32_t pos, uint32_t expo) {
@@ -694,17 +694,18 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
         }
     }
     if (staged) {
-        // Stage bytes [lead, lead + dbytes) go to the 4-byte aligned global
-        // address gbase + the same index.
+        // Stage bytes [lead, lead + dbytes) go to the 16-byte aligned global
+        // address gbase + the same index: whole 16-byte pieces as vectors,
+        // the partial first and last pieces byte by byte.
         __syncwarp();
         const uint32_t end = lead + dbytes;
         const uint64_t gbase = dbase - lead;
         const bool fits = dbase + dbytes <= p.cap;
-        for (uint32_t b0 = 4 * lane; b0 < end; b0 += 128) {
-            if (fits && b0 >= lead && b0 + 4 <= end) {
-                *reinterpret_cast<uint32_t*>(p.out + gbase + b0) = *reinterpret_cast<const uint32_t*>(stage + b0);
+        for (uint32_t b0 = 16 * lane; b0 < end; b0 += 512) {
+            if (fits && b0 >= lead && b0 + 16 <= end) {
+                *reinterpret_cast<uint4*>(p.out + gbase + b0) = *reinterpret_cast<const uint4*>(stage + b0);
             } else {
-                for (uint32_t i = max(b0, lead); i < min(b0 + 4, end); i++)
+                for (uint32_t i = max(b0, lead); i < min(b0 + 16, end); i++)
                     if (gbase + i < p.cap) p.out[gbase + i] = stage[i];
             }
         }
