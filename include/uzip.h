@@ -183,6 +183,18 @@ UZIP_API int uzip_encode_noalloc(const void *d_in_bf16, size_t n, uint32_t chunk
                                  void *d_out, size_t out_capacity, size_t *h_out_bytes,
                                  uzip_stream_t stream);
 
+/* Encode with a codebook built from the input itself (§4.3, Table 7: the
+ * "dynamic Top-16" alternative to offline calibration): the histogram of all
+ * n exponents, the Top-16 and the three tables are written to d_codebook
+ * (exactly what uzip_calibrate(d_in_bf16, n, d_codebook) writes), then the
+ * input is encoded with them; the input is read twice.
+ *   d_codebook     UZIP_CODEBOOK_BYTES of device memory, overwritten.
+ * Other arguments, output and errors are those of uzip_encode; the stream is
+ * byte-identical to uzip_encode's with that codebook. */
+UZIP_API int uzip_encode_dynamic(const void *d_in_bf16, size_t n, uint32_t chunk, void *d_codebook,
+                                 void *d_out, size_t out_capacity, void *d_workspace,
+                                 size_t workspace_bytes, size_t *h_out_bytes, uzip_stream_t stream);
+
 /* Decode a stream produced by uzip_encode (§3.2): dense unpack and lookup,
  * then the escape fix-up, fused per tile so each output byte is written once.
  *   d_stream       stream_bytes bytes (at least the header's total).

@@ -104,6 +104,24 @@ def encode(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, out: torc
     return out, (nbytes.value if sync else None)
 
 
+def encode_dynamic(x: torch.Tensor, chunk: int = 1024, codebook: torch.Tensor | None = None,
+                   out: torch.Tensor | None = None, workspace: torch.Tensor | None = None, sync: bool = True):
+    """Encode ``x`` with a codebook built from ``x`` itself (SplitZip §4.3,
+    Table 7). Returns ``(stream, nbytes, codebook)``."""
+    v = _flat16(x)
+    n = v.numel()
+    cb = new_codebook(v.device) if codebook is None else codebook
+    if out is None:
+        out = torch.empty(max_compressed_size(n, chunk), dtype=torch.uint8, device=v.device)
+    if workspace is None:
+        workspace = torch.empty(max(16, workspace_bytes(n, chunk)), dtype=torch.uint8, device=v.device)
+    nbytes = ctypes.c_size_t(0)
+    args = (_p(v), n, chunk, _p(cb), _p(out), out.numel(), _p(workspace), workspace.numel(),
+            ctypes.byref(nbytes) if sync else None)
+    check(load().uzip_encode_dynamic(*args, _sp(v.device)), "uzip_encode_dynamic")
+    return out, (nbytes.value if sync else None), cb
+
+
 def decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = None, status: torch.Tensor | None = None,
            stream_bytes: int | None = None, dtype=torch.bfloat16) -> torch.Tensor:
     """Decode ``n`` values from a stream (SplitZip §3.2). Device-side errors

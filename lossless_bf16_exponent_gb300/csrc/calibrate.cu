@@ -18,6 +18,8 @@
 //                     ascending) -- and the 16 lowest ranks become the
 //                     codebook; then it writes the three tables.
 //   luts_kernel       the same tables from 16 caller-given exponents.
+#include <algorithm>
+
 #include "uzip_internal.cuh"
 
 namespace uzip {
@@ -162,25 +164,35 @@ __global__ void __launch_bounds__(256) luts_kernel(Exps16 in, uint8_t* __restric
 
 using namespace uzip;
 
-extern "C" UZIP_API int uzip_calibrate(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
-                                       uzip_stream_t stream) {
+namespace uzip {
+
+int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook, cudaStream_t s) {
     if (!d_codebook || (n_sample > 0 && !d_sample_bf16)) return UZIP_ERR_ARG;
     if (!aligned16(d_codebook) || (n_sample > 0 && !aligned16(d_sample_bf16))) return UZIP_ERR_ALIGN;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     uint8_t* cb = static_cast<uint8_t*>(d_codebook);
     // Histogram totals and the block counter start at zero.
     UZIP_CUDA_TRY(cudaMemsetAsync(cb + UZIP_CB_HIST, 0, kCbCounter + 16 - UZIP_CB_HIST, s));
-    int dev = 0, sms = 0;
+    int dev = 0, sms = 0, per_sm = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
     UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    const uint64_t per_block = (uint64_t)kHistThreads * kLoadsPerThread;
-    uint64_t blocks = (n_sample / 8 + per_block - 1) / per_block;
-    if (blocks > (uint64_t)sms) blocks = sms;
+    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, calibrate_kernel, kHistThreads, 0));
+    // One block per 8192 values, up to a full resident wave: a small sample
+    // is a latency chain, a whole tensor is read at HBM speed.
+    const uint64_t per_block = (uint64_t)kHistThreads * kLoadsPerThread * 8;
+    uint64_t blocks = (n_sample + per_block - 1) / per_block;
+    blocks = std::min<uint64_t>(blocks, (uint64_t)sms * std::max(per_sm, 1));
     if (blocks == 0) blocks = 1;
     calibrate_kernel<<<(unsigned)blocks, kHistThreads, 0, s>>>(static_cast<const uint16_t*>(d_sample_bf16),
                                                                 n_sample, cb);
     UZIP_CUDA_TRY(cudaGetLastError());
     return UZIP_OK;
+}
+
+}  // namespace uzip
+
+extern "C" UZIP_API int uzip_calibrate(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
+                                       uzip_stream_t stream) {
+    return calibrate_impl(d_sample_bf16, n_sample, d_codebook, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" UZIP_API int uzip_codebook_from_exps(const uint8_t* h_exps16, void* d_codebook,

@@ -904,6 +904,23 @@ extern "C" UZIP_API int uzip_encode(const void* d_in_bf16, size_t n, uint32_t ch
                        h_out_bytes, stream);
 }
 
+// ------------------------------------------------------ per-input codebook
+
+// SplitZip review page, §4.3 Table 7 (dynamic Top-16): the codebook is rebuilt
+// for every input -- the histogram of all n exponents, the Top-16, the tables
+// -- and the input is then encoded with it. Two reads of the input: the
+// histogram must be complete before the first code is chosen.
+extern "C" UZIP_API int uzip_encode_dynamic(const void* d_in_bf16, size_t n, uint32_t chunk, void* d_codebook,
+                                            void* d_out, size_t out_capacity, void* d_workspace,
+                                            size_t workspace_bytes, size_t* h_out_bytes, uzip_stream_t stream) {
+    if (!chunk_valid(chunk)) return UZIP_ERR_CHUNK;
+    if (n > UZIP_MAX_N) return UZIP_ERR_ARG;
+    const int rc = calibrate_impl(d_in_bf16, n, d_codebook, reinterpret_cast<cudaStream_t>(stream));
+    if (rc != UZIP_OK) return rc;
+    return encode_impl(d_in_bf16, n, chunk, d_codebook, d_out, out_capacity, d_workspace, workspace_bytes,
+                       h_out_bytes, stream);
+}
+
 // ------------------------------------------------- encoding without allocation
 //
 // Some callers cannot allocate device memory for the encoder's workspace:

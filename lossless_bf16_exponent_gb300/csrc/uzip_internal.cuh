@@ -89,6 +89,12 @@ __device__ __forceinline__ void st_u8_keep(void* p, uint32_t v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.u8 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
 }
 
+// Launchers shared by the entry points (calibrate.cu, encode.cu).
+int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook, cudaStream_t stream);
+int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_codebook, void* d_out,
+                size_t out_capacity, void* d_workspace, size_t workspace_bytes, size_t* h_out_bytes,
+                uzip_stream_t stream);
+
 }  // namespace uzip
 
 #define UZIP_CUDA_TRY(expr)                          \
