@@ -533,14 +533,97 @@ def run_dynamic(args):
     }
 
 
+def run_pipeline(args):
+    """Streamed transfer (SplitZip review page, appendix B): the 256M KV tensor
+    in pieces through encode -> link -> decode, against the same pipeline
+    moving raw pieces, on two links (pinned host memory over NVLink-C2C; a
+    device-to-device copy), with B_hide = min(G_enc, G_dec) / rho and the
+    appendix's stage model next to the measured times."""
+    import statistics as stats
+
+    import torch
+
+    import lossless_bf16_exponent_gb300 as uz
+    import lossless_bf16_exponent_gb300.workloads as W
+    from lossless_bf16_exponent_gb300 import pipeline as PL
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist("nccl")
+    uz.load()
+    x, sample = W.workload(2, device=dev)
+    n = x.numel()
+    raw = 2 * n
+    cb = uz.calibrate(sample)
+    out = torch.empty(uz.max_compressed_size(n, CHUNK), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(uz.workspace_bytes(n, CHUNK), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(x)
+    _, nbytes = uz.encode(x, cb, CHUNK, out=out, workspace=wsb)
+    ratio = raw / nbytes
+    st = torch.cuda.current_stream(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    te, td = [], []
+    for k in range(args.warmup + 20):
+        ev[0].record(st)
+        uz.encode(x, cb, CHUNK, out=out, workspace=wsb, sync=False)
+        ev[1].record(st)
+        uz.decode(out, n, out=y, stream_bytes=nbytes)
+        ev[2].record(st)
+        torch.cuda.synchronize()
+        if k >= args.warmup:
+            te.append(ev[0].elapsed_time(ev[1]))
+            td.append(ev[1].elapsed_time(ev[2]))
+    g_enc = raw / (stats.median(te) * 1e-3)
+    g_dec = raw / (stats.median(td) * 1e-3)
+    pieces = 16
+    runs = max(3, min(args.steps, 10))
+    links = {}
+    for link in ("host", "d2d"):
+        res = {}
+        for name, fn in (("raw", lambda: PL.send_raw(x, pieces=pieces, link=link, out=y)),
+                         ("compressed", lambda: PL.send_compressed(x, cb, CHUNK, pieces=pieces, link=link, out=y))):
+            fn()  # warm-up (allocations, first touch of pinned memory)
+            secs = []
+            for _ in range(runs):
+                yy, tr = fn()
+                secs.append(tr.seconds)
+            assert torch.equal(y.view(torch.int16), x.view(torch.int16)), f"{link} {name}: not bit-exact"
+            res[name] = {"seconds": stats.median(secs), "raw_gbs": round(raw / stats.median(secs) / 1e9, 2),
+                         "sent_bytes": tr.sent_bytes}
+        b_link = raw / res["raw"]["seconds"]  # the link's own rate, from the raw pipeline
+        model = PL.model_seconds(raw, g_enc, g_dec, ratio, b_link, pieces)
+        links[link] = {
+            "raw_pipeline_gbs": res["raw"]["raw_gbs"], "compressed_pipeline_gbs": res["compressed"]["raw_gbs"],
+            "speedup": round(res["raw"]["seconds"] / res["compressed"]["seconds"], 3),
+            "link_gbs": round(b_link / 1e9, 1), "codec_hidden": bool(b_link <= PL.b_hide(g_enc, g_dec, ratio)),
+            "model_us": round(model * 1e6, 1), "measured_us": round(res["compressed"]["seconds"] * 1e6, 1),
+            "sent_bytes": res["compressed"]["sent_bytes"],
+        }
+    if rank != 0:
+        return None
+    return {
+        "mode": "pipeline", "metric": "compressed transfer GB/s (raw BF16 bytes through encode -> link -> decode)",
+        "value": links["host"]["compressed_pipeline_gbs"], "unit": "GB/s", "n_gpus": ws, "steps": runs,
+        "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "pieces": pieces, "value_link": "host"},
+        "g_enc_gbs": round(g_enc / 1e9, 1), "g_dec_gbs": round(g_dec / 1e9, 1), "ratio": round(ratio, 5),
+        "b_hide_gbs": round(PL.b_hide(g_enc, g_dec, ratio) / 1e9, 1), "links": links,
+        "note": ("the stage model assumes independent resources; the host link is one (copy engines over "
+                 "NVLink-C2C), the d2d link is not (its copies share HBM and SMs with the codec kernels)"),
+        "page_h200": {"b_hide_gbs": 463.2, "g_enc_gbs": 613.3, "g_dec_gbs": 2181.8, "ratio": 1.324},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["codec", "dynamic"], default="codec",
-                    help="codec = the benchmark step; dynamic = per-input codebook encode (next row)")
+    ap.add_argument("--mode", choices=["codec", "dynamic", "pipeline"], default="codec",
+                    help="codec = the benchmark step; dynamic = per-input codebook encode; "
+                         "pipeline = streamed compressed transfer (next rows)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--tokens", type=int, default=2048,
@@ -552,6 +635,8 @@ def main(argv=None):
         line = run_reference(args)
     elif args.mode == "dynamic":
         line = run_dynamic(args)
+    elif args.mode == "pipeline":
+        line = run_pipeline(args)
     else:
         line = run_ours(args)
     if line is not None:

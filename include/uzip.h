@@ -212,6 +212,25 @@ UZIP_API int uzip_encode_dynamic(const void *d_in_bf16, size_t n, uint32_t chunk
 UZIP_API int uzip_decode(const void *d_stream, size_t stream_bytes, void *d_out_bf16, size_t n,
                          uint32_t *d_status, uzip_stream_t stream);
 
+/* Copy one encoded stream, exactly its header's total bytes, without the
+ * host learning its length first (a sender in the encode -> transfer ->
+ * decode pipeline of appendix B). The kernel reads the header at src_stream;
+ * if it is a stream header of this version and its total is at most
+ * capacity, bytes [0, total) are copied to dst, else nothing is.
+ *   src_stream     16-byte aligned, at least capacity readable bytes; device
+ *                  memory or pinned (mapped) host memory.
+ *   dst            16-byte aligned, at least capacity writable bytes; device
+ *                  or pinned host memory.
+ *   capacity       at least UZIP_HEADER_BYTES.
+ *   d_copied       NULL or one 8-byte aligned device (or pinned host) word
+ *                  that receives the bytes copied (0 when nothing was).
+ * When either end is host memory the copy uses a small grid that fills the
+ * host link and leaves the SMs to concurrent codec kernels.
+ * Returns UZIP_ERR_ARG / UZIP_ERR_ALIGN / UZIP_ERR_CAPACITY / UZIP_ERR_CUDA,
+ * else UZIP_OK. Async. */
+UZIP_API int uzip_stream_copy(const void *src_stream, void *dst, size_t capacity,
+                              unsigned long long *d_copied, uzip_stream_t stream);
+
 /* Host view of a stream header. */
 typedef struct {
     uint64_t n;

@@ -8,10 +8,10 @@ missing.
 """
 from .codec import (CODEBOOK_BYTES, HEADER_BYTES, UzipError, calibrate, codebook_exps, codebook_from_exps,
                     codebook_histogram, compressed_size, decode, encode, encode_dynamic, load, max_compressed_size,
-                    new_codebook, roundtrip_ok, stream_info, workspace_bytes)
+                    new_codebook, roundtrip_ok, stream_copy, stream_info, workspace_bytes)
 
 __all__ = [
     "CODEBOOK_BYTES", "HEADER_BYTES", "UzipError", "calibrate", "codebook_exps", "codebook_from_exps",
     "codebook_histogram", "compressed_size", "decode", "encode", "encode_dynamic", "load", "max_compressed_size",
-    "new_codebook", "roundtrip_ok", "stream_info", "workspace_bytes",
+    "new_codebook", "roundtrip_ok", "stream_copy", "stream_info", "workspace_bytes",
 ]

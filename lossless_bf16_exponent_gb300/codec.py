@@ -135,6 +135,19 @@ def decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = None, status
     return out
 
 
+def stream_copy(src: torch.Tensor, dst: torch.Tensor, capacity: int | None = None,
+                copied: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None) -> None:
+    """Copy the stream at ``src`` (exactly its header's total bytes) to
+    ``dst``; either may be pinned host memory. ``copied`` (one int64 element,
+    device or pinned host) receives the byte count. Asynchronous on ``stream``
+    (default: the current stream of the device)."""
+    cap = min(src.numel(), dst.numel()) if capacity is None else capacity
+    dev = src.device if src.is_cuda else dst.device
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    check(load().uzip_stream_copy(_p(src), _p(dst), cap, _p(copied), ctypes.c_void_p(s.cuda_stream)),
+          "uzip_stream_copy")
+
+
 def stream_info(stream: torch.Tensor, stream_bytes: int | None = None) -> dict:
     info = _lib.Info()
     nb = stream.numel() if stream_bytes is None else stream_bytes
