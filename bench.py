@@ -615,13 +615,76 @@ def run_pipeline(args):
     }
 
 
+def run_chunks(args):
+    """Escape-capture chunk size (SplitZip review page, appendix D, Fig. 6):
+    the same KV tensor encoded with chunks of 256 .. 65536 values. The chunk
+    sets how many 16-bit escape positions share one 4-byte offset: small
+    chunks cost offset bytes, large chunks cost nothing in bytes but make
+    each decode tile walk longer escape blocks."""
+    import statistics as stats
+
+    import torch
+
+    import lossless_bf16_exponent_gb300 as uz
+    import lossless_bf16_exponent_gb300.workloads as W
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist("nccl")
+    uz.load()
+    x, sample = W.workload(2, device=dev)
+    n = x.numel()
+    raw = 2 * n
+    cb = uz.calibrate(sample)
+    y = torch.empty_like(x)
+    st = torch.cuda.current_stream(dev)
+    rows = []
+    for chunk in (256, 512, 1024, 2048, 4096, 16384, 65536):
+        out = torch.empty(uz.max_compressed_size(n, chunk), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(uz.workspace_bytes(n, chunk), dtype=torch.uint8, device=dev)
+        _, nbytes = uz.encode(x, cb, chunk, out=out, workspace=wsb)
+        info = uz.stream_info(out, nbytes)
+        reps = max(5, min(args.steps, 50))
+        for _ in range(args.warmup):
+            uz.encode(x, cb, chunk, out=out, workspace=wsb, sync=False)
+            uz.decode(out, n, out=y, stream_bytes=nbytes)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        torch.cuda.synchronize()
+        for ev in evs:  # back to back, as in the benchmark step
+            ev[0].record(st)
+            uz.encode(x, cb, chunk, out=out, workspace=wsb, sync=False)
+            ev[1].record(st)
+            uz.decode(out, n, out=y, stream_bytes=nbytes)
+            ev[2].record(st)
+        torch.cuda.synchronize()
+        te = [ev[0].elapsed_time(ev[1]) for ev in evs]
+        td = [ev[1].elapsed_time(ev[2]) for ev in evs]
+        assert torch.equal(y.view(torch.int16), x.view(torch.int16)), f"chunk {chunk}: not bit-exact"
+        m = int(info["escapes"])
+        nc = -(-n // chunk)
+        rows.append({"chunk": chunk, "stream_bytes": nbytes, "ratio": round(raw / nbytes, 5),
+                     "payload_ratio": round(raw / (n + (n + 1) // 2 + 3 * m), 5), "offset_bytes": 4 * (nc + 1),
+                     "encode_us": round(stats.median(te) * 1e3, 2), "decode_us": round(stats.median(td) * 1e3, 2),
+                     "encode_gbs_raw": round(raw / (stats.median(te) * 1e-3) / 1e9, 1),
+                     "decode_gbs_raw": round(raw / (stats.median(td) * 1e-3) / 1e9, 1)})
+        del out, wsb
+    if rank != 0:
+        return None
+    best = next(r for r in rows if r["chunk"] == CHUNK)
+    return {"mode": "chunks", "metric": "encode/decode GB/s and ratio vs escape chunk size @256M elems",
+            "value": best["decode_gbs_raw"], "unit": "GB/s", "n_gpus": ws, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "value": "decode GB/s at chunk 1024"}, "rows": rows}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["codec", "dynamic", "pipeline"], default="codec",
+    ap.add_argument("--mode", choices=["codec", "dynamic", "pipeline", "chunks"], default="codec",
                     help="codec = the benchmark step; dynamic = per-input codebook encode; "
                          "pipeline = streamed compressed transfer (next rows)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -637,6 +700,8 @@ def main(argv=None):
         line = run_dynamic(args)
     elif args.mode == "pipeline":
         line = run_pipeline(args)
+    elif args.mode == "chunks":
+        line = run_chunks(args)
     else:
         line = run_ours(args)
     if line is not None:
