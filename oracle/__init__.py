@@ -9,9 +9,14 @@ The arithmetic lives in ``uzip_oracle.c`` (plain scalar C, one loop per step of
 the method as the SplitZip review page states it in §3.2-§3.4). This module
 only compiles it with gcc and marshals numpy arrays through ctypes.
 
-Parity pins: every function is pinned in ``tests/test_oracle_pins.py`` against
-IEEE-754 semantics, the page's closed-form size, exhaustive and brute-force
-checks; none is "parity unpinned".
+The FP8 E5M2 variant (the page's §4.2 / appendix C: the same Top-16
+framework on E5M2 values) is in the same C file, after the BF16 codec.
+
+Parity pins: every function is pinned against IEEE-754 semantics, the page's
+closed-form sizes, hand-worked streams, exhaustive and brute-force checks --
+the BF16 codec in ``tests/test_oracle_pins.py``, the E5M2 variant in
+``tests/test_oracle_e5m2_pins.py`` (with planted-mistake batteries in the
+matching ``*_mutants.py``); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -60,7 +65,18 @@ def load(path: str | None = None):
     lib.orc_encode.restype = ctypes.c_int
     lib.orc_decode.argtypes = [p, u64, p, u64]
     lib.orc_decode.restype = ctypes.c_int
-    for f in ("orc_split", "orc_merge", "orc_histogram", "orc_top16", "orc_luts", "orc_calibrate"):
+    lib.orc_e5m2_split.argtypes = [p, u64, p, p]
+    lib.orc_e5m2_merge.argtypes = [p, p, u64, p]
+    lib.orc_e5m2_histogram.argtypes = [p, u64, p]
+    lib.orc_e5m2_calibrate.argtypes = [p, u64, p]
+    lib.orc_e5m2_stream_bytes.argtypes = [u64, u64, u32]
+    lib.orc_e5m2_stream_bytes.restype = u64
+    lib.orc_e5m2_encode.argtypes = [p, u64, u32, p, p, u64, ctypes.POINTER(u64)]
+    lib.orc_e5m2_encode.restype = ctypes.c_int
+    lib.orc_e5m2_decode.argtypes = [p, u64, p, u64]
+    lib.orc_e5m2_decode.restype = ctypes.c_int
+    for f in ("orc_split", "orc_merge", "orc_histogram", "orc_top16", "orc_luts", "orc_calibrate",
+              "orc_e5m2_split", "orc_e5m2_merge", "orc_e5m2_histogram", "orc_e5m2_calibrate"):
         getattr(lib, f).restype = None
     if path is None:
         _lib = lib
@@ -150,4 +166,55 @@ class Oracle:
         s = np.ascontiguousarray(stream, np.uint8)
         x = np.zeros(max(n, 1), np.uint16)
         rc = self.lib.orc_decode(_ptr(s), s.size, _ptr(x), n)
+        return rc, x[:n]
+
+    # ------------------------------------------------ FP8 E5M2 (page §4.2, appendix C)
+
+    def e5m2_split(self, x):
+        x = np.ascontiguousarray(x, np.uint8).reshape(-1)
+        e = np.empty(x.size, np.uint8)
+        a = np.empty(x.size, np.uint8)
+        self.lib.orc_e5m2_split(_ptr(x), x.size, _ptr(e), _ptr(a))
+        return e, a
+
+    def e5m2_merge(self, a, e):
+        a = np.ascontiguousarray(a, np.uint8)
+        e = np.ascontiguousarray(e, np.uint8)
+        x = np.empty(a.size, np.uint8)
+        self.lib.orc_e5m2_merge(_ptr(a), _ptr(e), a.size, _ptr(x))
+        return x
+
+    def e5m2_histogram(self, x):
+        x = np.ascontiguousarray(x, np.uint8).reshape(-1)
+        h = np.zeros(256, np.uint64)
+        self.lib.orc_e5m2_histogram(_ptr(x), x.size, _ptr(h))
+        return h
+
+    def e5m2_calibrate(self, sample):
+        x = np.ascontiguousarray(sample, np.uint8).reshape(-1)
+        exps = np.zeros(16, np.uint8)
+        self.lib.orc_e5m2_calibrate(_ptr(x), x.size, _ptr(exps))
+        return exps
+
+    def e5m2_stream_bytes(self, n, m, chunk):
+        return int(self.lib.orc_e5m2_stream_bytes(n, m, chunk))
+
+    def e5m2_encode(self, x, exps, chunk=1024, cap=None):
+        """Return (status, stream bytes as a uint8 array)."""
+        x = np.ascontiguousarray(x, np.uint8).reshape(-1)
+        exps = np.ascontiguousarray(exps, np.uint8)
+        if cap is None:
+            cap = self.e5m2_stream_bytes(x.size, x.size, chunk) if 8 <= chunk <= 65536 and chunk % 8 == 0 else 64
+        out = np.zeros(max(cap, 1), np.uint8)
+        nbytes = ctypes.c_uint64(0)
+        rc = self.lib.orc_e5m2_encode(_ptr(x), x.size, chunk, _ptr(exps), _ptr(out), cap, ctypes.byref(nbytes))
+        if rc != OK:
+            return rc, None
+        return rc, out[: nbytes.value].copy()
+
+    def e5m2_decode(self, stream, n):
+        """Return (status, uint8 array of n E5M2 values)."""
+        s = np.ascontiguousarray(stream, np.uint8)
+        x = np.zeros(max(n, 1), np.uint8)
+        rc = self.lib.orc_e5m2_decode(_ptr(s), s.size, _ptr(x), n)
         return rc, x[:n]

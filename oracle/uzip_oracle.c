@@ -319,3 +319,192 @@ int orc_decode(const uint8_t *in, uint64_t in_bytes, uint16_t *x, uint64_t n)
     }
     return ORC_OK;
 }
+
+/* ====================================================== FP8 E5M2 variant
+ *
+ * Source page §4.2 and appendix C: the same Top-16 framework applied to FP8
+ * E5M2 KV values compresses them a further 1.14x. An E5M2 value is one byte:
+ * sign (bit 7), 5-bit exponent (bits 6..2), 2-bit mantissa (bits 1..0).
+ * Readings (choices, not facts of the page):
+ *   - split e = (x >> 2) & 0x1f and a 3-bit sign-mantissa field
+ *     a = ((x >> 5) & 4) | (x & 3); rebuild x = ((a & 4) << 5) | (e << 2) | (a & 3);
+ *   - the Top-16 of the 5-bit exponents is chosen with the same rules as for
+ *     BF16 (count descending, smaller exponent first; unseen exponents fill in
+ *     ascending order), over a 256-bin histogram whose bins 32..255 stay 0;
+ *   - the 3-bit fields of values 8j .. 8j+7 form the 24-bit little-endian
+ *     word sum(a_{8j+i} << 3i) at bytes 3j .. 3j+2 (a partial last group
+ *     padded with zero fields): 3 bytes per 8 values, so 7 bits per value with
+ *     the 4-bit code, i.e. 8/7 = 1.14x before escapes;
+ *   - codes, chunk offsets and escape blocks exactly as for BF16, the raw
+ *     exponent of an escape in a whole byte;
+ *   - the stream is a 64-byte header with magic "UZE1" (otherwise as for
+ *     BF16), the packed fields, the codes, the offsets and the escape blocks,
+ *     the first four parts padded with zeros to a multiple of 16 bytes. */
+
+static uint8_t e5m2_exponent(uint8_t x) { return (uint8_t)((x >> 2) & 0x1F); }
+
+static uint8_t e5m2_sign_mantissa(uint8_t x) { return (uint8_t)(((x >> 5) & 4) | (x & 3)); }
+
+static uint8_t e5m2_rebuild(uint8_t a, uint8_t e) { return (uint8_t)(((a & 4) << 5) | ((e & 0x1F) << 2) | (a & 3)); }
+
+void orc_e5m2_split(const uint8_t *x, uint64_t n, uint8_t *e, uint8_t *a)
+{
+    for (uint64_t i = 0; i < n; i++) {
+        e[i] = e5m2_exponent(x[i]);
+        a[i] = e5m2_sign_mantissa(x[i]);
+    }
+}
+
+void orc_e5m2_merge(const uint8_t *a, const uint8_t *e, uint64_t n, uint8_t *x)
+{
+    for (uint64_t i = 0; i < n; i++) x[i] = e5m2_rebuild(a[i], e[i]);
+}
+
+void orc_e5m2_histogram(const uint8_t *x, uint64_t n, uint64_t *hist)
+{
+    for (int b = 0; b < 256; b++) hist[b] = 0;
+    for (uint64_t i = 0; i < n; i++) hist[e5m2_exponent(x[i])]++;
+}
+
+void orc_e5m2_calibrate(const uint8_t *x, uint64_t n, uint8_t *exps)
+{
+    uint64_t hist[256];
+    orc_e5m2_histogram(x, n, hist);
+    orc_top16(hist, exps);
+}
+
+static layout_t e5m2_layout_of(uint64_t n, uint32_t chunk)
+{
+    layout_t L;
+    L.n = n;
+    L.nc = (n + chunk - 1) / chunk;
+    L.off_a = 64;
+    L.off_b = L.off_a + pad16(3 * ((n + 7) / 8));
+    L.off_c = L.off_b + pad16((n + 1) / 2);
+    L.off_d = L.off_c + pad16(4 * (L.nc + 1));
+    return L;
+}
+
+uint64_t orc_e5m2_stream_bytes(uint64_t n, uint64_t m, uint32_t chunk)
+{
+    if (!chunk_ok(chunk)) return 0;
+    return e5m2_layout_of(n, chunk).off_d + 3 * m;
+}
+
+int orc_e5m2_encode(const uint8_t *x, uint64_t n, uint32_t chunk, const uint8_t *exps, uint8_t *out, uint64_t cap,
+                    uint64_t *out_bytes)
+{
+    if (!chunk_ok(chunk)) return ORC_ERR_CHUNK;
+    if (n >= ((uint64_t)1 << 32)) return ORC_ERR_ARG;
+    if (n > 0 && x == NULL) return ORC_ERR_ARG;
+    if (out == NULL || exps == NULL) return ORC_ERR_ARG;
+    uint8_t enc[256], dec[16], esc[256];
+    orc_luts(exps, enc, dec, esc);
+    layout_t L = e5m2_layout_of(n, chunk);
+    uint64_t m = 0;
+    for (uint64_t i = 0; i < n; i++) m += esc[e5m2_exponent(x[i])];
+    uint64_t total = L.off_d + 3 * m;
+    if (out_bytes) *out_bytes = total;
+    if (total > cap) return ORC_ERR_CAPACITY;
+    memset(out, 0, total);
+
+    /* Dense: each 3-bit field into its group's 24-bit word, each exponent
+     * through the code table, two codes per byte. */
+    uint8_t *A = out + L.off_a;
+    uint8_t *B = out + L.off_b;
+    for (uint64_t i = 0; i < n; i++) {
+        uint32_t bit = 3 * (uint32_t)(i % 8);
+        uint8_t *w = A + 3 * (i / 8);
+        uint32_t word = (uint32_t)w[0] | ((uint32_t)w[1] << 8) | ((uint32_t)w[2] << 16);
+        word |= (uint32_t)e5m2_sign_mantissa(x[i]) << bit;
+        w[0] = (uint8_t)(word & 0xFF);
+        w[1] = (uint8_t)((word >> 8) & 0xFF);
+        w[2] = (uint8_t)((word >> 16) & 0xFF);
+        uint8_t code = enc[e5m2_exponent(x[i])];
+        if (i % 2 == 0)
+            B[i / 2] = code;
+        else
+            B[i / 2] = (uint8_t)(B[i / 2] | (code << 4));
+    }
+
+    /* Escapes, chunk by chunk, as for BF16. */
+    uint8_t *C = out + L.off_c;
+    uint8_t *D = out + L.off_d;
+    uint64_t running = 0;
+    for (uint64_t c = 0; c < L.nc; c++) {
+        uint64_t start = c * chunk;
+        uint64_t end = start + chunk < n ? start + chunk : n;
+        uint64_t k = 0;
+        for (uint64_t i = start; i < end; i++) k += esc[e5m2_exponent(x[i])];
+        put_u32(C + 4 * c, (uint32_t)running);
+        uint8_t *block = D + 3 * running;
+        uint64_t j = 0;
+        for (uint64_t i = start; i < end; i++) {
+            uint8_t e = e5m2_exponent(x[i]);
+            if (!esc[e]) continue;
+            put_u16(block + 2 * j, (uint32_t)(i - start));
+            block[2 * k + j] = e;
+            j++;
+        }
+        running += k;
+    }
+    put_u32(C + 4 * L.nc, (uint32_t)running);
+
+    memcpy(out, "UZE1", 4);
+    out[4] = 1;
+    out[5] = 0;
+    put_u64(out + 8, n);
+    put_u32(out + 16, chunk);
+    put_u32(out + 20, (uint32_t)L.nc);
+    put_u64(out + 24, m);
+    memcpy(out + 32, exps, 16);
+    put_u64(out + 48, total);
+    return ORC_OK;
+}
+
+int orc_e5m2_decode(const uint8_t *in, uint64_t in_bytes, uint8_t *x, uint64_t n)
+{
+    if (in == NULL || (n > 0 && x == NULL)) return ORC_ERR_ARG;
+    if (in_bytes < 64) return ORC_ERR_CORRUPT;
+    if (memcmp(in, "UZE1", 4) != 0 || get_u16(in + 4) != 1 || get_u16(in + 6) != 0) return ORC_ERR_CORRUPT;
+    uint64_t hn = get_u64(in + 8);
+    uint32_t chunk = get_u32(in + 16);
+    uint64_t nc = get_u32(in + 20);
+    uint64_t m = get_u64(in + 24);
+    uint64_t total = get_u64(in + 48);
+    if (hn != n || !chunk_ok(chunk) || n >= ((uint64_t)1 << 32)) return ORC_ERR_CORRUPT;
+    layout_t L = e5m2_layout_of(n, chunk);
+    if (nc != L.nc || m > n || total != L.off_d + 3 * m || total > in_bytes) return ORC_ERR_CORRUPT;
+    const uint8_t *dec = in + 32;
+    const uint8_t *A = in + L.off_a;
+    const uint8_t *B = in + L.off_b;
+    const uint8_t *C = in + L.off_c;
+    const uint8_t *D = in + L.off_d;
+    if (get_u32(C) != 0 || get_u32(C + 4 * nc) != m) return ORC_ERR_CORRUPT;
+    for (uint64_t c = 0; c < nc; c++)
+        if (get_u32(C + 4 * c) > get_u32(C + 4 * (c + 1))) return ORC_ERR_CORRUPT;
+
+    /* Dense: field and code of every value, rebuilt with the decoded exponent. */
+    for (uint64_t i = 0; i < n; i++) {
+        const uint8_t *w = A + 3 * (i / 8);
+        uint32_t word = (uint32_t)w[0] | ((uint32_t)w[1] << 8) | ((uint32_t)w[2] << 16);
+        uint8_t a = (uint8_t)((word >> (3 * (i % 8))) & 7);
+        uint8_t code = (uint8_t)((B[i / 2] >> (4 * (i % 2))) & 0x0F);
+        x[i] = e5m2_rebuild(a, dec[code]);
+    }
+    /* Sparse fix-up of the escapes. */
+    for (uint64_t c = 0; c < nc; c++) {
+        uint64_t o = get_u32(C + 4 * c);
+        uint64_t k = get_u32(C + 4 * (c + 1)) - o;
+        uint64_t start = c * chunk;
+        uint64_t len = start + chunk < n ? chunk : n - start;
+        if (k > len) return ORC_ERR_CORRUPT;
+        const uint8_t *block = D + 3 * o;
+        for (uint64_t j = 0; j < k; j++) {
+            uint64_t pos = get_u16(block + 2 * j);
+            if (pos >= len) return ORC_ERR_CORRUPT;
+            x[start + pos] = (uint8_t)((x[start + pos] & 0x83) | ((block[2 * k + j] & 0x1F) << 2));
+        }
+    }
+    return ORC_OK;
+}

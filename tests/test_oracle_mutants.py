@@ -15,6 +15,7 @@ import pytest
 import oracle
 
 HERE = os.path.dirname(os.path.abspath(__file__))
+E5M2_MARKER = "/* ====================================================== FP8 E5M2 variant"
 
 MUTANTS = {
     "exponent shift": ("return (uint8_t)((x >> 7) & 0xFF);", "return (uint8_t)((x >> 8) & 0xFF);"),
@@ -81,9 +82,10 @@ def test_battery_passes_on_the_real_oracle():
 def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(os.path.join(os.path.dirname(HERE), "oracle", "uzip_oracle.c")).read()
-    assert src.count(old) == 1, f"mutation site for {name!r} not unique"
+    head, tail = src.split(E5M2_MARKER, 1)  # the BF16 part, then the E5M2 variant
+    assert head.count(old) == 1, f"mutation site for {name!r} not unique"
     mut_src = tmp_path / "mutant.c"
-    mut_src.write_text(src.replace(old, new))
+    mut_src.write_text(head.replace(old, new) + E5M2_MARKER + tail)
     lib = oracle.build(force=True, src=str(mut_src), out=str(tmp_path / "libmutant.so"))
     r = _run_battery(lib)
     assert r.returncode != 0, f"mutant {name!r} survived the pins:\n{r.stdout}{r.stderr}"
