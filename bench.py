@@ -678,13 +678,78 @@ def run_chunks(args):
             "config": {"workload": WORKLOAD, "value": "decode GB/s at chunk 1024"}, "rows": rows}
 
 
+def run_e5m2(args):
+    """FP8 E5M2 codec (SplitZip review page, §4.2 / appendix C: the Top-16
+    framework on E5M2 KV, a further 1.14x): the KV-cache law quantised to
+    E5M2 (268,435,456 one-byte values), encode and decode timed back to back."""
+    import statistics as stats
+
+    import torch
+
+    import lossless_bf16_exponent_gb300 as uz
+    import lossless_bf16_exponent_gb300.workloads as W
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist("nccl")
+    uz.load()
+    x, sample = W.workload_e5m2(device=dev)
+    n = x.numel()
+    cb = uz.e5m2_calibrate(sample)
+    out = torch.empty(uz.e5m2_compressed_size(n, n, CHUNK), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(uz.workspace_bytes(n, CHUNK), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(x)
+    _, nbytes = uz.e5m2_encode(x, cb, CHUNK, out=out, workspace=wsb)
+    uz.e5m2_decode(out, n, out=y, stream_bytes=nbytes)
+    assert torch.equal(y, x), "E5M2 round trip is not bit-exact"
+    m = int.from_bytes(bytes(out[24:32].cpu().numpy()), "little")
+    st = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        uz.e5m2_encode(x, cb, CHUNK, out=out, workspace=wsb, sync=False)
+        uz.e5m2_decode(out, n, out=y, stream_bytes=nbytes)
+    reps = max(10, min(args.steps, 200))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    barrier()
+    torch.cuda.synchronize()
+    for ev in evs:
+        ev[0].record(st)
+        uz.e5m2_encode(x, cb, CHUNK, out=out, workspace=wsb, sync=False)
+        ev[1].record(st)
+        uz.e5m2_decode(out, n, out=y, stream_bytes=nbytes)
+        ev[2].record(st)
+    torch.cuda.synchronize()
+    te = stats.mean(e[0].elapsed_time(e[1]) for e in evs)
+    td = stats.mean(e[1].elapsed_time(e[2]) for e in evs)
+    step_ms = max_over_ranks(evs[0][0].elapsed_time(evs[-1][2]) / reps, dev)
+    if rank != 0:
+        return None
+    peak, peak_src = measured_peak()
+    alg = n + nbytes
+    enc_gbs, dec_gbs = alg / (te * 1e-3) / 1e9, alg / (td * 1e-3) / 1e9
+    dom, gbs = ("encode", enc_gbs) if te >= td else ("decode", dec_gbs)
+    return {
+        "mode": "e5m2", "metric": "E5M2 encode/decode GB/s (raw FP8 bytes) @256M elems; ratio",
+        "value": round(n * ws / (step_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": ws, "steps": reps,
+        "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "kv_cache [64,2,8,2048,128] quantised to FP8 E5M2 = 268,435,456 values, chunk 1024",
+                   "step": "encode + decode"},
+        "encode_us": round(te * 1e3, 2), "decode_us": round(td * 1e3, 2),
+        "encode_gbs_raw": round(n / (te * 1e-3) / 1e9, 1), "decode_gbs_raw": round(n / (td * 1e-3) / 1e9, 1),
+        "ratio": round(n / nbytes, 5), "escape_rate": m / n, "page_ratio": 1.14,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "peak_source": peak_src, "algorithmic_bytes": alg},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["codec", "dynamic", "pipeline", "chunks"], default="codec",
+    ap.add_argument("--mode", choices=["codec", "dynamic", "pipeline", "chunks", "e5m2"], default="codec",
                     help="codec = the benchmark step; dynamic = per-input codebook encode; "
                          "pipeline = streamed compressed transfer (next rows)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -702,6 +767,8 @@ def main(argv=None):
         line = run_pipeline(args)
     elif args.mode == "chunks":
         line = run_chunks(args)
+    elif args.mode == "e5m2":
+        line = run_e5m2(args)
     else:
         line = run_ours(args)
     if line is not None:

@@ -231,6 +231,37 @@ UZIP_API int uzip_decode(const void *d_stream, size_t stream_bytes, void *d_out_
 UZIP_API int uzip_stream_copy(const void *src_stream, void *dst, size_t capacity,
                               unsigned long long *d_copied, uzip_stream_t stream);
 
+/* ------------------------------------------------------------ FP8 E5M2
+ * The same Top-16 framework on FP8 E5M2 values (§4.2, appendix C: "a further
+ * 1.14x on FP8 KV"). An E5M2 byte x splits into its 5-bit exponent
+ * e = (x >> 2) & 0x1f and a 3-bit sign-mantissa field a = sign << 2 | mantissa;
+ * the stream is laid out as for BF16 with magic "UZE1" and a sign-mantissa
+ * section of 3 * ceil(n / 8) bytes (the 3-bit fields of values 8j .. 8j+7 form
+ * the 24-bit little-endian word sum(a_{8j+i} << 3i) at bytes 3j .. 3j+2);
+ * codes, offsets and escape blocks (raw 5-bit exponent in a byte) as for
+ * BF16. Size 64 + A16(3 ceil(n/8)) + A16(ceil(n/2)) + A16(4(nc+1)) + 3M.
+ * Codebook blobs have the BF16 layout (exponents 0..31 only); a workspace of
+ * uzip_encode_workspace_bytes(n, chunk) bytes serves uzip_e5m2_encode. */
+
+/* Calibrate a codebook from n_sample E5M2 bytes (as uzip_calibrate). */
+UZIP_API int uzip_e5m2_calibrate(const void *d_sample_e5m2, size_t n_sample, void *d_codebook,
+                                 uzip_stream_t stream);
+
+/* Exact E5M2 stream bytes for n values with n_escapes escapes; 0 on invalid
+ * arguments. Host only. */
+UZIP_API size_t uzip_e5m2_compressed_size(size_t n, size_t n_escapes, uint32_t chunk);
+
+/* Encode n E5M2 values (16-byte aligned bytes); arguments, output and errors
+ * as uzip_encode's. */
+UZIP_API int uzip_e5m2_encode(const void *d_in_e5m2, size_t n, uint32_t chunk, const void *d_codebook,
+                              void *d_out, size_t out_capacity, void *d_workspace, size_t workspace_bytes,
+                              size_t *h_out_bytes, uzip_stream_t stream);
+
+/* Decode an E5M2 stream into n bytes; arguments, checks and errors as
+ * uzip_decode's (a BF16 stream is refused as corrupt, and vice versa). */
+UZIP_API int uzip_e5m2_decode(const void *d_stream, size_t stream_bytes, void *d_out_e5m2, size_t n,
+                              uint32_t *d_status, uzip_stream_t stream);
+
 /* Host view of a stream header. */
 typedef struct {
     uint64_t n;

@@ -7,11 +7,13 @@ load the library; the first codec call does, and fails loudly if it is
 missing.
 """
 from .codec import (CODEBOOK_BYTES, HEADER_BYTES, UzipError, calibrate, codebook_exps, codebook_from_exps,
-                    codebook_histogram, compressed_size, decode, encode, encode_dynamic, load, max_compressed_size,
-                    new_codebook, roundtrip_ok, stream_copy, stream_info, workspace_bytes)
+                    codebook_histogram, compressed_size, decode, e5m2_calibrate, e5m2_compressed_size,
+                    e5m2_decode, e5m2_encode, encode, encode_dynamic, load, max_compressed_size, new_codebook,
+                    roundtrip_ok, stream_copy, stream_info, workspace_bytes)
 
 __all__ = [
     "CODEBOOK_BYTES", "HEADER_BYTES", "UzipError", "calibrate", "codebook_exps", "codebook_from_exps",
-    "codebook_histogram", "compressed_size", "decode", "encode", "encode_dynamic", "load", "max_compressed_size",
+    "codebook_histogram", "compressed_size", "decode", "e5m2_calibrate", "e5m2_compressed_size", "e5m2_decode",
+    "e5m2_encode", "encode", "encode_dynamic", "load", "max_compressed_size",
     "new_codebook", "roundtrip_ok", "stream_copy", "stream_info", "workspace_bytes",
 ]

@@ -20,7 +20,8 @@ MAX_N = 0xFFFFFFFF
 EXPORTS = (
     "uzip_calibrate", "uzip_codebook_from_exps", "uzip_compressed_size", "uzip_encode_workspace_bytes",
     "uzip_encode", "uzip_encode_noalloc", "uzip_encode_dynamic", "uzip_decode", "uzip_stream_copy",
-    "uzip_stream_info", "uzip_status_string",
+    "uzip_stream_info", "uzip_status_string", "uzip_e5m2_calibrate", "uzip_e5m2_compressed_size",
+    "uzip_e5m2_encode", "uzip_e5m2_decode",
     "uzip_version",
 )
 NOALLOC_MAX_N = 1 << 25
@@ -68,13 +69,19 @@ def load(path: str | None = None):
     L.uzip_encode_noalloc.argtypes = [vp, sz, u32, vp, vp, sz, ctypes.POINTER(sz), vp]
     L.uzip_encode_dynamic.argtypes = [vp, sz, u32, vp, vp, sz, vp, sz, ctypes.POINTER(sz), vp]
     L.uzip_stream_copy.argtypes = [vp, vp, sz, vp, vp]
+    L.uzip_e5m2_calibrate.argtypes = [vp, sz, vp, vp]
+    L.uzip_e5m2_compressed_size.argtypes = [sz, sz, u32]
+    L.uzip_e5m2_compressed_size.restype = sz
+    L.uzip_e5m2_encode.argtypes = [vp, sz, u32, vp, vp, sz, vp, sz, ctypes.POINTER(sz), vp]
+    L.uzip_e5m2_decode.argtypes = [vp, sz, vp, sz, vp, vp]
     L.uzip_decode.argtypes = [vp, sz, vp, sz, vp, vp]
     L.uzip_stream_info.argtypes = [vp, sz, ctypes.POINTER(Info), vp]
     L.uzip_status_string.argtypes = [i]
     L.uzip_status_string.restype = ctypes.c_char_p
     L.uzip_version.argtypes = []
     for f in ("uzip_calibrate", "uzip_codebook_from_exps", "uzip_encode", "uzip_encode_noalloc",
-              "uzip_encode_dynamic", "uzip_decode", "uzip_stream_copy", "uzip_stream_info", "uzip_version"):
+              "uzip_encode_dynamic", "uzip_decode", "uzip_stream_copy", "uzip_stream_info", "uzip_version",
+              "uzip_e5m2_calibrate", "uzip_e5m2_encode", "uzip_e5m2_decode"):
         getattr(L, f).restype = i
     if path is None:
         _lib = L

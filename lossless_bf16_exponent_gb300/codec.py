@@ -169,3 +169,55 @@ __all__ = [
     "codebook_exps", "codebook_histogram", "compressed_size", "max_compressed_size", "workspace_bytes",
     "encode", "decode", "stream_info", "roundtrip_ok",
 ]
+
+
+# ------------------------------------------------------------ FP8 E5M2
+
+def _flat8(x: torch.Tensor) -> torch.Tensor:
+    if not x.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if x.element_size() != 1:
+        raise TypeError("expected one-byte FP8 E5M2 values (torch.float8_e5m2 or uint8 bit patterns)")
+    if not x.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return x.reshape(-1).view(torch.uint8)
+
+
+def e5m2_calibrate(sample: torch.Tensor, codebook: torch.Tensor | None = None) -> torch.Tensor:
+    """Codebook from E5M2 values (SplitZip §4.2 / appendix C)."""
+    s = _flat8(sample)
+    cb = new_codebook(s.device) if codebook is None else codebook
+    check(load().uzip_e5m2_calibrate(_p(s), s.numel(), _p(cb), _sp(s.device)), "uzip_e5m2_calibrate")
+    return cb
+
+
+def e5m2_compressed_size(n: int, n_escapes: int, chunk: int = 1024) -> int:
+    return int(load().uzip_e5m2_compressed_size(n, n_escapes, chunk))
+
+
+def e5m2_encode(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, out: torch.Tensor | None = None,
+                workspace: torch.Tensor | None = None, sync: bool = True):
+    """Encode E5M2 values; returns ``(stream, nbytes)`` as :func:`encode`."""
+    v = _flat8(x)
+    n = v.numel()
+    if out is None:
+        out = torch.empty(e5m2_compressed_size(n, n, chunk), dtype=torch.uint8, device=v.device)
+    if workspace is None:
+        workspace = torch.empty(max(16, workspace_bytes(n, chunk)), dtype=torch.uint8, device=v.device)
+    nbytes = ctypes.c_size_t(0)
+    args = (_p(v), n, chunk, _p(codebook), _p(out), out.numel(), _p(workspace), workspace.numel(),
+            ctypes.byref(nbytes) if sync else None)
+    check(load().uzip_e5m2_encode(*args, _sp(v.device)), "uzip_e5m2_encode")
+    return out, (nbytes.value if sync else None)
+
+
+def e5m2_decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = None, status: torch.Tensor | None = None,
+                stream_bytes: int | None = None) -> torch.Tensor:
+    """Decode an E5M2 stream into ``n`` bytes (uint8 bit patterns)."""
+    if out is None:
+        out = torch.empty(max(n, 1), dtype=torch.uint8, device=stream.device)[:n]
+    o = _flat8(out) if n else out
+    nb = stream.numel() if stream_bytes is None else stream_bytes
+    check(load().uzip_e5m2_decode(_p(stream), nb, _p(o) if n else None, n, _p(status), _sp(stream.device)),
+          "uzip_e5m2_decode")
+    return out

@@ -43,8 +43,12 @@ constexpr uint32_t kCbCounter = UZIP_CB_HIST + 256 * 8;
 
 __device__ void rank_and_write(uint8_t* cb, uint64_t n_sample);
 
-__global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const uint16_t* __restrict__ x, uint64_t n,
+// kFmt: kBF16 (8 values per 16-byte load, exponent bits 14..7) or kE5M2 (16
+// values per load, exponent bits 6..2 of each byte).
+template <int kFmt>
+__global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const void* __restrict__ xv, uint64_t n,
                                                                  uint8_t* __restrict__ cb) {
+    constexpr uint32_t kPerVec = kFmt == kE5M2 ? 16 : 8;
     __shared__ uint32_t sh[kHistWarps][256];
     __shared__ bool s_last;
     unsigned long long* hist = reinterpret_cast<unsigned long long*>(cb + UZIP_CB_HIST);
@@ -53,7 +57,7 @@ __global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const uint16_t*
     __syncthreads();
     uint32_t* h = sh[threadIdx.x / 32];
 
-    const uint64_t groups = n / 8;
+    const uint64_t groups = n / kPerVec;
     const uint64_t stride = (uint64_t)gridDim.x * kHistThreads * kLoadsPerThread;
     // Group g of a round is lane + 32 * (warp + kHistWarps * (j + kLoadsPerThread * block)); the
     // trip count is warp-uniform so __match_any_sync always sees the full warp.
@@ -66,23 +70,32 @@ __global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const uint16_t*
         for (int j = 0; j < kLoadsPerThread; j++) {
             const uint64_t g = base + first + (uint64_t)j * kHistThreads;
             valid[j] = g < groups;
-            v[j] = valid[j] ? ld_stream_v4(x + 8 * g) : make_uint4(0, 0, 0, 0);
+            v[j] = valid[j] ? ld_stream_v4(static_cast<const uint8_t*>(xv) + 16 * g) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int j = 0; j < kLoadsPerThread; j++) {
             const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
             for (int q = 0; q < 4; q++) {
-                warp_hist_add(h, (w[q] >> 7) & 0xFF, valid[j]);
-                warp_hist_add(h, (w[q] >> 23) & 0xFF, valid[j]);
+                if (kFmt == kE5M2) {
+#pragma unroll
+                    for (int b = 0; b < 4; b++) warp_hist_add(h, (w[q] >> (8 * b + 2)) & 0x1F, valid[j]);
+                } else {
+                    warp_hist_add(h, (w[q] >> 7) & 0xFF, valid[j]);
+                    warp_hist_add(h, (w[q] >> 23) & 0xFF, valid[j]);
+                }
             }
         }
     }
-    // Ragged tail (< 8 values): block 0's first warp.
+    // Ragged tail (< kPerVec values): block 0's first warp.
     if (blockIdx.x == 0 && threadIdx.x < 32) {
-        const uint64_t i = groups * 8 + threadIdx.x;
-        const bool valid = i < n && threadIdx.x < 8;
-        warp_hist_add(h, valid ? (uint32_t)(x[i] >> 7) & 0xFF : 0, valid);
+        const uint64_t i = groups * kPerVec + threadIdx.x;
+        const bool valid = i < n && threadIdx.x < kPerVec;
+        uint32_t e = 0;
+        if (valid)
+            e = kFmt == kE5M2 ? (static_cast<const uint8_t*>(xv)[i] >> 2) & 0x1F
+                              : (static_cast<const uint16_t*>(xv)[i] >> 7) & 0xFF;
+        warp_hist_add(h, e, valid);
     }
     __syncthreads();
     for (int b = threadIdx.x; b < 256; b += kHistThreads) {
@@ -166,7 +179,7 @@ using namespace uzip;
 
 namespace uzip {
 
-int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook, cudaStream_t s) {
+int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook, cudaStream_t s, uint32_t fmt) {
     if (!d_codebook || (n_sample > 0 && !d_sample_bf16)) return UZIP_ERR_ARG;
     if (!aligned16(d_codebook) || (n_sample > 0 && !aligned16(d_sample_bf16))) return UZIP_ERR_ALIGN;
     uint8_t* cb = static_cast<uint8_t*>(d_codebook);
@@ -175,15 +188,16 @@ int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
     int dev = 0, sms = 0, per_sm = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
     UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, calibrate_kernel, kHistThreads, 0));
-    // One block per 8192 values, up to a full resident wave: a small sample
-    // is a latency chain, a whole tensor is read at HBM speed.
-    const uint64_t per_block = (uint64_t)kHistThreads * kLoadsPerThread * 8;
+    auto* kernel = fmt == kE5M2 ? calibrate_kernel<kE5M2> : calibrate_kernel<kBF16>;
+    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kHistThreads, 0));
+    // One block per kHistThreads * kLoadsPerThread 16-byte loads, up to a
+    // full resident wave: a small sample is a latency chain, a whole tensor
+    // is read at HBM speed.
+    const uint64_t per_block = (uint64_t)kHistThreads * kLoadsPerThread * (fmt == kE5M2 ? 16 : 8);
     uint64_t blocks = (n_sample + per_block - 1) / per_block;
     blocks = std::min<uint64_t>(blocks, (uint64_t)sms * std::max(per_sm, 1));
     if (blocks == 0) blocks = 1;
-    calibrate_kernel<<<(unsigned)blocks, kHistThreads, 0, s>>>(static_cast<const uint16_t*>(d_sample_bf16),
-                                                                n_sample, cb);
+    kernel<<<(unsigned)blocks, kHistThreads, 0, s>>>(d_sample_bf16, n_sample, cb);
     UZIP_CUDA_TRY(cudaGetLastError());
     return UZIP_OK;
 }
@@ -193,6 +207,11 @@ int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
 extern "C" UZIP_API int uzip_calibrate(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
                                        uzip_stream_t stream) {
     return calibrate_impl(d_sample_bf16, n_sample, d_codebook, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" UZIP_API int uzip_e5m2_calibrate(const void* d_sample_e5m2, size_t n_sample, void* d_codebook,
+                                            uzip_stream_t stream) {
+    return calibrate_impl(d_sample_e5m2, n_sample, d_codebook, reinterpret_cast<cudaStream_t>(stream), kE5M2);
 }
 
 extern "C" UZIP_API int uzip_codebook_from_exps(const uint8_t* h_exps16, void* d_codebook,

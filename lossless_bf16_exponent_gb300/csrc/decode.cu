@@ -203,15 +203,157 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
     if (s_bad && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
 }
 
+// ------------------------------------------------------------ FP8 E5M2
+
+// Twelve bits of packed 3-bit fields (four values) -> four bytes, field i in
+// byte i.
+__device__ __forceinline__ uint32_t spread_fields4(uint32_t f12) {
+    const uint32_t lo = f12 & 0x3F, hi = (f12 >> 6) & 0x3F;
+    return ((lo & 7) | ((lo & 0x38) << 5)) | (((hi & 7) | ((hi & 0x38) << 5)) << 16);
+}
+
+// Decoder for FP8 E5M2 streams (page §4.2 / appendix C): tiles of 8192
+// values as in decode_kernel, each thread taking 32 consecutive values (12
+// bytes of packed sign-mantissa fields, 16 bytes of codes, 32 bytes out);
+// the escape fix-up goes through shared memory as for BF16.
+__global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_kernel(const Params p) {
+    static_assert(kTile == kThreads * 32, "one 32-value slot per thread");
+    __shared__ uint32_t s_mask[2][kTile / 32];
+    __shared__ uint8_t s_val[kTile];
+    __shared__ int s_bad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint4* h = reinterpret_cast<const uint4*>(p.s);
+    const uint4 h0 = h[0], h1 = h[1], h2 = h[2], h3 = h[3];
+    const uint64_t hn = (uint64_t)h0.z | ((uint64_t)h0.w << 32);
+    const uint32_t chunk = h1.x;
+    const uint64_t nc = h1.y;
+    const uint64_t m = (uint64_t)h1.z | ((uint64_t)h1.w << 32);
+    const uint64_t total = (uint64_t)h3.x | ((uint64_t)h3.y << 32);
+    bool ok = h0.x == kStreamMagicE5 && (h0.y & 0xFFFF) == 1 && (h0.y >> 16) == 0 && hn == p.n &&
+              chunk_valid(chunk) && m <= hn;
+    Layout L;
+    if (ok) {
+        L = layout_e5m2_of(hn, chunk);
+        ok = nc == L.nc && total == L.off_d + 3 * m && total <= p.stream_bytes;
+    }
+    if (!ok) {
+        if (blockIdx.x == 0 && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
+        return;
+    }
+    const uint32_t n32 = (uint32_t)p.n;
+    const uint8_t* A = p.s + L.off_a;
+    const uint8_t* B = p.s + L.off_b;
+    const uint8_t* C = p.s + L.off_c;
+    const uint8_t* D = p.s + L.off_d;
+    uint8_t* out8 = reinterpret_cast<uint8_t*>(p.out);
+    const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;
+    const uint32_t tiles = (n32 + kTile - 1) / kTile;
+
+    for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[0][i] = 0;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    int par = 0;
+    for (uint32_t t = blockIdx.x; t < tiles; t += gridDim.x, par ^= 1) {
+        const uint32_t e0 = t * kTile;
+        const uint32_t tlen = min(kTile, n32 - e0);
+        const uint32_t v0 = 32 * tid;  // this thread's values e0 + v0 .. + 31
+        const bool mine = v0 < tlen;
+        // 1. dense loads (the padded sections keep a whole slot inside the stream)
+        uint32_t f[3] = {0, 0, 0};
+        uint4 cv = make_uint4(0, 0, 0, 0);
+        if (mine) {
+            const uint32_t* fa = reinterpret_cast<const uint32_t*>(A + (e0 / 8) * 3 + 12 * tid);
+            f[0] = __ldg(fa);
+            f[1] = __ldg(fa + 1);
+            f[2] = __ldg(fa + 2);
+            cv = __ldg(reinterpret_cast<const uint4*>(B + e0 / 2 + 16 * tid));
+        }
+        // 2. escapes of the chunks overlapping the tile -> shared memory
+        for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[par ^ 1][i] = 0;
+        const uint32_t c_first = e0 / chunk, c_last = (e0 + tlen - 1) / chunk;
+        bool bad = false;
+        for (uint32_t c = c_first + warp; c <= c_last; c += kThreads / 32) {
+            const uint32_t o = *reinterpret_cast<const uint32_t*>(C + 4ull * c);
+            const uint32_t o1 = *reinterpret_cast<const uint32_t*>(C + 4ull * (c + 1));
+            const uint32_t cbase = c * chunk;
+            const uint32_t clen = min(chunk, n32 - cbase);
+            if (o1 < o || o1 > m || o1 - o > clen) {
+                bad = true;
+                continue;
+            }
+            const uint32_t k = o1 - o;
+            const uint8_t* blk = D + 3ull * o;
+            for (uint32_t j = lane; j < k; j += 32) {
+                const uint32_t pos = (uint32_t)blk[2 * j] | ((uint32_t)blk[2 * j + 1] << 8);
+                if (pos >= clen) {
+                    bad = true;
+                    continue;
+                }
+                const uint32_t el = cbase + pos;
+                if (el >= e0 && el < e0 + tlen) {
+                    const uint32_t li = el - e0;
+                    s_val[li] = blk[2 * k + j];
+                    atomicOr(&s_mask[par][li >> 5], 1u << (li & 31));
+                }
+            }
+        }
+        if (bad) s_bad = 1;
+        __syncthreads();
+
+        // 3. decode the slot's 32 values, patch, store
+        if (mine) {
+            const uint32_t fix = s_mask[par][tid];
+            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+            const uint32_t g24[4] = {f[0] & 0xFFFFFF, ((f[0] >> 24) | (f[1] << 8)) & 0xFFFFFF,
+                                     ((f[1] >> 16) | (f[2] << 16)) & 0xFFFFFF, f[2] >> 8};
+            uint32_t o[8];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+#pragma unroll
+                for (int hh = 0; hh < 2; hh++) {
+                    uint32_t e4 = lookup4((cw[q] >> (16 * hh)) & 0xFFFF, d0, d1, d2, d3);
+                    const uint32_t bits = (fix >> (8 * q + 4 * hh)) & 0xF;
+                    if (bits) {
+#pragma unroll
+                        for (int i = 0; i < 4; i++)
+                            if (bits & (1u << i)) {
+                                const uint32_t sh = 8 * i;
+                                e4 = (e4 & ~(0xFFu << sh)) | ((uint32_t)s_val[v0 + 8 * q + 4 * hh + i] << sh);
+                            }
+                    }
+                    const uint32_t a4 = spread_fields4((g24[q] >> (12 * hh)) & 0xFFF);
+                    o[2 * q + hh] = ((a4 & 0x04040404u) << 5) | ((e4 & 0x1F1F1F1Fu) << 2) | (a4 & 0x03030303u);
+                }
+            }
+            const uint32_t ge = e0 + v0;
+            if (ge + 32 <= n32) {
+                uint4* dst = reinterpret_cast<uint4*>(out8 + ge);
+                dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            } else {
+#pragma unroll
+                for (uint32_t i = 0; i < 32; i++)
+                    if (ge + i < n32) out8[ge + i] = (uint8_t)(o[i / 4] >> (8 * (i & 3)));
+            }
+        }
+        __syncthreads();  // s_val and this bitmap are rewritten by the next tile
+    }
+    if (s_bad && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
+}
+
 }  // namespace
 }  // namespace uzip
 
 using namespace uzip;
 
-extern "C" UZIP_API int uzip_decode(const void* d_stream, size_t stream_bytes, void* d_out_bf16, size_t n,
-                                    uint32_t* d_status, uzip_stream_t stream) {
-    if (!d_stream || (n > 0 && !d_out_bf16) || n > UZIP_MAX_N) return UZIP_ERR_ARG;
-    if (!aligned16(d_stream) || (n > 0 && !aligned16(d_out_bf16)) ||
+namespace {
+
+int decode_launch(void (*kernel)(Params), const void* d_stream, size_t stream_bytes, void* d_out, size_t n,
+                  uint32_t* d_status, uzip_stream_t stream) {
+    if (!d_stream || (n > 0 && !d_out) || n > UZIP_MAX_N) return UZIP_ERR_ARG;
+    if (!aligned16(d_stream) || (n > 0 && !aligned16(d_out)) ||
         (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3)))
         return UZIP_ERR_ALIGN;
     if (stream_bytes < UZIP_HEADER_BYTES) return UZIP_ERR_CAPACITY;
@@ -220,17 +362,29 @@ extern "C" UZIP_API int uzip_decode(const void* d_stream, size_t stream_bytes, v
     Params p;
     p.s = static_cast<const uint8_t*>(d_stream);
     p.stream_bytes = stream_bytes;
-    p.out = static_cast<uint16_t*>(d_out_bf16);
+    p.out = static_cast<uint16_t*>(d_out);
     p.n = n;
     p.status = d_status;
     int dev = 0, sms = 0, per_sm = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
     UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel, kThreads, 0));
+    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0));
     if (per_sm < 1) return UZIP_ERR_CUDA;
     const uint64_t tiles = (n + kTile - 1) / kTile;
     const uint64_t grid = std::max<uint64_t>(1, std::min<uint64_t>(tiles, (uint64_t)sms * per_sm));
-    decode_kernel<<<(unsigned)grid, kThreads, 0, s>>>(p);
+    kernel<<<(unsigned)grid, kThreads, 0, s>>>(p);
     UZIP_CUDA_TRY(cudaGetLastError());
     return UZIP_OK;
+}
+
+}  // namespace
+
+extern "C" UZIP_API int uzip_decode(const void* d_stream, size_t stream_bytes, void* d_out_bf16, size_t n,
+                                    uint32_t* d_status, uzip_stream_t stream) {
+    return decode_launch(decode_kernel, d_stream, stream_bytes, d_out_bf16, n, d_status, stream);
+}
+
+extern "C" UZIP_API int uzip_e5m2_decode(const void* d_stream, size_t stream_bytes, void* d_out_e5m2, size_t n,
+                                         uint32_t* d_status, uzip_stream_t stream) {
+    return decode_launch(decode_e5m2_kernel, d_stream, stream_bytes, d_out_e5m2, n, d_status, stream);
 }

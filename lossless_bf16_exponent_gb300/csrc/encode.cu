@@ -95,7 +95,10 @@ __host__ __device__ constexpr Geometry geometry_of(uint64_t n) {
 }
 
 struct Params {
-    const uint16_t* in;
+    const uint16_t* in;   // BF16 input
+    const uint8_t* in8;   // FP8 E5M2 input
+    uint32_t fmt;         // kBF16 or kE5M2
+    uint64_t a_bytes;     // bytes of the sign-mantissa section (before its padding)
     uint64_t n;
     uint32_t chunk;
     uint32_t seg_units;   // units per segment
@@ -168,10 +171,16 @@ __device__ void write_header(const Params& p, uint64_t m, uint32_t flags) {
     uint4* h = reinterpret_cast<uint4*>(p.out);
     const uint64_t total = p.L.off_d + 3 * m;
     const uint4 exps = *reinterpret_cast<const uint4*>(p.cb + UZIP_CB_EXPS);
-    h[0] = make_uint4(kStreamMagic, 1u | (flags << 16), (uint32_t)p.n, (uint32_t)(p.n >> 32));
+    h[0] = make_uint4(p.fmt == kE5M2 ? kStreamMagicE5 : kStreamMagic, 1u | (flags << 16), (uint32_t)p.n,
+                      (uint32_t)(p.n >> 32));
     h[1] = make_uint4(p.chunk, (uint32_t)p.L.nc, (uint32_t)m, (uint32_t)(m >> 32));
     h[2] = exps;
     h[3] = make_uint4((uint32_t)total, (uint32_t)(total >> 32), 0u, 0u);
+}
+
+// Zero bytes [from, to) of the stream, byte by byte (a few padding bytes).
+__device__ void zero_bytes(uint8_t* out, uint64_t from, uint64_t to) {
+    for (uint64_t o = from; o < to; o++) out[o] = 0;
 }
 
 // Zero bytes [from, to) of the stream, 4-byte aligned bounds.
@@ -296,6 +305,154 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
             for (int it = 0; it < 2; it++)
 #pragma unroll
                 for (int r = 0; r < 4; r++) st_u8_keep(gmask + it * 128 + r * 32 + lane, (mbytes[it] >> (8 * r)) & 0xFF, keep);
+        }
+        if (lane == 0) {
+            st_u32_keep(p.counts + u, cnt, keep);
+            if (cnt) atomicAdd(&p.segs[u / p.seg_units], cnt);
+        }
+    }
+}
+
+// ------------------------------------------------------- FP8 E5M2 dense kernel
+
+// Eight E5M2 values (w0, w1: value i in byte i) -> their 8 codes (one word,
+// value i in nibble i), their 3-bit sign-mantissa fields (24 bits, value i at
+// bits 3i), the escape flags (bit 7 of byte i of esc_lo / esc_hi for value i /
+// i + 4) and the exponents (bytes of e_lo / e_hi).
+__device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, const uint8_t* tab, uint32_t& codes,
+                                                  uint32_t& fields, uint32_t& esc_lo, uint32_t& esc_hi,
+                                                  uint32_t& e_lo, uint32_t& e_hi) {
+    const uint32_t w[2] = {w0, w1};
+    uint32_t packed[2], esc[2], ex[2], f[2];
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+        const uint32_t e4 = (w[h] >> 2) & 0x1F1F1F1Fu;                      // exponent bytes
+        const uint32_t a4 = ((w[h] >> 5) & 0x04040404u) | (w[h] & 0x03030303u);  // sign << 2 | mantissa
+        const uint32_t pr = a4 | (a4 >> 5);  // bits 0..5: a0 | a1 << 3; bits 16..21: a2 | a3 << 3
+        f[h] = (pr & 0x3Fu) | ((pr >> 10) & 0xFC0u);
+        ex[h] = e4;
+        const uint32_t t0 = tab[e4 & 0xFF];
+        const uint32_t t1 = tab[prmt(e4, 0, 0x4441)];
+        const uint32_t t2 = tab[prmt(e4, 0, 0x4442)];
+        const uint32_t t3 = tab[e4 >> 24];
+        const uint32_t t4 = prmt(prmt(t0, t1, 0x0040), prmt(t2, t3, 0x0040), 0x5410);
+        const uint32_t c = t4 & 0x0F0F0F0Fu;
+        packed[h] = c | (c >> 4);
+        esc[h] = t4 & 0x80808080u;
+    }
+    codes = prmt(packed[0], packed[1], 0x6420);
+    fields = f[0] | (f[1] << 12);
+    esc_lo = esc[0];
+    esc_hi = esc[1];
+    e_lo = ex[0];
+    e_hi = ex[1];
+}
+
+// The dense pass for E5M2 input: as encode_dense_kernel, one warp per unit
+// of 2048 values in grid-stride order, but each lane takes 32 consecutive
+// values per step (two 16-byte loads; 12 bytes of packed fields and 16 bytes
+// of codes stored), so a row of the warp covers 1024 values in ascending
+// lane order and its escapes are ranked with one scan.
+__global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5m2_kernel(const Params p) {
+    __shared__ uint32_t s_tab_words[64];
+    uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_tab_words);
+    s_tab[threadIdx.x] = p.cb[UZIP_CB_ENC + threadIdx.x] | (p.cb[UZIP_CB_ESC + threadIdx.x] ? 0x80 : 0);
+    __syncthreads();
+    allow_dependent_launch();
+
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t stride = (uint64_t)gridDim.x * kWarps;
+    const uint64_t keep = l2_policy_evict_last();
+    for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride) {
+        const uint64_t ubase = u * kUnit;
+        const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
+        const uint8_t* src = p.in8 + ubase;
+        uint8_t* dst_a = p.out + p.L.off_a + u * (kUnit / 8 * 3);
+        uint8_t* dst_b = p.out + p.L.off_b + u * (kUnit / 2);
+        uint32_t* list = p.lists + u * kListCap;
+        const bool full = ulen == kUnit;
+        uint32_t cnt = 0;
+        uint32_t mwords[2] = {0, 0};
+#pragma unroll
+        for (int it = 0; it < 2; it++) {
+            const uint32_t slot = it * 32 + lane;
+            const uint32_t v0 = 32 * slot;  // this lane's values v0 .. v0 + 31 of the unit
+            uint32_t w[8];
+            if (full || v0 + 32 <= ulen) {
+                const uint4 x0 = ld_stream_v4(src + v0), x1 = ld_stream_v4(src + v0 + 16);
+                w[0] = x0.x, w[1] = x0.y, w[2] = x0.z, w[3] = x0.w;
+                w[4] = x1.x, w[5] = x1.y, w[6] = x1.z, w[7] = x1.w;
+            } else {  // the tensor's ragged tail
+#pragma unroll
+                for (int k = 0; k < 8; k++) w[k] = 0;
+#pragma unroll
+                for (uint32_t i = 0; i < 32; i++)
+                    if (v0 + i < ulen) w[i / 4] |= (uint32_t)src[v0 + i] << (8 * (i & 3));
+            }
+            uint32_t codes[4], fields[4], ex[8];
+            uint32_t emask = 0;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                uint32_t esc_lo, esc_hi;
+                encode_group_e5m2(w[2 * q], w[2 * q + 1], s_tab, codes[q], fields[q], esc_lo, esc_hi, ex[2 * q],
+                                  ex[2 * q + 1]);
+                emask |= escape_mask(esc_lo, esc_hi) << (8 * q);
+            }
+            const uint32_t valid = ulen > v0 ? min(ulen - v0, 32u) : 0u;
+            if (valid < 32) {  // only real values have codes, fields and escapes
+                emask &= (1u << valid) - 1;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const uint32_t vq = valid > 8u * q ? min(valid - 8u * q, 8u) : 0u;
+                    if (vq < 8) {
+                        codes[q] &= (1u << (4 * vq)) - 1;
+                        fields[q] &= (1u << (3 * vq)) - 1;
+                    }
+                }
+            }
+            const uint32_t f0 = fields[0] | (fields[1] << 24), f1 = (fields[1] >> 8) | (fields[2] << 16),
+                           f2 = (fields[2] >> 16) | (fields[3] << 8);
+            if (valid == 32) {
+                *reinterpret_cast<uint4*>(dst_b + 16 * slot) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+                uint32_t* fa = reinterpret_cast<uint32_t*>(dst_a + 12 * slot);
+                fa[0] = f0;
+                fa[1] = f1;
+                fa[2] = f2;
+            } else if (valid > 0) {  // the last groups of the tensor: nothing past their bytes
+                const uint32_t gv = (valid + 7) / 8;
+#pragma unroll
+                for (uint32_t q = 0; q < 4; q++)
+                    if (q < gv) *reinterpret_cast<uint32_t*>(dst_b + 16 * slot + 4 * q) = codes[q];
+#pragma unroll
+                for (uint32_t b = 0; b < 12; b++)
+                    if (b < 3 * gv) dst_a[12 * slot + b] = (uint8_t)((b < 4 ? f0 : b < 8 ? f1 : f2) >> (8 * (b & 3)));
+            }
+            // Escapes of this row (1024 values, lane-major): one scan ranks them.
+            if (__any_sync(0xffffffffu, emask != 0)) {
+                const uint32_t c = __popc(emask);
+                uint32_t incl = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += t;
+                }
+                uint32_t j = cnt + incl - c;
+                for (uint32_t bits = emask; bits; bits &= bits - 1, j++) {
+                    const uint32_t b = __ffs(bits) - 1;
+                    const uint32_t k = b >> 2;  // exponent word of value b, chosen in registers
+                    const uint32_t lo = (k & 2) ? ((k & 1) ? ex[3] : ex[2]) : ((k & 1) ? ex[1] : ex[0]);
+                    const uint32_t hi = (k & 2) ? ((k & 1) ? ex[7] : ex[6]) : ((k & 1) ? ex[5] : ex[4]);
+                    const uint32_t e = (((k & 4) ? hi : lo) >> (8 * (b & 3))) & 0x1F;
+                    if (j < kListCap) st_u32_keep(list + j, (v0 + b) | (e << 16), keep);
+                }
+                cnt += __shfl_sync(0xffffffffu, incl, 31);
+                mwords[it] = emask;
+            }
+        }
+        if (cnt > kListCap) {  // the list overflowed: keep the masks (word s = unit positions 32 s ..)
+            uint8_t* gmask = p.masks + u * kUnitGroups;
+#pragma unroll
+            for (int it = 0; it < 2; it++) st_u32_keep(gmask + 4 * (it * 32 + lane), mwords[it], keep);
         }
         if (lane == 0) {
             st_u32_keep(p.counts + u, cnt, keep);
@@ -550,7 +707,7 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
         *reinterpret_cast<uint32_t*>(offs + 4 * p.L.nc) = (uint32_t)m;
         zero_words(p.out, p.L.off_c + 4 * (p.L.nc + 1), p.L.off_d);
         const uint64_t groups_all = (p.n + 7) / 8;
-        zero_words(p.out, p.L.off_a + 8 * groups_all, p.L.off_b);
+        zero_bytes(p.out, p.L.off_a + p.a_bytes, p.L.off_b);
         zero_words(p.out, p.L.off_b + 4 * groups_all, p.L.off_c);
         // Escape bytes are written only below out_capacity; the stream is
         // complete exactly when its total fits.
@@ -686,7 +843,10 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
                     }
                 }
 #pragma unroll
-                for (int t = 0; t < kBatch; t++) ex[t] = t < got ? (__ldg(p.in + s + offs_b[t]) >> 7) & 0xFF : 0;
+                for (int t = 0; t < kBatch; t++)
+                    ex[t] = t >= got ? 0
+                            : p.fmt == kE5M2 ? (__ldg(p.in8 + s + offs_b[t]) >> 2) & 0x1F
+                                             : (__ldg(p.in + s + offs_b[t]) >> 7) & 0xFF;
 #pragma unroll
                 for (int t = 0; t < kBatch; t++)
                     if (t < got) put(offs_b[t], running++, div_chunk(p, offs_b[t]), ex[t]);
@@ -776,7 +936,7 @@ namespace {
 // Per-device launch facts, looked up on the first call on each device (the
 // results are the same whichever thread gets there first).
 struct DeviceFacts {
-    int sms, per_sm1;
+    int sms, per_sm1, per_sm1e;
 };
 constexpr int kMaxFactDevices = 64;
 std::atomic<int> g_facts_ready[kMaxFactDevices];
@@ -795,13 +955,14 @@ int device_facts(DeviceFacts& f) {
     }
     UZIP_CUDA_TRY(cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev));
     UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm1, encode_dense_kernel, kThreads, 0));
+    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm1e, encode_dense_e5m2_kernel, kThreads, 0));
     void (*esc[2])(Params) = {encode_escape_kernel<1>, encode_escape_kernel<2>};
     for (int k = 0; k < 2; k++) {
         const size_t smem_max = escape_smem(kMaxRangeChunks, k + 1);
         if (smem_max > 48 * 1024)
             UZIP_CUDA_TRY(cudaFuncSetAttribute(esc[k], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max));
     }
-    if (f.sms < 1 || f.per_sm1 < 1) return UZIP_ERR_CUDA;
+    if (f.sms < 1 || f.per_sm1 < 1 || f.per_sm1e < 1) return UZIP_ERR_CUDA;
     if (dev < kMaxFactDevices) {
         g_facts[dev] = f;
         g_facts_ready[dev].store(1, std::memory_order_release);
@@ -813,13 +974,13 @@ int device_facts(DeviceFacts& f) {
 
 int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_codebook, void* d_out,
                 size_t out_capacity, void* d_workspace, size_t workspace_bytes, size_t* h_out_bytes,
-                uzip_stream_t stream) {
+                uzip_stream_t stream, uint32_t fmt) {
     if (!chunk_valid(chunk)) return UZIP_ERR_CHUNK;
     if (n > UZIP_MAX_N || !d_out || !d_codebook || (n > 0 && !d_in_bf16) || !d_workspace) return UZIP_ERR_ARG;
     if (!aligned16(d_out) || !aligned16(d_codebook) || !aligned16(d_workspace) ||
         (n > 0 && !aligned16(d_in_bf16)))
         return UZIP_ERR_ALIGN;
-    const Layout L = layout_of(n, chunk);
+    const Layout L = layout_for(fmt, n, chunk);
     if (out_capacity < L.off_d) return UZIP_ERR_CAPACITY;
     const Geometry g = geometry_of(n);
     if (workspace_bytes < g.bytes) return UZIP_ERR_CAPACITY;
@@ -828,6 +989,9 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
     uint8_t* ws = static_cast<uint8_t*>(d_workspace);
     Params p;
     p.in = static_cast<const uint16_t*>(d_in_bf16);
+    p.in8 = static_cast<const uint8_t*>(d_in_bf16);
+    p.fmt = fmt;
+    p.a_bytes = fmt == kE5M2 ? 3 * ((n + 7) / 8) : n;
     p.n = n;
     p.chunk = chunk;
     p.chunk_shift = (chunk & (chunk - 1)) == 0 ? (uint32_t)__builtin_ctz(chunk) : 32u;
@@ -851,7 +1015,8 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         const int rc = device_facts(f);
         if (rc != UZIP_OK) return rc;
         // Dense kernel: one resident wave.
-        const uint64_t grid1 = std::min<uint64_t>((g.units + kWarps - 1) / kWarps, (uint64_t)f.sms * f.per_sm1);
+        const uint64_t grid1 = std::min<uint64_t>((g.units + kWarps - 1) / kWarps,
+                                                  (uint64_t)f.sms * (fmt == kE5M2 ? f.per_sm1e : f.per_sm1));
         // Escape kernel: ranges of whole chunks, sized so every resident warp
         // gets at most one (the per-range cost is mostly load latency).
         const int two_rounds = chunk > 32 * kUnit - 2040 && chunk % kUnit != 0;
@@ -869,7 +1034,10 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         const uint64_t grid2 = std::min<uint64_t>((p.ranges + kWarps - 1) / kWarps, (uint64_t)f.sms * per_sm2);
 
         UZIP_CUDA_TRY(cudaMemsetAsync(p.segs, 0, 4ull * g.nseg, s));  // segment totals
-        encode_dense_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
+        if (fmt == kE5M2)
+            encode_dense_e5m2_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
+        else
+            encode_dense_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid2);
@@ -902,6 +1070,20 @@ extern "C" UZIP_API int uzip_encode(const void* d_in_bf16, size_t n, uint32_t ch
                                     size_t* h_out_bytes, uzip_stream_t stream) {
     return encode_impl(d_in_bf16, n, chunk, d_codebook, d_out, out_capacity, d_workspace, workspace_bytes,
                        h_out_bytes, stream);
+}
+
+// ------------------------------------------------------------ FP8 E5M2
+
+extern "C" UZIP_API int uzip_e5m2_encode(const void* d_in_e5m2, size_t n, uint32_t chunk, const void* d_codebook,
+                                         void* d_out, size_t out_capacity, void* d_workspace, size_t workspace_bytes,
+                                         size_t* h_out_bytes, uzip_stream_t stream) {
+    return encode_impl(d_in_e5m2, n, chunk, d_codebook, d_out, out_capacity, d_workspace, workspace_bytes,
+                       h_out_bytes, stream, kE5M2);
+}
+
+extern "C" UZIP_API size_t uzip_e5m2_compressed_size(size_t n, size_t n_escapes, uint32_t chunk) {
+    if (!chunk_valid(chunk) || n > UZIP_MAX_N || n_escapes > n) return 0;
+    return (size_t)(layout_e5m2_of(n, chunk).off_d + 3 * (uint64_t)n_escapes);
 }
 
 // ------------------------------------------------------ per-input codebook

@@ -14,6 +14,7 @@
 namespace uzip {
 
 constexpr uint32_t kStreamMagic = 0x31505A55u;    // "UZP1" little endian
+constexpr uint32_t kStreamMagicE5 = 0x31455A55u;  // "UZE1": the FP8 E5M2 stream
 constexpr uint32_t kCodebookMagic = 0x42435A55u;  // "UZCB" little endian
 
 __host__ __device__ __forceinline__ uint64_t pad16(uint64_t v) { return (v + 15) & ~uint64_t(15); }
@@ -31,6 +32,26 @@ __host__ __device__ __forceinline__ Layout layout_of(uint64_t n, uint32_t chunk)
     L.off_c = L.off_b + pad16((n + 1) / 2);
     L.off_d = L.off_c + pad16(4 * (L.nc + 1));
     return L;
+}
+
+// Value formats: BF16 (the codec of the page's §3) and FP8 E5M2 (§4.2 /
+// appendix C: the same Top-16 framework on E5M2 bytes). An E5M2 stream keeps
+// three bits of sign and mantissa per value, eight values per 3 bytes.
+enum Format : uint32_t { kBF16 = 0, kE5M2 = 1 };
+
+__host__ __device__ __forceinline__ Layout layout_e5m2_of(uint64_t n, uint32_t chunk) {
+    Layout L;
+    L.n = n;
+    L.nc = (n + chunk - 1) / chunk;
+    L.off_a = UZIP_HEADER_BYTES;
+    L.off_b = L.off_a + pad16(3 * ((n + 7) / 8));
+    L.off_c = L.off_b + pad16((n + 1) / 2);
+    L.off_d = L.off_c + pad16(4 * (L.nc + 1));
+    return L;
+}
+
+__host__ __device__ __forceinline__ Layout layout_for(uint32_t fmt, uint64_t n, uint32_t chunk) {
+    return fmt == kE5M2 ? layout_e5m2_of(n, chunk) : layout_of(n, chunk);
 }
 
 __host__ __device__ __forceinline__ bool chunk_valid(uint32_t chunk) {
@@ -90,10 +111,11 @@ __device__ __forceinline__ void st_u8_keep(void* p, uint32_t v, uint64_t pol) {
 }
 
 // Launchers shared by the entry points (calibrate.cu, encode.cu).
-int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook, cudaStream_t stream);
+int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook, cudaStream_t stream,
+                   uint32_t fmt = kBF16);
 int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_codebook, void* d_out,
                 size_t out_capacity, void* d_workspace, size_t workspace_bytes, size_t* h_out_bytes,
-                uzip_stream_t stream);
+                uzip_stream_t stream, uint32_t fmt = kBF16);
 
 }  // namespace uzip
 

@@ -149,6 +149,25 @@ def workload(k: int, device="cpu", small: bool = False):
     raise ValueError(f"workload {k}: use sweep() for the message-size sweep (4)")
 
 
+def workload_e5m2(device="cpu", small: bool = False):
+    """(data, calibration sample) for the FP8 E5M2 codec: the KV-cache law of
+    workload 2 quantised to E5M2 (round to nearest even, as an FP8 KV cache
+    stores it), as uint8 bit patterns. The page measures FP8 KV from real
+    models; this is its synthetic stand-in."""
+    x, s = workload(2, device=device, small=small)
+    return to_e5m2_bits(x), to_e5m2_bits(s)
+
+
+def to_e5m2_bits(x: torch.Tensor) -> torch.Tensor:
+    """E5M2 bit patterns (uint8) of x, rounded to nearest even."""
+    return x.float().to(torch.float8_e5m2).view(torch.uint8)
+
+
+def as_u8(x: torch.Tensor):
+    """Host numpy uint8 copy of a one-byte tensor's bit patterns."""
+    return x.detach().contiguous().view(torch.uint8).cpu().numpy().reshape(-1)
+
+
 def sweep_sample(device="cpu", n: int = 1 << 20) -> torch.Tensor:
     return gaussian(n, seed=CALIB_SEED + 4, device=device)
 
