@@ -10,12 +10,15 @@ the method as the SplitZip review page states it in §3.2-§3.4). This module
 only compiles it with gcc and marshals numpy arrays through ctypes.
 
 The FP8 E5M2 variant (the page's §4.2 / appendix C: the same Top-16
-framework on E5M2 values) is in the same C file, after the BF16 codec.
+framework on E5M2 values) and the Top-15 + sentinel variant (§3.4, Table 6:
+the alternative the page rejects) are in the same C file, after the BF16
+codec.
 
 Parity pins: every function is pinned against IEEE-754 semantics, the page's
 closed-form sizes, hand-worked streams, exhaustive and brute-force checks --
 the BF16 codec in ``tests/test_oracle_pins.py``, the E5M2 variant in
-``tests/test_oracle_e5m2_pins.py`` (with planted-mistake batteries in the
+``tests/test_oracle_e5m2_pins.py``, the sentinel variant in
+``tests/test_oracle_sentinel_pins.py`` (with planted-mistake batteries in the
 matching ``*_mutants.py``); none is "parity unpinned".
 """
 from __future__ import annotations
@@ -75,8 +78,15 @@ def load(path: str | None = None):
     lib.orc_e5m2_encode.restype = ctypes.c_int
     lib.orc_e5m2_decode.argtypes = [p, u64, p, u64]
     lib.orc_e5m2_decode.restype = ctypes.c_int
+    lib.orc_sentinel_luts.argtypes = [p, p, p, p]
+    lib.orc_sentinel_stream_bytes.argtypes = [u64, u64, u32]
+    lib.orc_sentinel_stream_bytes.restype = u64
+    lib.orc_sentinel_encode.argtypes = [p, u64, u32, p, p, u64, ctypes.POINTER(u64)]
+    lib.orc_sentinel_encode.restype = ctypes.c_int
+    lib.orc_sentinel_decode.argtypes = [p, u64, p, u64]
+    lib.orc_sentinel_decode.restype = ctypes.c_int
     for f in ("orc_split", "orc_merge", "orc_histogram", "orc_top16", "orc_luts", "orc_calibrate",
-              "orc_e5m2_split", "orc_e5m2_merge", "orc_e5m2_histogram", "orc_e5m2_calibrate"):
+              "orc_e5m2_split", "orc_e5m2_merge", "orc_e5m2_histogram", "orc_e5m2_calibrate", "orc_sentinel_luts"):
         getattr(lib, f).restype = None
     if path is None:
         _lib = lib
@@ -217,4 +227,36 @@ class Oracle:
         s = np.ascontiguousarray(stream, np.uint8)
         x = np.zeros(max(n, 1), np.uint8)
         rc = self.lib.orc_e5m2_decode(_ptr(s), s.size, _ptr(x), n)
+        return rc, x[:n]
+
+    # ------------------------------------------- Top-15 + sentinel (page §3.4, Table 6)
+
+    def sentinel_luts(self, exps):
+        exps = np.ascontiguousarray(exps, np.uint8)
+        enc = np.zeros(256, np.uint8)
+        dec = np.zeros(16, np.uint8)
+        esc = np.zeros(256, np.uint8)
+        self.lib.orc_sentinel_luts(_ptr(exps), _ptr(enc), _ptr(dec), _ptr(esc))
+        return enc, dec, esc
+
+    def sentinel_stream_bytes(self, n, m, chunk):
+        return int(self.lib.orc_sentinel_stream_bytes(n, m, chunk))
+
+    def sentinel_encode(self, x, exps, chunk=1024, cap=None):
+        """Return (status, stream bytes); exps: the codebook's first 15 are used."""
+        x = _u16(x)
+        exps = np.ascontiguousarray(exps, np.uint8)
+        if cap is None:
+            cap = self.sentinel_stream_bytes(x.size, x.size, chunk) if 8 <= chunk <= 65536 and chunk % 8 == 0 else 64
+        out = np.zeros(max(cap, 1), np.uint8)
+        nbytes = ctypes.c_uint64(0)
+        rc = self.lib.orc_sentinel_encode(_ptr(x), x.size, chunk, _ptr(exps), _ptr(out), cap, ctypes.byref(nbytes))
+        if rc != OK:
+            return rc, None
+        return rc, out[: nbytes.value].copy()
+
+    def sentinel_decode(self, stream, n):
+        s = np.ascontiguousarray(stream, np.uint8)
+        x = np.zeros(max(n, 1), np.uint16)
+        rc = self.lib.orc_sentinel_decode(_ptr(s), s.size, _ptr(x), n)
         return rc, x[:n]

@@ -508,3 +508,134 @@ int orc_e5m2_decode(const uint8_t *in, uint64_t in_bytes, uint8_t *x, uint64_t n
     }
     return ORC_OK;
 }
+
+/* ============================================= Top-15 + sentinel variant
+ *
+ * Source page §3.4 and §4.3 Table 6: the alternative the page rejects keeps
+ * one code word as an explicit escape token -- the Top-15 exponents get codes
+ * 0..14, code 15 marks an escape -- so the decoder finds escapes in the code
+ * stream and no positions are stored (a slightly higher ratio, 1.331x on the
+ * page, and a slower decode). Readings (choices, not facts of the page):
+ *   - the Top-15 are the first 15 of the Top-16 ranking (same rules);
+ *   - an escape stores only its raw exponent byte, in ascending element order;
+ *     u32 offsets[nc + 1] (exclusive prefix of per-chunk escape counts) are
+ *     kept so every chunk decodes on its own: chunk c's values start at byte
+ *     offsets[c] of the value section;
+ *   - the stream is a 64-byte header with magic "UZS1" (codebook bytes: the 15
+ *     exponents, then 0), the sign-mantissa bytes, the codes, the offsets and
+ *     the values, the first four parts padded with zeros to 16 bytes. */
+
+void orc_sentinel_luts(const uint8_t *exps, uint8_t *enc, uint8_t *dec, uint8_t *esc)
+{
+    for (int v = 0; v < 256; v++) {
+        enc[v] = 15;
+        esc[v] = 1;
+    }
+    for (int k = 0; k < 15; k++) {
+        enc[exps[k]] = (uint8_t)k;
+        esc[exps[k]] = 0;
+        dec[k] = exps[k];
+    }
+    dec[15] = 0;
+}
+
+uint64_t orc_sentinel_stream_bytes(uint64_t n, uint64_t m, uint32_t chunk)
+{
+    if (!chunk_ok(chunk)) return 0;
+    return layout_of(n, chunk).off_d + m;
+}
+
+int orc_sentinel_encode(const uint16_t *x, uint64_t n, uint32_t chunk, const uint8_t *exps, uint8_t *out,
+                        uint64_t cap, uint64_t *out_bytes)
+{
+    if (!chunk_ok(chunk)) return ORC_ERR_CHUNK;
+    if (n >= ((uint64_t)1 << 32)) return ORC_ERR_ARG;
+    if (n > 0 && x == NULL) return ORC_ERR_ARG;
+    if (out == NULL || exps == NULL) return ORC_ERR_ARG;
+    uint8_t enc[256], dec[16], esc[256];
+    orc_sentinel_luts(exps, enc, dec, esc);
+    layout_t L = layout_of(n, chunk);
+    uint64_t m = 0;
+    for (uint64_t i = 0; i < n; i++) m += esc[exponent_of(x[i])];
+    uint64_t total = L.off_d + m;
+    if (out_bytes) *out_bytes = total;
+    if (total > cap) return ORC_ERR_CAPACITY;
+    memset(out, 0, total);
+
+    /* Dense: as for Top-16, with code 15 for every escape. */
+    uint8_t *A = out + L.off_a;
+    uint8_t *B = out + L.off_b;
+    for (uint64_t i = 0; i < n; i++) {
+        A[i] = sign_mantissa_of(x[i]);
+        uint8_t code = enc[exponent_of(x[i])];
+        B[i / 2] = (uint8_t)(B[i / 2] | (code << (4 * (i % 2))));
+    }
+    /* Escape values only, chunk by chunk, behind per-chunk offsets. */
+    uint8_t *C = out + L.off_c;
+    uint8_t *D = out + L.off_d;
+    uint64_t running = 0;
+    for (uint64_t c = 0; c < L.nc; c++) {
+        uint64_t start = c * chunk;
+        uint64_t end = start + chunk < n ? start + chunk : n;
+        put_u32(C + 4 * c, (uint32_t)running);
+        for (uint64_t i = start; i < end; i++) {
+            uint8_t e = exponent_of(x[i]);
+            if (esc[e]) D[running++] = e;
+        }
+    }
+    put_u32(C + 4 * L.nc, (uint32_t)running);
+
+    memcpy(out, "UZS1", 4);
+    out[4] = 1;
+    out[5] = 0;
+    put_u64(out + 8, n);
+    put_u32(out + 16, chunk);
+    put_u32(out + 20, (uint32_t)L.nc);
+    put_u64(out + 24, m);
+    memcpy(out + 32, exps, 15);
+    out[47] = 0;
+    put_u64(out + 48, total);
+    return ORC_OK;
+}
+
+int orc_sentinel_decode(const uint8_t *in, uint64_t in_bytes, uint16_t *x, uint64_t n)
+{
+    if (in == NULL || (n > 0 && x == NULL)) return ORC_ERR_ARG;
+    if (in_bytes < 64) return ORC_ERR_CORRUPT;
+    if (memcmp(in, "UZS1", 4) != 0 || get_u16(in + 4) != 1 || get_u16(in + 6) != 0) return ORC_ERR_CORRUPT;
+    uint64_t hn = get_u64(in + 8);
+    uint32_t chunk = get_u32(in + 16);
+    uint64_t nc = get_u32(in + 20);
+    uint64_t m = get_u64(in + 24);
+    uint64_t total = get_u64(in + 48);
+    if (hn != n || !chunk_ok(chunk) || n >= ((uint64_t)1 << 32)) return ORC_ERR_CORRUPT;
+    layout_t L = layout_of(n, chunk);
+    if (nc != L.nc || m > n || total != L.off_d + m || total > in_bytes) return ORC_ERR_CORRUPT;
+    const uint8_t *dec = in + 32;
+    const uint8_t *A = in + L.off_a;
+    const uint8_t *B = in + L.off_b;
+    const uint8_t *C = in + L.off_c;
+    const uint8_t *D = in + L.off_d;
+    if (get_u32(C) != 0 || get_u32(C + 4 * nc) != m) return ORC_ERR_CORRUPT;
+    /* Each chunk on its own: a code 15 takes the chunk's next value. */
+    for (uint64_t c = 0; c < nc; c++) {
+        uint64_t o = get_u32(C + 4 * c), o1 = get_u32(C + 4 * (c + 1));
+        if (o > o1) return ORC_ERR_CORRUPT;
+        uint64_t start = c * chunk;
+        uint64_t end = start + chunk < n ? start + chunk : n;
+        uint64_t next = o;
+        for (uint64_t i = start; i < end; i++) {
+            uint8_t code = (uint8_t)((B[i / 2] >> (4 * (i % 2))) & 0x0F);
+            uint8_t e;
+            if (code == 15) {
+                if (next >= o1) return ORC_ERR_CORRUPT;
+                e = D[next++];
+            } else {
+                e = dec[code];
+            }
+            x[i] = rebuild(A[i], e);
+        }
+        if (next != o1) return ORC_ERR_CORRUPT;
+    }
+    return ORC_OK;
+}

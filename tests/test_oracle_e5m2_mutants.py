@@ -15,6 +15,7 @@ import oracle
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 E5M2_MARKER = "/* ====================================================== FP8 E5M2 variant"
+SENTINEL_MARKER = "/* ============================================= Top-15 + sentinel variant"
 
 MUTANTS = {
     "exponent shift": ("return (uint8_t)((x >> 2) & 0x1F);", "return (uint8_t)((x >> 3) & 0x1F);"),
@@ -75,9 +76,10 @@ def test_mutant_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(os.path.join(os.path.dirname(HERE), "oracle", "uzip_oracle.c")).read()
     head, tail = src.split(E5M2_MARKER, 1)
-    assert tail.count(old) == 1, f"mutation site for {name!r} not unique"
+    part, rest = tail.split(SENTINEL_MARKER, 1)  # the E5M2 part only
+    assert part.count(old) == 1, f"mutation site for {name!r} not unique"
     mut_src = tmp_path / "mutant.c"
-    mut_src.write_text(head + E5M2_MARKER + tail.replace(old, new))
+    mut_src.write_text(head + E5M2_MARKER + part.replace(old, new) + SENTINEL_MARKER + rest)
     lib = oracle.build(force=True, src=str(mut_src), out=str(tmp_path / "libmutant.so"))
     r = _run_battery(lib)
     assert r.returncode != 0, f"mutant {name!r} survived the pins:\n{r.stdout}{r.stderr}"
