@@ -743,13 +743,94 @@ def run_e5m2(args):
     }
 
 
+def run_sentinel(args):
+    """Top-15 + sentinel against Top-16 with explicit positions (SplitZip
+    review page, §3.4 and Table 6): the same KV tensor and calibration sample,
+    the sentinel codebook made from the Top-16 one's first 15 exponents, each
+    codec's encode and decode timed back to back; ratio of each stream."""
+    import statistics as stats
+
+    import torch
+
+    import lossless_bf16_exponent_gb300 as uz
+    import lossless_bf16_exponent_gb300.workloads as W
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist("nccl")
+    uz.load()
+    x, sample = W.workload(2, device=dev)
+    n = x.numel()
+    raw = 2 * n
+    cb16 = uz.calibrate(sample)
+    cb15 = uz.make_sentinel(cb16.clone())
+    out = torch.empty(uz.max_compressed_size(n, CHUNK), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(uz.workspace_bytes(n, CHUNK), dtype=torch.uint8, device=dev)
+    y = torch.empty_like(x)
+    st = torch.cuda.current_stream(dev)
+    codecs = {
+        "top16": (lambda: uz.encode(x, cb16, CHUNK, out=out, workspace=wsb, sync=False),
+                  lambda nb: uz.decode(out, n, out=y, stream_bytes=nb)),
+        "top15_sentinel": (lambda: uz.sentinel_encode(x, cb15, CHUNK, out=out, workspace=wsb, sync=False),
+                           lambda nb: uz.sentinel_decode(out, n, out=y, stream_bytes=nb)),
+    }
+    reps = max(10, min(args.steps, 200))
+    res = {}
+    for name, (enc, dec) in codecs.items():
+        enc()
+        info = uz.stream_info(out)
+        nbytes = int(info["total_bytes"])
+        dec(nbytes)
+        torch.cuda.synchronize()
+        assert info["status"] == 0 and torch.equal(y.view(torch.int16), x.view(torch.int16)), name
+        for _ in range(args.warmup):
+            enc()
+            dec(nbytes)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+        barrier()
+        torch.cuda.synchronize()
+        for ev in evs:
+            ev[0].record(st)
+            enc()
+            ev[1].record(st)
+            dec(nbytes)
+            ev[2].record(st)
+        torch.cuda.synchronize()
+        te = stats.mean(e[0].elapsed_time(e[1]) for e in evs)
+        td = stats.mean(e[1].elapsed_time(e[2]) for e in evs)
+        m = int(info["escapes"])
+        res[name] = {"stream_bytes": nbytes, "ratio": round(raw / nbytes, 5),
+                     "payload_ratio": round(raw / int(info["payload_bytes"]), 5), "escapes": m,
+                     "encode_us": round(te * 1e3, 2), "decode_us": round(td * 1e3, 2),
+                     "encode_gbs_raw": round(raw / (te * 1e-3) / 1e9, 1),
+                     "decode_gbs_raw": round(raw / (td * 1e-3) / 1e9, 1),
+                     "decode_frac_of_peak": None, "_alg": raw + nbytes, "_td": td}
+    if rank != 0:
+        return None
+    peak, peak_src = measured_peak()
+    for r in res.values():
+        r["decode_frac_of_peak"] = round(r.pop("_alg") / (r.pop("_td") * 1e-3) / 1e9 / peak, 4)
+    s15 = res["top15_sentinel"]
+    return {
+        "mode": "sentinel", "metric": "Top-15+sentinel vs Top-16 decode GB/s (raw BF16 bytes) and ratio @256M elems",
+        "value": s15["decode_gbs_raw"], "unit": "GB/s", "n_gpus": ws, "steps": reps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "value": "Top-15 + sentinel decode GB/s", "peak_gbs": peak,
+                   "peak_source": peak_src},
+        "codecs": res,
+        "decode_speed_top16_over_sentinel": round(res["top15_sentinel"]["decode_us"] / res["top16"]["decode_us"], 3),
+        "page_table6": {"sentinel_ratio": 1.331, "sentinel_decode_gbs": 620.8, "top16_decode_speedup": 3.5},
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["codec", "dynamic", "pipeline", "chunks", "e5m2"], default="codec",
+    ap.add_argument("--mode", choices=["codec", "dynamic", "pipeline", "chunks", "e5m2", "sentinel"], default="codec",
                     help="codec = the benchmark step; dynamic = per-input codebook encode; "
                          "pipeline = streamed compressed transfer (next rows)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -769,6 +850,8 @@ def main(argv=None):
         line = run_chunks(args)
     elif args.mode == "e5m2":
         line = run_e5m2(args)
+    elif args.mode == "sentinel":
+        line = run_sentinel(args)
     else:
         line = run_ours(args)
     if line is not None:

@@ -215,7 +215,8 @@ UZIP_API int uzip_decode(const void *d_stream, size_t stream_bytes, void *d_out_
 /* Copy one encoded stream, exactly its header's total bytes, without the
  * host learning its length first (a sender in the encode -> transfer ->
  * decode pipeline of appendix B). The kernel reads the header at src_stream;
- * if it is a stream header of this version and its total is at most
+ * if it is a stream header of this version (any format: BF16, E5M2 or
+ * Top-15 + sentinel) and its total is at most
  * capacity, bytes [0, total) are copied to dst, else nothing is.
  *   src_stream     16-byte aligned, at least capacity readable bytes; device
  *                  memory or pinned (mapped) host memory.
@@ -262,20 +263,60 @@ UZIP_API int uzip_e5m2_encode(const void *d_in_e5m2, size_t n, uint32_t chunk, c
 UZIP_API int uzip_e5m2_decode(const void *d_stream, size_t stream_bytes, void *d_out_e5m2, size_t n,
                               uint32_t *d_status, uzip_stream_t stream);
 
+/* ----------------------------------------------------- Top-15 + sentinel
+ * The alternative the page measures and rejects (§3.4, Table 6): the 15 most
+ * frequent exponents get codes 0..14, code 15 marks an escape and only the
+ * escape's raw exponent is stored (no position), so the decoder finds escapes
+ * by scanning the code stream. Stream: magic "UZS1", the BF16 layout, the
+ * codebook bytes = the 15 exponents then 0, u32 per-chunk offsets, then one
+ * byte per escape in ascending element order (chunk c's values at byte
+ * offsets[c] of that section). Size 64 + A16(n) + A16(ceil(n/2)) +
+ * A16(4(nc+1)) + M. */
+
+/* Turn a codebook (uzip_calibrate / uzip_codebook_from_exps) into the
+ * Top-15 + sentinel codebook of its first 15 exponents, in place. Async. */
+UZIP_API int uzip_codebook_make_sentinel(void *d_codebook, uzip_stream_t stream);
+
+/* Exact sentinel stream bytes for n values with n_escapes escapes. Host only. */
+UZIP_API size_t uzip_sentinel_compressed_size(size_t n, size_t n_escapes, uint32_t chunk);
+
+/* Encode BF16 values with a sentinel codebook; arguments, output and errors
+ * as uzip_encode's. */
+UZIP_API int uzip_sentinel_encode(const void *d_in_bf16, size_t n, uint32_t chunk, const void *d_codebook,
+                                  void *d_out, size_t out_capacity, void *d_workspace, size_t workspace_bytes,
+                                  size_t *h_out_bytes, uzip_stream_t stream);
+
+/* Decode a sentinel stream; arguments, checks and errors as uzip_decode's.
+ * An escape past its chunk's values, or a chunk inside a decode tile whose
+ * code-15 count differs from its offsets, gives UZIP_ERR_CORRUPT. */
+UZIP_API int uzip_sentinel_decode(const void *d_stream, size_t stream_bytes, void *d_out_bf16, size_t n,
+                                  uint32_t *d_status, uzip_stream_t stream);
+
 /* Host view of a stream header. */
 typedef struct {
     uint64_t n;
     uint64_t escapes;     /* M */
     uint64_t total_bytes; /* whole stream */
-    uint64_t payload_bytes; /* n + ceil(n/2) + 3M: the page's size */
+    uint64_t payload_bytes; /* the page's size: n + ceil(n/2) + 3M for BF16,
+                               3 ceil(n/8) + ceil(n/2) + 3M for E5M2,
+                               n + ceil(n/2) + M for Top-15 + sentinel */
     uint32_t chunk;
     uint32_t nc;
     uint32_t version;
     uint32_t flags;       /* UZIP_FLAG_* */
     uint8_t exps[16];
+    uint32_t format;      /* UZIP_FORMAT_* from the magic */
+    uint32_t reserved;
 } uzip_info_t;
 
-/* Copy the header to the host (synchronises `stream`) and check it. Returns
+enum uzip_format {
+    UZIP_FORMAT_BF16 = 0,     /* "UZP1" */
+    UZIP_FORMAT_E5M2 = 1,     /* "UZE1" */
+    UZIP_FORMAT_SENTINEL = 2  /* "UZS1" */
+};
+
+/* Copy the header of a stream of any format to the host (synchronises
+ * `stream`) and check it. Returns
  * UZIP_ERR_CORRUPT for a bad magic, version or inconsistent sizes, else
  * UZIP_OK (h_info is filled in both cases when the header was readable). */
 UZIP_API int uzip_stream_info(const void *d_stream, size_t stream_bytes, uzip_info_t *h_info,

@@ -15,13 +15,15 @@ HEADER_BYTES = 64
 CODEBOOK_BYTES = 4096
 CB_EXPS, CB_DEC, CB_ENC, CB_ESC, CB_HIST = 16, 32, 48, 304, 1024
 FLAG_CAPACITY = 0x1
+FORMAT_BF16, FORMAT_E5M2, FORMAT_SENTINEL = range(3)
 MAX_N = 0xFFFFFFFF
 
 EXPORTS = (
     "uzip_calibrate", "uzip_codebook_from_exps", "uzip_compressed_size", "uzip_encode_workspace_bytes",
     "uzip_encode", "uzip_encode_noalloc", "uzip_encode_dynamic", "uzip_decode", "uzip_stream_copy",
     "uzip_stream_info", "uzip_status_string", "uzip_e5m2_calibrate", "uzip_e5m2_compressed_size",
-    "uzip_e5m2_encode", "uzip_e5m2_decode",
+    "uzip_e5m2_encode", "uzip_e5m2_decode", "uzip_codebook_make_sentinel", "uzip_sentinel_compressed_size",
+    "uzip_sentinel_encode", "uzip_sentinel_decode",
     "uzip_version",
 )
 NOALLOC_MAX_N = 1 << 25
@@ -32,6 +34,7 @@ class Info(ctypes.Structure):
         ("n", ctypes.c_uint64), ("escapes", ctypes.c_uint64), ("total_bytes", ctypes.c_uint64),
         ("payload_bytes", ctypes.c_uint64), ("chunk", ctypes.c_uint32), ("nc", ctypes.c_uint32),
         ("version", ctypes.c_uint32), ("flags", ctypes.c_uint32), ("exps", ctypes.c_uint8 * 16),
+        ("format", ctypes.c_uint32), ("reserved", ctypes.c_uint32),
     ]
 
 
@@ -74,6 +77,11 @@ def load(path: str | None = None):
     L.uzip_e5m2_compressed_size.restype = sz
     L.uzip_e5m2_encode.argtypes = [vp, sz, u32, vp, vp, sz, vp, sz, ctypes.POINTER(sz), vp]
     L.uzip_e5m2_decode.argtypes = [vp, sz, vp, sz, vp, vp]
+    L.uzip_codebook_make_sentinel.argtypes = [vp, vp]
+    L.uzip_sentinel_compressed_size.argtypes = [sz, sz, u32]
+    L.uzip_sentinel_compressed_size.restype = sz
+    L.uzip_sentinel_encode.argtypes = [vp, sz, u32, vp, vp, sz, vp, sz, ctypes.POINTER(sz), vp]
+    L.uzip_sentinel_decode.argtypes = [vp, sz, vp, sz, vp, vp]
     L.uzip_decode.argtypes = [vp, sz, vp, sz, vp, vp]
     L.uzip_stream_info.argtypes = [vp, sz, ctypes.POINTER(Info), vp]
     L.uzip_status_string.argtypes = [i]
@@ -81,7 +89,8 @@ def load(path: str | None = None):
     L.uzip_version.argtypes = []
     for f in ("uzip_calibrate", "uzip_codebook_from_exps", "uzip_encode", "uzip_encode_noalloc",
               "uzip_encode_dynamic", "uzip_decode", "uzip_stream_copy", "uzip_stream_info", "uzip_version",
-              "uzip_e5m2_calibrate", "uzip_e5m2_encode", "uzip_e5m2_decode"):
+              "uzip_e5m2_calibrate", "uzip_e5m2_encode", "uzip_e5m2_decode", "uzip_codebook_make_sentinel",
+              "uzip_sentinel_encode", "uzip_sentinel_decode"):
         getattr(L, f).restype = i
     if path is None:
         _lib = L

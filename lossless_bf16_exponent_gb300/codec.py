@@ -221,3 +221,44 @@ def e5m2_decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = None, s
     check(load().uzip_e5m2_decode(_p(stream), nb, _p(o) if n else None, n, _p(status), _sp(stream.device)),
           "uzip_e5m2_decode")
     return out
+
+
+# ------------------------------------------------------ Top-15 + sentinel
+
+def make_sentinel(codebook: torch.Tensor) -> torch.Tensor:
+    """Turn a codebook into the Top-15 + sentinel codebook of its first 15
+    exponents, in place (SplitZip §3.4, Table 6)."""
+    check(load().uzip_codebook_make_sentinel(_p(codebook), _sp(codebook.device)), "uzip_codebook_make_sentinel")
+    return codebook
+
+
+def sentinel_compressed_size(n: int, n_escapes: int, chunk: int = 1024) -> int:
+    return int(load().uzip_sentinel_compressed_size(n, n_escapes, chunk))
+
+
+def sentinel_encode(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, out: torch.Tensor | None = None,
+                    workspace: torch.Tensor | None = None, sync: bool = True):
+    """Encode BF16 values in the Top-15 + sentinel format; ``(stream, nbytes)``."""
+    v = _flat16(x)
+    n = v.numel()
+    if out is None:
+        out = torch.empty(sentinel_compressed_size(n, n, chunk), dtype=torch.uint8, device=v.device)
+    if workspace is None:
+        workspace = torch.empty(max(16, workspace_bytes(n, chunk)), dtype=torch.uint8, device=v.device)
+    nbytes = ctypes.c_size_t(0)
+    args = (_p(v), n, chunk, _p(codebook), _p(out), out.numel(), _p(workspace), workspace.numel(),
+            ctypes.byref(nbytes) if sync else None)
+    check(load().uzip_sentinel_encode(*args, _sp(v.device)), "uzip_sentinel_encode")
+    return out, (nbytes.value if sync else None)
+
+
+def sentinel_decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = None,
+                    status: torch.Tensor | None = None, stream_bytes: int | None = None) -> torch.Tensor:
+    """Decode a Top-15 + sentinel stream into ``n`` BF16 values."""
+    if out is None:
+        out = torch.empty(max(n, 1), dtype=torch.bfloat16, device=stream.device)[:n]
+    o = _flat16(out) if n else out
+    nb = stream.numel() if stream_bytes is None else stream_bytes
+    check(load().uzip_sentinel_decode(_p(stream), nb, _p(o) if n else None, n, _p(status), _sp(stream.device)),
+          "uzip_sentinel_decode")
+    return out

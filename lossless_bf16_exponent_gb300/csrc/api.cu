@@ -31,12 +31,20 @@ extern "C" UZIP_API int uzip_stream_info(const void* d_stream, size_t stream_byt
     h_info->escapes = rd(24, 8);
     for (int k = 0; k < 16; k++) h_info->exps[k] = h[32 + k];
     h_info->total_bytes = rd(48, 8);
-    h_info->payload_bytes = h_info->n + (h_info->n + 1) / 2 + 3 * h_info->escapes;
-    if ((uint32_t)rd(0, 4) != kStreamMagic || h_info->version != UZIP_VERSION) return UZIP_ERR_CORRUPT;
+    const uint32_t magic = (uint32_t)rd(0, 4);
+    const uint32_t fmt = magic == kStreamMagicE5 ? kE5M2 : magic == kStreamMagicS ? kSentinel : kBF16;
+    h_info->format = fmt;
+    // The page's size: dense bytes, packed codes, escape bytes.
+    const uint64_t dense = fmt == kE5M2 ? 3 * ((h_info->n + 7) / 8) : h_info->n;
+    const uint64_t per_escape = fmt == kSentinel ? 1 : 3;
+    h_info->payload_bytes = dense + (h_info->n + 1) / 2 + per_escape * h_info->escapes;
+    if ((magic != kStreamMagic && magic != kStreamMagicE5 && magic != kStreamMagicS) ||
+        h_info->version != UZIP_VERSION)
+        return UZIP_ERR_CORRUPT;
     if (!chunk_valid(h_info->chunk) || h_info->n > UZIP_MAX_N || h_info->escapes > h_info->n)
         return UZIP_ERR_CORRUPT;
-    const Layout L = layout_of(h_info->n, h_info->chunk);
-    if (h_info->nc != L.nc || h_info->total_bytes != L.off_d + 3 * h_info->escapes ||
+    const Layout L = layout_for(fmt, h_info->n, h_info->chunk);
+    if (h_info->nc != L.nc || h_info->total_bytes != L.off_d + per_escape * h_info->escapes ||
         h_info->total_bytes > stream_bytes)
         return UZIP_ERR_CORRUPT;
     return UZIP_OK;

@@ -214,6 +214,41 @@ extern "C" UZIP_API int uzip_e5m2_calibrate(const void* d_sample_e5m2, size_t n_
     return calibrate_impl(d_sample_e5m2, n_sample, d_codebook, reinterpret_cast<cudaStream_t>(stream), kE5M2);
 }
 
+namespace uzip {
+namespace {
+
+// Top-15 + sentinel tables from a codebook's exponents (page §3.4, Table 6):
+// codes 0..14 for exps[0..14], code 15 for every other exponent (an escape),
+// decode-table entry 15 = 0, blob version 2.
+__global__ void __launch_bounds__(256) sentinel_tables_kernel(uint8_t* __restrict__ cb) {
+    __shared__ uint8_t exps[16];
+    const int t = threadIdx.x;
+    if (t < 16) exps[t] = cb[UZIP_CB_EXPS + t];
+    __syncthreads();
+    uint8_t code = 15, esc = 1;
+#pragma unroll
+    for (int k = 0; k < 15; k++)
+        if (exps[k] == t) {
+            code = (uint8_t)k;
+            esc = 0;
+        }
+    cb[UZIP_CB_ENC + t] = code;
+    cb[UZIP_CB_ESC + t] = esc;
+    if (t < 16) cb[UZIP_CB_DEC + t] = t < 15 ? exps[t] : 0;
+    if (t == 0) reinterpret_cast<uint32_t*>(cb)[1] = 2;
+}
+
+}  // namespace
+}  // namespace uzip
+
+extern "C" UZIP_API int uzip_codebook_make_sentinel(void* d_codebook, uzip_stream_t stream) {
+    if (!d_codebook) return UZIP_ERR_ARG;
+    if (!aligned16(d_codebook)) return UZIP_ERR_ALIGN;
+    sentinel_tables_kernel<<<1, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(static_cast<uint8_t*>(d_codebook));
+    UZIP_CUDA_TRY(cudaGetLastError());
+    return UZIP_OK;
+}
+
 extern "C" UZIP_API int uzip_codebook_from_exps(const uint8_t* h_exps16, void* d_codebook,
                                                 uzip_stream_t stream) {
     if (!h_exps16 || !d_codebook) return UZIP_ERR_ARG;

@@ -24,7 +24,8 @@ __global__ void __launch_bounds__(kCopyThreads) stream_copy_kernel(const uint8_t
     const uint4* h = reinterpret_cast<const uint4*>(src);
     const uint4 h0 = h[0], h3 = h[3];
     uint64_t total = 0;
-    if (h0.x == kStreamMagic && (h0.y & 0xFFFF) == UZIP_VERSION) total = (uint64_t)h3.x | ((uint64_t)h3.y << 32);
+    const bool magic = h0.x == kStreamMagic || h0.x == kStreamMagicE5 || h0.x == kStreamMagicS;
+    if (magic && (h0.y & 0xFFFF) == UZIP_VERSION) total = (uint64_t)h3.x | ((uint64_t)h3.y << 32);
     if (total < UZIP_HEADER_BYTES || total > capacity) total = 0;  // not a whole stream: copy nothing
     if (copied && blockIdx.x == 0 && threadIdx.x == 0) *copied = total;
     const uint4* s4 = reinterpret_cast<const uint4*>(src);

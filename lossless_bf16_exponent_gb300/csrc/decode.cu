@@ -343,6 +343,171 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
     if (s_bad && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
 }
 
+// ------------------------------------------------------ Top-15 + sentinel
+
+// Sentinel (code 15) flags of eight codes: bit 4i set when nibble i is 15.
+__device__ __forceinline__ uint32_t sentinel_bits(uint32_t w) { return w & (w >> 1) & (w >> 2) & (w >> 3) & 0x11111111u; }
+
+// Decoder for the Top-15 + sentinel format (page §3.4, Table 6): no escape
+// positions are stored, so every tile first counts code 15s -- per thread,
+// then a block scan -- to give each escape its rank inside its chunk and
+// hence its value's index behind the chunk's offset; the dense lookup, the
+// patch and the store follow. Each thread takes 32 consecutive values.
+__global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_sentinel_kernel(const Params p) {
+    static_assert(kTile == kThreads * 32, "one 32-value slot per thread");
+    __shared__ uint32_t s_codes[kTile / 8];       // the tile's code words, one per group of 8 values
+    __shared__ uint32_t s_pre[kThreads + 1];      // code 15s before each thread's slot
+    __shared__ uint32_t s_warp[kThreads / 32];
+    __shared__ uint32_t s_cbase[kTile / 8 + 1];   // per chunk of the tile: tile count at its start - its earlier count
+    __shared__ int s_bad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint4* h = reinterpret_cast<const uint4*>(p.s);
+    const uint4 h0 = h[0], h1 = h[1], h2 = h[2], h3 = h[3];
+    const uint64_t hn = (uint64_t)h0.z | ((uint64_t)h0.w << 32);
+    const uint32_t chunk = h1.x;
+    const uint64_t nc = h1.y;
+    const uint64_t m = (uint64_t)h1.z | ((uint64_t)h1.w << 32);
+    const uint64_t total = (uint64_t)h3.x | ((uint64_t)h3.y << 32);
+    bool ok = h0.x == kStreamMagicS && (h0.y & 0xFFFF) == 1 && (h0.y >> 16) == 0 && hn == p.n &&
+              chunk_valid(chunk) && m <= hn;
+    Layout L;
+    if (ok) {
+        L = layout_of(hn, chunk);
+        ok = nc == L.nc && total == L.off_d + m && total <= p.stream_bytes;
+    }
+    if (!ok) {
+        if (blockIdx.x == 0 && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
+        return;
+    }
+    const uint32_t n32 = (uint32_t)p.n;
+    const uint8_t* A = p.s + L.off_a;
+    const uint8_t* B = p.s + L.off_b;
+    const uint32_t* Cw = reinterpret_cast<const uint32_t*>(p.s + L.off_c);
+    const uint8_t* D = p.s + L.off_d;
+    const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;
+    const uint32_t tiles = (n32 + kTile - 1) / kTile;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+
+    // code 15s of the tile before value f (0 <= f <= tlen)
+    auto before = [&](uint32_t f) {
+        const uint32_t t = f / 32, r = f % 32;
+        uint32_t c = s_pre[t];
+        for (uint32_t q = 0; q < r / 8; q++) c += __popc(sentinel_bits(s_codes[4 * t + q]));
+        if (r % 8) c += __popc(sentinel_bits(s_codes[4 * t + r / 8]) & ((1u << (4 * (r % 8))) - 1));
+        return c;
+    };
+
+    for (uint32_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        const uint32_t e0 = t * kTile;
+        const uint32_t tlen = min(kTile, n32 - e0);
+        const uint32_t v0 = 32 * tid;
+        const bool mine = v0 < tlen;
+        uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, cv = a0;
+        if (mine) {  // padded sections: a whole slot stays inside the stream, zeros past n
+            a0 = __ldg(reinterpret_cast<const uint4*>(A + e0 + v0));
+            a1 = __ldg(reinterpret_cast<const uint4*>(A + e0 + v0 + 16));
+            cv = __ldg(reinterpret_cast<const uint4*>(B + e0 / 2 + 16 * tid));
+        }
+        const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+        uint32_t cnt = 0;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            s_codes[4 * tid + q] = cw[q];
+            cnt += __popc(sentinel_bits(cw[q]));
+        }
+        // block-wide exclusive scan of the per-thread counts
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        uint32_t off = 0;
+        for (int w = 0; w < warp; w++) off += s_warp[w];
+        s_pre[tid] = off + incl - cnt;
+        if (tid == kThreads - 1) s_pre[kThreads] = off + incl;
+        __syncthreads();
+        // code 15s that the tile's first chunk holds in earlier tiles (at most chunk / 8 code words), summed
+        // by the whole block; s_warp is free again since the barrier above
+        const uint32_t c_first = e0 / chunk, c_last = (e0 + tlen - 1) / chunk;
+        uint32_t early = 0;
+        if (c_first * chunk < e0) {
+            const uint32_t* B32 = reinterpret_cast<const uint32_t*>(B);
+            for (uint32_t g = c_first * chunk / 8 + tid; g < e0 / 8; g += kThreads)
+                early += __popc(sentinel_bits(__ldg(B32 + g)));
+            early = __reduce_add_sync(0xffffffffu, early);
+            if (lane == 0) s_warp[warp] = early;
+            __syncthreads();
+            early = 0;
+#pragma unroll
+            for (int w = 0; w < kThreads / 32; w++) early += s_warp[w];
+        }
+        // every chunk overlapping the tile: its rank base, and its count checked when it lies inside the tile
+        for (uint32_t cc = tid; cc <= c_last - c_first; cc += kThreads) {
+            const uint32_t c = c_first + cc, cs = c * chunk;
+            uint32_t base;
+            if (cs >= e0) {
+                base = before(cs - e0);
+                const uint32_t ce = min(cs + chunk, n32);
+                if (ce <= e0 + tlen && before(ce - e0) - base != Cw[c + 1] - Cw[c]) s_bad = 1;
+            } else {  // the chunk began in an earlier tile
+                base = 0u - early;
+            }
+            s_cbase[cc] = base;
+        }
+        __syncthreads();
+        if (mine) {
+            const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t valid = min(32u, tlen - v0);  // values of the slot below n
+            uint32_t o[16];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                uint32_t e_lo = lookup4(cw[q] & 0xFFFF, d0, d1, d2, d3);
+                uint32_t e_hi = lookup4(cw[q] >> 16, d0, d1, d2, d3);
+                uint32_t sb = sentinel_bits(cw[q]);
+                // a code 15 in the padding past n (only in a corrupt stream) is not an escape
+                if (valid < 8 * q + 8) sb &= valid > 8u * q ? (1u << (4 * (valid - 8 * q))) - 1 : 0u;
+                while (sb) {  // escapes: their values, in order, behind their chunk's offset
+                    const uint32_t i = (__ffs(sb) - 1) / 4;  // value i of the group
+                    sb &= sb - 1;
+                    const uint32_t el = e0 + v0 + 8 * q + i;
+                    const uint32_t c = el / chunk;
+                    const uint32_t rank = before(v0 + 8 * q + i) - s_cbase[c - c_first];
+                    const uint32_t idx = Cw[c] + rank;
+                    uint32_t ev = 0;
+                    if (idx < Cw[c + 1] && idx < m) ev = D[idx];
+                    else s_bad = 1;
+                    const uint32_t sh = 8 * (i & 3);
+                    if (i < 4) e_lo = (e_lo & ~(0xFFu << sh)) | (ev << sh);
+                    else e_hi = (e_hi & ~(0xFFu << sh)) | (ev << sh);
+                }
+                const uint2 lo = rebuild4(e_lo, aw[2 * q]);
+                const uint2 hi = rebuild4(e_hi, aw[2 * q + 1]);
+                o[4 * q] = lo.x;
+                o[4 * q + 1] = lo.y;
+                o[4 * q + 2] = hi.x;
+                o[4 * q + 3] = hi.y;
+            }
+            const uint32_t ge = e0 + v0;
+            if (ge + 32 <= n32) {
+                uint4* dst = reinterpret_cast<uint4*>(p.out + ge);
+#pragma unroll
+                for (int k = 0; k < 4; k++) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+            } else {
+#pragma unroll
+                for (uint32_t i = 0; i < 32; i++)
+                    if (ge + i < n32) p.out[ge + i] = (uint16_t)(o[i / 2] >> (16 * (i & 1)));
+            }
+        }
+        __syncthreads();  // the shared tables are rewritten by the next tile
+    }
+    if (s_bad && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
+}
+
 }  // namespace
 }  // namespace uzip
 
@@ -382,6 +547,11 @@ int decode_launch(void (*kernel)(Params), const void* d_stream, size_t stream_by
 extern "C" UZIP_API int uzip_decode(const void* d_stream, size_t stream_bytes, void* d_out_bf16, size_t n,
                                     uint32_t* d_status, uzip_stream_t stream) {
     return decode_launch(decode_kernel, d_stream, stream_bytes, d_out_bf16, n, d_status, stream);
+}
+
+extern "C" UZIP_API int uzip_sentinel_decode(const void* d_stream, size_t stream_bytes, void* d_out_bf16, size_t n,
+                                             uint32_t* d_status, uzip_stream_t stream) {
+    return decode_launch(decode_sentinel_kernel, d_stream, stream_bytes, d_out_bf16, n, d_status, stream);
 }
 
 extern "C" UZIP_API int uzip_e5m2_decode(const void* d_stream, size_t stream_bytes, void* d_out_e5m2, size_t n,

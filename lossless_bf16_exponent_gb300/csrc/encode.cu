@@ -167,12 +167,19 @@ __device__ __forceinline__ uint32_t escape_mask(uint32_t esc_lo, uint32_t esc_hi
     return m_lo | (m_hi << 4);
 }
 
+// Stream bytes for m escapes: 3 per escape (position + value), 1 for the
+// sentinel format (value only).
+__device__ __forceinline__ uint64_t stream_total(const Params& p, uint64_t m) {
+    return p.L.off_d + (p.fmt == kSentinel ? m : 3 * m);
+}
+
 __device__ void write_header(const Params& p, uint64_t m, uint32_t flags) {
     uint4* h = reinterpret_cast<uint4*>(p.out);
-    const uint64_t total = p.L.off_d + 3 * m;
-    const uint4 exps = *reinterpret_cast<const uint4*>(p.cb + UZIP_CB_EXPS);
-    h[0] = make_uint4(p.fmt == kE5M2 ? kStreamMagicE5 : kStreamMagic, 1u | (flags << 16), (uint32_t)p.n,
-                      (uint32_t)(p.n >> 32));
+    const uint64_t total = stream_total(p, m);
+    uint4 exps = *reinterpret_cast<const uint4*>(p.cb + UZIP_CB_EXPS);
+    if (p.fmt == kSentinel) exps.w &= 0x00FFFFFFu;  // only 15 exponents have codes
+    const uint32_t magic = p.fmt == kE5M2 ? kStreamMagicE5 : p.fmt == kSentinel ? kStreamMagicS : kStreamMagic;
+    h[0] = make_uint4(magic, 1u | (flags << 16), (uint32_t)p.n, (uint32_t)(p.n >> 32));
     h[1] = make_uint4(p.chunk, (uint32_t)p.L.nc, (uint32_t)m, (uint32_t)(m >> 32));
     h[2] = exps;
     h[3] = make_uint4((uint32_t)total, (uint32_t)(total >> 32), 0u, 0u);
@@ -711,7 +718,7 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
         zero_words(p.out, p.L.off_b + 4 * groups_all, p.L.off_c);
         // Escape bytes are written only below out_capacity; the stream is
         // complete exactly when its total fits.
-        write_header(p, m, p.L.off_d + 3 * m > p.cap ? UZIP_FLAG_CAPACITY : 0u);
+        write_header(p, m, stream_total(p, m) > p.cap ? UZIP_FLAG_CAPACITY : 0u);
     }
     if (rtotal == 0) return;
 
@@ -721,16 +728,21 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
     // 16-byte piece, so whole pieces can be copied out -- and store them with
     // coalesced 16-byte stores, unless there are too many, then store them
     // directly.
-    const uint64_t dbase = p.L.off_d + 3ull * pre;
-    const uint32_t dbytes = 3 * rtotal;
+    const bool sent = p.fmt == kSentinel;  // values only, at the escape's rank
+    const uint64_t dbase = p.L.off_d + (sent ? (uint64_t)pre : 3ull * pre);
+    const uint32_t dbytes = sent ? rtotal : 3 * rtotal;
     const uint32_t lead = (uint32_t)(dbase & 15);
     const bool staged = lead + dbytes <= kStageBytes;
     // One escape: its position bytes at block offset rel_pos, its value at rel_val.
     auto emit = [&](uint32_t rel_pos, uint32_t rel_val, uint32_t pos, uint32_t expo) {
         if (staged) {
-            stage[lead + rel_pos] = (uint8_t)(pos & 0xFF);
-            stage[lead + rel_pos + 1] = (uint8_t)(pos >> 8);
+            if (!sent) {
+                stage[lead + rel_pos] = (uint8_t)(pos & 0xFF);
+                stage[lead + rel_pos + 1] = (uint8_t)(pos >> 8);
+            }
             stage[lead + rel_val] = (uint8_t)expo;
+        } else if (sent) {
+            if (dbase + rel_val < p.cap) p.out[dbase + rel_val] = (uint8_t)expo;
         } else if (dbase + rel_val < p.cap && dbase + rel_pos + 1 < p.cap) {
             p.out[dbase + rel_pos] = (uint8_t)(pos & 0xFF);
             p.out[dbase + rel_pos + 1] = (uint8_t)(pos >> 8);
@@ -741,7 +753,10 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
         const uint32_t cstart = s_cp[q];
         const uint32_t k = s_cp[q + 1] - cstart;
         const uint32_t rank = rank_in_range - cstart;
-        emit(3 * cstart + 2 * rank, 3 * cstart + 2 * k + rank, off - q * C, expo);
+        if (sent)
+            emit(0, rank_in_range, 0, expo);
+        else
+            emit(3 * cstart + 2 * rank, 3 * cstart + 2 * k + rank, off - q * C, expo);
     };
     if (kRounds == 1 && __any_sync(0xffffffffu, n_in[0] > kParallelAbove)) {
         // Some unit has many escapes: go escape-parallel. Lane l takes range
@@ -789,7 +804,7 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
                     const uint32_t cstart = s_cp[q];
                     const uint32_t k = s_cp[q + 1] - cstart;
                     uint32_t rel_pos = 3 * cstart + 2 * (rank - cstart);
-                    uint32_t rel_val = 3 * cstart + 2 * k + (rank - cstart);
+                    uint32_t rel_val = sent ? rank : 3 * cstart + 2 * k + (rank - cstart);
                     bool more;
                     for (;;) {
                         const uint32_t pos = off - qbeg, expo = ent >> 16;
@@ -1079,6 +1094,21 @@ extern "C" UZIP_API int uzip_e5m2_encode(const void* d_in_e5m2, size_t n, uint32
                                          size_t* h_out_bytes, uzip_stream_t stream) {
     return encode_impl(d_in_e5m2, n, chunk, d_codebook, d_out, out_capacity, d_workspace, workspace_bytes,
                        h_out_bytes, stream, kE5M2);
+}
+
+// ------------------------------------------------------ Top-15 + sentinel
+
+extern "C" UZIP_API int uzip_sentinel_encode(const void* d_in_bf16, size_t n, uint32_t chunk,
+                                             const void* d_codebook, void* d_out, size_t out_capacity,
+                                             void* d_workspace, size_t workspace_bytes, size_t* h_out_bytes,
+                                             uzip_stream_t stream) {
+    return encode_impl(d_in_bf16, n, chunk, d_codebook, d_out, out_capacity, d_workspace, workspace_bytes,
+                       h_out_bytes, stream, kSentinel);
+}
+
+extern "C" UZIP_API size_t uzip_sentinel_compressed_size(size_t n, size_t n_escapes, uint32_t chunk) {
+    if (!chunk_valid(chunk) || n > UZIP_MAX_N || n_escapes > n) return 0;
+    return (size_t)(layout_of(n, chunk).off_d + (uint64_t)n_escapes);
 }
 
 extern "C" UZIP_API size_t uzip_e5m2_compressed_size(size_t n, size_t n_escapes, uint32_t chunk) {

@@ -15,6 +15,7 @@ namespace uzip {
 
 constexpr uint32_t kStreamMagic = 0x31505A55u;    // "UZP1" little endian
 constexpr uint32_t kStreamMagicE5 = 0x31455A55u;  // "UZE1": the FP8 E5M2 stream
+constexpr uint32_t kStreamMagicS = 0x31535A55u;   // "UZS1": the Top-15 + sentinel stream
 constexpr uint32_t kCodebookMagic = 0x42435A55u;  // "UZCB" little endian
 
 __host__ __device__ __forceinline__ uint64_t pad16(uint64_t v) { return (v + 15) & ~uint64_t(15); }
@@ -34,10 +35,11 @@ __host__ __device__ __forceinline__ Layout layout_of(uint64_t n, uint32_t chunk)
     return L;
 }
 
-// Value formats: BF16 (the codec of the page's §3) and FP8 E5M2 (§4.2 /
-// appendix C: the same Top-16 framework on E5M2 bytes). An E5M2 stream keeps
-// three bits of sign and mantissa per value, eight values per 3 bytes.
-enum Format : uint32_t { kBF16 = 0, kE5M2 = 1 };
+// Stream formats: BF16 (the codec of the page's §3), FP8 E5M2 (§4.2 /
+// appendix C: the same Top-16 framework on E5M2 bytes; three bits of sign and
+// mantissa per value, eight values per 3 bytes) and BF16 Top-15 + sentinel
+// (§3.4, Table 6: code 15 marks an escape, one byte per escape, no positions).
+enum Format : uint32_t { kBF16 = 0, kE5M2 = 1, kSentinel = 2 };
 
 __host__ __device__ __forceinline__ Layout layout_e5m2_of(uint64_t n, uint32_t chunk) {
     Layout L;
