@@ -286,9 +286,9 @@ UZIP_API int uzip_sentinel_encode(const void *d_in_bf16, size_t n, uint32_t chun
                                   void *d_out, size_t out_capacity, void *d_workspace, size_t workspace_bytes,
                                   size_t *h_out_bytes, uzip_stream_t stream);
 
-/* Decode a sentinel stream; arguments, checks and errors as uzip_decode's.
- * An escape past its chunk's values, or a chunk inside a decode tile whose
- * code-15 count differs from its offsets, gives UZIP_ERR_CORRUPT. */
+/* Decode a sentinel stream; arguments and errors as uzip_decode's. Besides
+ * the header, a chunk holding more or fewer code 15s than its offsets give
+ * values, or offsets that do not run from 0 to M, give UZIP_ERR_CORRUPT. */
 UZIP_API int uzip_sentinel_decode(const void *d_stream, size_t stream_bytes, void *d_out_bf16, size_t n,
                                   uint32_t *d_status, uzip_stream_t stream);
 

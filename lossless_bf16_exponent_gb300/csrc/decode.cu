@@ -348,17 +348,54 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
 // Sentinel (code 15) flags of eight codes: bit 4i set when nibble i is 15.
 __device__ __forceinline__ uint32_t sentinel_bits(uint32_t w) { return w & (w >> 1) & (w >> 2) & (w >> 3) & 0x11111111u; }
 
-// Decoder for the Top-15 + sentinel format (page §3.4, Table 6): no escape
-// positions are stored, so every tile first counts code 15s -- per thread,
-// then a block scan -- to give each escape its rank inside its chunk and
-// hence its value's index behind the chunk's offset; the dense lookup, the
-// patch and the store follow. Each thread takes 32 consecutive values.
-__global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_sentinel_kernel(const Params p) {
-    static_assert(kTile == kThreads * 32, "one 32-value slot per thread");
-    __shared__ uint32_t s_codes[kTile / 8];       // the tile's code words, one per group of 8 values
-    __shared__ uint32_t s_pre[kThreads + 1];      // code 15s before each thread's slot
-    __shared__ uint32_t s_warp[kThreads / 32];
-    __shared__ uint32_t s_cbase[kTile / 8 + 1];   // per chunk of the tile: tile count at its start - its earlier count
+// 16-byte asynchronous global -> shared copy (cp.async) and its wait.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+#ifndef UZIP_SDEC_MIN_BLOCKS
+#define UZIP_SDEC_MIN_BLOCKS 4
+#endif
+#ifndef UZIP_SDEC_WINDOW
+#define UZIP_SDEC_WINDOW 256
+#endif
+
+// Decoder for the Top-15 + sentinel format (page §3.4, Table 6). No escape
+// positions are stored: the k-th code 15 of the stream takes value k of the
+// value array (chunk c's values start at offsets[c]), so a tile's escapes are
+// one contiguous run of values. Each CTA decodes one contiguous range of
+// tiles of 8192 values and carries g0 -- the index of its tile's first
+// escape -- from tile to tile; only its first tile derives g0 from the
+// offsets (plus, when that tile's chunk began earlier, a count of the
+// chunk's earlier code 15s). Groups of eight values as in decode_kernel
+// (group g = tid + r * threads: coalesced loads and stores). Per tile
+//   1. each thread loads its four groups and the tile's chunk offsets;
+//   2. code-15 counts of the four group rows, packed two per word, are
+//      scanned within each warp (shuffles); one barrier publishes the warp
+//      totals, giving every thread the code 15s before each of its groups;
+//   3. the next tile's run of values (a window of UZIP_SDEC_WINDOW bytes
+//      from its g0) is requested with cp.async, so a tile's patch reads
+//      shared memory (values past the window are read from global memory);
+//   4. lookup, patch, rebuild, 16-byte stores.
+// Shared buffers are double-buffered by tile parity: one barrier per tile.
+// Checks, the oracle's: the header; offsets[0] = 0, offsets[nc] = M; every
+// chunk holds as many code 15s as its offsets give values (checked in the
+// tile where the chunk ends: its end offset must equal g0 + the code 15s
+// before it), so a stream is refused exactly when the oracle refuses it.
+// Every value index is checked against M before the read.
+__global__ void __launch_bounds__(kThreads, UZIP_SDEC_MIN_BLOCKS) decode_sentinel_kernel(const Params p) {
+    constexpr int kWarps = kThreads / 32;
+    constexpr uint32_t kMaxOffs = kTile / UZIP_MIN_CHUNK + 2;  // offsets a tile can need
+    constexpr uint32_t kWin = UZIP_SDEC_WINDOW + 16;           // window bytes from g0 rounded down to 16
+    static_assert(kGroupsPerThread == 4, "two packed rows of two 16-bit counts");
+    static_assert(kWin / 16 <= kThreads, "one 16-byte copy per thread");
+    __shared__ uint32_t s_pre[2][2][kThreads];  // per thread: rows (0,1) and (2,3) of code 15s of earlier lanes
+    __shared__ uint32_t s_wt[2][2][kWarps];     // per warp: the same, totals
+    __shared__ uint32_t s_off[2][kMaxOffs];     // offsets[c_first ..]
+    __shared__ __align__(16) uint8_t s_win[2][kWin];
+    __shared__ uint32_t s_red[kWarps];
     __shared__ int s_bad;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -381,130 +418,174 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_sentinel
         return;
     }
     const uint32_t n32 = (uint32_t)p.n;
+    const uint32_t m32 = (uint32_t)m;
     const uint8_t* A = p.s + L.off_a;
     const uint8_t* B = p.s + L.off_b;
     const uint32_t* Cw = reinterpret_cast<const uint32_t*>(p.s + L.off_c);
     const uint8_t* D = p.s + L.off_d;
+    const uint64_t d_room = p.stream_bytes - L.off_d;  // readable bytes from D on
     const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;
     const uint32_t tiles = (n32 + kTile - 1) / kTile;
+    const uint32_t t_begin = (uint32_t)((uint64_t)tiles * blockIdx.x / gridDim.x);
+    const uint32_t t_end = (uint32_t)((uint64_t)tiles * (blockIdx.x + 1) / gridDim.x);
     if (tid == 0) s_bad = 0;
-    __syncthreads();
+    if (t_begin >= t_end) return;  // uniform per CTA; no barrier has been passed
 
-    // code 15s of the tile before value f (0 <= f <= tlen)
-    auto before = [&](uint32_t f) {
-        const uint32_t t = f / 32, r = f % 32;
-        uint32_t c = s_pre[t];
-        for (uint32_t q = 0; q < r / 8; q++) c += __popc(sentinel_bits(s_codes[4 * t + q]));
-        if (r % 8) c += __popc(sentinel_bits(s_codes[4 * t + r / 8]) & ((1u << (4 * (r % 8))) - 1));
-        return c;
+    // the window of values [w0, w0 + kWin) from index g into s_win[b] (16-byte copies inside the buffer)
+    auto request_window = [&](uint32_t g, int b) {
+        const uint64_t w0 = g & ~15u;
+        if (tid < (int)(kWin / 16) && w0 + 16 * (tid + 1) <= d_room) cp_async16(&s_win[b][16 * tid], D + w0 + 16 * tid);
     };
 
-    for (uint32_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+    // g0 of the first tile: offsets[c_first] + the code 15s of chunk c_first before the tile
+    uint32_t g0;
+    {
+        const uint32_t e0 = t_begin * kTile, c_first = e0 / chunk;
+        uint32_t e = 0;
+        for (uint32_t w = c_first * chunk / 8 + tid; w < e0 / 8; w += kThreads)
+            e += __popc(sentinel_bits(__ldg(reinterpret_cast<const uint32_t*>(B) + w)));
+        e = __reduce_add_sync(0xffffffffu, e);
+        if (lane == 0) s_red[warp] = e;
+        __syncthreads();
+        g0 = __ldg(Cw + c_first);
+#pragma unroll
+        for (int w = 0; w < kWarps; w++) g0 += s_red[w];
+        request_window(g0, 0);
+    }
+
+    int par = 0;
+    for (uint32_t t = t_begin; t < t_end; t++, par ^= 1) {
         const uint32_t e0 = t * kTile;
         const uint32_t tlen = min(kTile, n32 - e0);
-        const uint32_t v0 = 32 * tid;
-        const bool mine = v0 < tlen;
-        uint4 a0 = make_uint4(0, 0, 0, 0), a1 = a0, cv = a0;
-        if (mine) {  // padded sections: a whole slot stays inside the stream, zeros past n
-            a0 = __ldg(reinterpret_cast<const uint4*>(A + e0 + v0));
-            a1 = __ldg(reinterpret_cast<const uint4*>(A + e0 + v0 + 16));
-            cv = __ldg(reinterpret_cast<const uint4*>(B + e0 / 2 + 16 * tid));
-        }
-        const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-        uint32_t cnt = 0;
+        const uint32_t tgroups = (tlen + 7) / 8;
+        const uint32_t c_first = e0 / chunk, c_last = (e0 + tlen - 1) / chunk;
+
+        // 1. loads (the padded sections make whole-group loads safe at the ragged tail)
+        uint2 av[kGroupsPerThread];
+        uint32_t cv[kGroupsPerThread];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            s_codes[4 * tid + q] = cw[q];
-            cnt += __popc(sentinel_bits(cw[q]));
+        for (int r = 0; r < kGroupsPerThread; r++) {
+            const uint32_t g = tid + r * kThreads;
+            av[r] = make_uint2(0, 0);
+            cv[r] = 0;
+            if (g < tgroups) {
+                av[r] = ld_stream_v2(A + e0 + 8 * g);
+                cv[r] = ld_stream_u32(B + e0 / 2 + 4 * g);
+            }
         }
-        // block-wide exclusive scan of the per-thread counts
-        uint32_t incl = cnt;
+        for (uint32_t k = tid; k <= c_last - c_first + 1; k += kThreads) s_off[par][k] = __ldg(Cw + c_first + k);
+
+        // 2. counts, warp scans, one barrier
+        uint32_t sb[kGroupsPerThread];
+        uint32_t p01 = 0, p23 = 0;
+#pragma unroll
+        for (int r = 0; r < kGroupsPerThread; r++) {
+            const uint32_t g = tid + r * kThreads;
+            sb[r] = sentinel_bits(cv[r]);
+            if (8 * g + 8 > tlen) sb[r] &= 8 * g < tlen ? (1u << (4 * (tlen - 8 * g))) - 1 : 0u;  // padding past n
+            const uint32_t c = __popc(sb[r]) << (16 * (r & 1));
+            if (r < 2) p01 += c;
+            else p23 += c;
+        }
+        uint32_t i01 = p01, i23 = p23;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) s_warp[warp] = incl;
-        __syncthreads();
-        uint32_t off = 0;
-        for (int w = 0; w < warp; w++) off += s_warp[w];
-        s_pre[tid] = off + incl - cnt;
-        if (tid == kThreads - 1) s_pre[kThreads] = off + incl;
-        __syncthreads();
-        // code 15s that the tile's first chunk holds in earlier tiles (at most chunk / 8 code words), summed
-        // by the whole block; s_warp is free again since the barrier above
-        const uint32_t c_first = e0 / chunk, c_last = (e0 + tlen - 1) / chunk;
-        uint32_t early = 0;
-        if (c_first * chunk < e0) {
-            const uint32_t* B32 = reinterpret_cast<const uint32_t*>(B);
-            for (uint32_t g = c_first * chunk / 8 + tid; g < e0 / 8; g += kThreads)
-                early += __popc(sentinel_bits(__ldg(B32 + g)));
-            early = __reduce_add_sync(0xffffffffu, early);
-            if (lane == 0) s_warp[warp] = early;
-            __syncthreads();
-            early = 0;
-#pragma unroll
-            for (int w = 0; w < kThreads / 32; w++) early += s_warp[w];
-        }
-        // every chunk overlapping the tile: its rank base, and its count checked when it lies inside the tile
-        for (uint32_t cc = tid; cc <= c_last - c_first; cc += kThreads) {
-            const uint32_t c = c_first + cc, cs = c * chunk;
-            uint32_t base;
-            if (cs >= e0) {
-                base = before(cs - e0);
-                const uint32_t ce = min(cs + chunk, n32);
-                if (ce <= e0 + tlen && before(ce - e0) - base != Cw[c + 1] - Cw[c]) s_bad = 1;
-            } else {  // the chunk began in an earlier tile
-                base = 0u - early;
+            const uint32_t v01 = __shfl_up_sync(0xffffffffu, i01, o);
+            const uint32_t v23 = __shfl_up_sync(0xffffffffu, i23, o);
+            if (lane >= o) {
+                i01 += v01;
+                i23 += v23;
             }
-            s_cbase[cc] = base;
         }
+        s_pre[par][0][tid] = i01 - p01;
+        s_pre[par][1][tid] = i23 - p23;
+        if (lane == 31) {
+            s_wt[par][0][warp] = i01;
+            s_wt[par][1][warp] = i23;
+        }
+        cp_async_wait_all();  // this tile's window
         __syncthreads();
-        if (mine) {
-            const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const uint32_t valid = min(32u, tlen - v0);  // values of the slot below n
-            uint32_t o[16];
+
+        uint32_t w01 = 0, w23 = 0, t01 = 0, t23 = 0;
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-                uint32_t e_lo = lookup4(cw[q] & 0xFFFF, d0, d1, d2, d3);
-                uint32_t e_hi = lookup4(cw[q] >> 16, d0, d1, d2, d3);
-                uint32_t sb = sentinel_bits(cw[q]);
-                // a code 15 in the padding past n (only in a corrupt stream) is not an escape
-                if (valid < 8 * q + 8) sb &= valid > 8u * q ? (1u << (4 * (valid - 8 * q))) - 1 : 0u;
-                while (sb) {  // escapes: their values, in order, behind their chunk's offset
-                    const uint32_t i = (__ffs(sb) - 1) / 4;  // value i of the group
-                    sb &= sb - 1;
-                    const uint32_t el = e0 + v0 + 8 * q + i;
-                    const uint32_t c = el / chunk;
-                    const uint32_t rank = before(v0 + 8 * q + i) - s_cbase[c - c_first];
-                    const uint32_t idx = Cw[c] + rank;
+        for (int w = 0; w < kWarps; w++) {
+            const uint32_t x01 = s_wt[par][0][w], x23 = s_wt[par][1][w];
+            if (w < warp) {
+                w01 += x01;
+                w23 += x23;
+            }
+            t01 += x01;
+            t23 += x23;
+        }
+        // code 15s before each group row, in element order
+        const uint32_t row1 = t01 & 0xFFFF, row2 = row1 + (t01 >> 16), row3 = row2 + (t23 & 0xFFFF);
+        const uint32_t tile_total = row3 + (t23 >> 16);
+
+        // 3. the next tile's window
+        if (t + 1 < t_end) request_window(g0 + tile_total, par ^ 1);
+
+        // code 15s of the tile before value f (f a multiple of 8, or f = tlen)
+        auto before = [&](uint32_t f) {
+            if (f >= tlen) return tile_total;
+            const uint32_t G = f / 8, r = G / kThreads, tt = G % kThreads, ww = tt / 32;
+            uint32_t x = s_pre[par][r >> 1][tt];
+            for (uint32_t k = 0; k < ww; k++) x += s_wt[par][r >> 1][k];
+            const uint32_t base = r == 0 ? 0u : r == 1 ? row1 : r == 2 ? row2 : row3;
+            return base + ((x >> (16 * (r & 1))) & 0xFFFF);
+        };
+        // every chunk ending in the tile: its end offset against the code 15s before it
+        for (uint32_t k = tid; k <= c_last - c_first; k += kThreads) {
+            const uint32_t c = c_first + k;
+            const uint32_t ce = min((c + 1) * chunk, n32);
+            const uint32_t o1 = s_off[par][k + 1];
+            if (ce <= e0 + tlen && g0 + before(ce - e0) != o1) s_bad = 1;
+            if ((c == 0 && s_off[par][k] != 0) || (c + 1 == nc && o1 != m32)) s_bad = 1;
+        }
+
+        // 4. decode, patch, store
+        const uint32_t own01 = w01 + s_pre[par][0][tid], own23 = w23 + s_pre[par][1][tid];
+        const uint32_t wbase = g0 & ~15u;
+#pragma unroll
+        for (int r = 0; r < kGroupsPerThread; r++) {
+            const uint32_t g = tid + r * kThreads;
+            if (g >= tgroups) continue;
+            uint32_t e_lo = lookup4(cv[r] & 0xFFFF, d0, d1, d2, d3);
+            uint32_t e_hi = lookup4(cv[r] >> 16, d0, d1, d2, d3);
+            uint32_t bits = sb[r];
+            if (bits) {
+                const uint32_t own = r == 0 ? (own01 & 0xFFFF) : r == 1 ? (own01 >> 16) + row1
+                                   : r == 2 ? (own23 & 0xFFFF) + row2 : (own23 >> 16) + row3;
+                uint32_t idx = g0 + own;
+                do {
+                    const uint32_t i = (__ffs(bits) - 1) / 4;  // value i of the group
+                    bits &= bits - 1;
                     uint32_t ev = 0;
-                    if (idx < Cw[c + 1] && idx < m) ev = D[idx];
-                    else s_bad = 1;
+                    const uint32_t wo = idx - wbase;
+                    if (idx >= m32) s_bad = 1;
+                    else if (wo < kWin && wbase + 16 * (wo / 16 + 1) <= d_room) ev = s_win[par][wo];
+                    else ev = D[idx];
+                    idx++;
                     const uint32_t sh = 8 * (i & 3);
                     if (i < 4) e_lo = (e_lo & ~(0xFFu << sh)) | (ev << sh);
                     else e_hi = (e_hi & ~(0xFFu << sh)) | (ev << sh);
-                }
-                const uint2 lo = rebuild4(e_lo, aw[2 * q]);
-                const uint2 hi = rebuild4(e_hi, aw[2 * q + 1]);
-                o[4 * q] = lo.x;
-                o[4 * q + 1] = lo.y;
-                o[4 * q + 2] = hi.x;
-                o[4 * q + 3] = hi.y;
+                } while (bits);
             }
-            const uint32_t ge = e0 + v0;
-            if (ge + 32 <= n32) {
-                uint4* dst = reinterpret_cast<uint4*>(p.out + ge);
-#pragma unroll
-                for (int k = 0; k < 4; k++) dst[k] = make_uint4(o[4 * k], o[4 * k + 1], o[4 * k + 2], o[4 * k + 3]);
+            const uint2 lo = rebuild4(e_lo, av[r].x);
+            const uint2 hi = rebuild4(e_hi, av[r].y);
+            const uint32_t ge = e0 + 8 * g;
+            if (ge + 8 <= n32) {
+                *reinterpret_cast<uint4*>(p.out + ge) = make_uint4(lo.x, lo.y, hi.x, hi.y);
             } else {
+                const uint32_t wv[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
-                for (uint32_t i = 0; i < 32; i++)
-                    if (ge + i < n32) p.out[ge + i] = (uint16_t)(o[i / 2] >> (16 * (i & 1)));
+                for (uint32_t i = 0; i < 8; i++)
+                    if (ge + i < n32) p.out[ge + i] = (uint16_t)(wv[i / 2] >> (16 * (i & 1)));
             }
         }
-        __syncthreads();  // the shared tables are rewritten by the next tile
+        g0 += tile_total;
     }
+    cp_async_wait_all();
+    __syncthreads();  // every thread's s_bad write before it is read
     if (s_bad && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
 }
 

@@ -180,6 +180,52 @@ def test_corrupt_streams_are_refused(uz, orc, chunk):
     assert int(status.item()) == _lib.ERR_CORRUPT
 
 
+@pytest.mark.parametrize("chunk", [8, 1000, 1024, 8200, 65536])
+def test_refused_exactly_when_the_oracle_refuses(uz, orc, chunk):
+    """Random damage to the header, the offsets and the codes: the GPU status
+    equals the oracle's, and where both accept, the values are equal."""
+    rng = np.random.default_rng(chunk + 1)
+    n = 3 * 65536 + 1001
+    xh = (rng.standard_normal(n).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    xh[rng.integers(0, n, 2000)] = 0x7F80
+    exps = orc.calibrate(xh)
+    rc, good = orc.sentinel_encode(xh, exps, chunk)
+    off_c, nc = _offsets(good)
+    off_b = 64 + -(-n // 16) * 16
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    refusals = 0
+    for trial in range(60):
+        bad = good.copy()
+        kind = trial % 4
+        if kind == 0:  # one offset moved
+            j = int(rng.integers(0, nc + 1))
+            o = bad[off_c:off_c + 4 * (nc + 1)].view("<u4")
+            o[j] = max(0, int(o[j]) + int(rng.choice([-2, -1, 1, 2])))
+        elif kind == 1:  # a code turned into 15 or a 15 into another code
+            i = int(rng.integers(0, n))
+            b = off_b + i // 2
+            sh = 4 * (i % 2)
+            code = (bad[b] >> sh) & 15
+            new = int(rng.integers(0, 15)) if code == 15 else 15
+            bad[b] = (bad[b] & (0xF0 >> sh)) | (new << sh)
+        elif kind == 2:  # a random byte of codes or offsets
+            j = int(rng.integers(off_b, good.size - int.from_bytes(good[24:32].tobytes(), "little")))
+            bad[j] ^= np.uint8(1 << int(rng.integers(0, 8)))
+        else:  # a random header byte
+            j = int(rng.integers(0, 64))
+            bad[j] ^= np.uint8(1 << int(rng.integers(0, 8)))
+        orc_rc, want = orc.sentinel_decode(bad, n)
+        status.zero_()
+        y = uz.sentinel_decode(torch.from_numpy(bad).cuda(), n, status=status)
+        got = int(status.item())
+        assert (got == 0) == (orc_rc == 0), (trial, kind, got, orc_rc)
+        if got == 0:
+            assert np.array_equal(W.as_u16(y), want), trial
+        else:
+            refusals += 1
+    assert refusals >= 20
+
+
 def test_code_count_mismatch_inside_a_tile(uz, orc):
     """A chunk that lies inside one decode tile and holds more code 15s than
     its offsets give values is refused."""
