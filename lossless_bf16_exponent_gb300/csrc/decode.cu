@@ -57,6 +57,18 @@ __device__ __forceinline__ uint32_t lookup4(uint32_t c16, uint32_t d0, uint32_t 
     return prmt(lo, hi, 0x3210u | ((c16 & 0x8888u) >> 1));
 }
 
+// Eight codes (nibbles of a code word) -> eight exponent bytes (e_lo: values
+// 0..3, e_hi: values 4..7). The selectors of both halves are formed once for
+// the whole word; prmt reads only the low 16 bits of a selector.
+__device__ __forceinline__ void lookup8(uint32_t cw, uint32_t d0, uint32_t d1, uint32_t d2, uint32_t d3,
+                                        uint32_t& e_lo, uint32_t& e_hi) {
+    const uint32_t sel = cw & 0x77777777u;                       // byte of the 8-entry half
+    const uint32_t pick = ((cw >> 1) & 0x44444444u) | 0x32103210u;  // half per value
+    const uint32_t sel_hi = sel >> 16, pick_hi = pick >> 16;
+    e_lo = prmt(prmt(d0, d1, sel), prmt(d2, d3, sel), pick);
+    e_hi = prmt(prmt(d0, d1, sel_hi), prmt(d2, d3, sel_hi), pick_hi);
+}
+
 // Four exponent bytes + four sign-mantissa bytes -> four BF16 values.
 __device__ __forceinline__ uint2 rebuild4(uint32_t e4, uint32_t a4) {
     const uint32_t hi = (a4 & 0x80808080u) | ((e4 >> 1) & 0x7F7F7F7Fu);  // sign | exponent bits 7..1
@@ -79,7 +91,10 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
 }
 
 __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(const Params p) {
-    __shared__ uint32_t s_mask[2][kTile / 32];  // escape bitmap, double-buffered by tile parity
+    static_assert(kGroupsPerThread == 4, "one 32-bit escape word per thread");
+    // escape bitmap, double-buffered by tile parity: word w holds the four groups w + r * threads, bit
+    // 8 r + i for value i of group r, so each thread reads one word per tile
+    __shared__ uint32_t s_mask[2][kThreads];
     __shared__ uint8_t s_val[kTile];
     __shared__ int s_bad;
 
@@ -110,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
     const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;  // decode table: code k -> byte k
     const uint32_t tiles = (n32 + kTile - 1) / kTile;
 
-    for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[0][i] = 0;
+    s_mask[0][tid] = 0;
     if (tid == 0) s_bad = 0;
     __syncthreads();
 
@@ -118,9 +133,10 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
     for (uint32_t t = blockIdx.x; t < tiles; t += gridDim.x, par ^= 1) {
         const uint32_t e0 = t * kTile;
         const uint32_t tlen = min(kTile, n32 - e0);
+        const bool full = tlen == kTile;  // uniform: every group whole
         const uint32_t tgroups = (tlen + 7) / 8;
-        const uint8_t* At = A + e0;
-        const uint8_t* Bt = B + e0 / 2;
+        const uint8_t* At = A + e0 + 8 * tid;
+        const uint8_t* Bt = B + e0 / 2 + 4 * tid;
 
         // 1. dense loads first, so their latency overlaps the escape pass (the
         //    padded sections make whole-group loads safe at the ragged tail).
@@ -128,15 +144,17 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
         uint32_t cv[kGroupsPerThread];
 #pragma unroll
         for (int r = 0; r < kGroupsPerThread; r++) {
-            const uint32_t g = tid + r * kThreads;
-            if (g < tgroups) {
-                av[r] = ld_stream_v2(At + 8 * g);
-                cv[r] = ld_stream_u32(Bt + 4 * g);
+            if (full || tid + r * kThreads < tgroups) {
+                av[r] = ld_stream_v2(At + 8 * r * kThreads);
+                cv[r] = ld_stream_u32(Bt + 4 * r * kThreads);
+            } else {
+                av[r] = make_uint2(0, 0);
+                cv[r] = 0;
             }
         }
         // 2. clear the other bitmap for the next tile; scatter this tile's
         //    escapes (chunks overlapping [e0, e0 + tlen)) into this one.
-        for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[par ^ 1][i] = 0;
+        s_mask[par ^ 1][tid] = 0;
         const uint32_t c_first = e0 / chunk, c_last = (e0 + tlen - 1) / chunk;
         bool bad = false;
         for (uint32_t c = c_first + warp; c <= c_last; c += kThreads / 32) {
@@ -158,9 +176,9 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
                 }
                 const uint32_t el = cbase + pos;
                 if (el >= e0 && el < e0 + tlen) {
-                    const uint32_t li = el - e0;
+                    const uint32_t li = el - e0, g = li >> 3;
                     s_val[li] = blk[2 * k + j];
-                    atomicOr(&s_mask[par][li >> 5], 1u << (li & 31));
+                    atomicOr(&s_mask[par][g % kThreads], 1u << (8 * (g / kThreads) + (li & 7)));
                 }
             }
         }
@@ -168,13 +186,15 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
         __syncthreads();
 
         // 3. decode, patch, store.
+        const uint32_t fix_all = s_mask[par][tid];
+        uint16_t* out = p.out + e0 + 8 * tid;
 #pragma unroll
         for (int r = 0; r < kGroupsPerThread; r++) {
             const uint32_t g = tid + r * kThreads;
-            if (g >= tgroups) continue;
-            uint32_t e_lo = lookup4(cv[r] & 0xFFFF, d0, d1, d2, d3);
-            uint32_t e_hi = lookup4(cv[r] >> 16, d0, d1, d2, d3);
-            const uint32_t fix = (s_mask[par][g >> 2] >> ((g & 3) * 8)) & 0xFF;
+            if (!full && g >= tgroups) continue;
+            uint32_t e_lo, e_hi;
+            lookup8(cv[r], d0, d1, d2, d3, e_lo, e_hi);
+            const uint32_t fix = (fix_all >> (8 * r)) & 0xFF;
             if (fix) {
 #pragma unroll
                 for (int i = 0; i < 8; i++) {
@@ -188,10 +208,10 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
             }
             const uint2 lo = rebuild4(e_lo, av[r].x);
             const uint2 hi = rebuild4(e_hi, av[r].y);
-            const uint32_t ge = e0 + 8 * g;
-            if (ge + 8 <= n32) {
-                *reinterpret_cast<uint4*>(p.out + ge) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            if (full || e0 + 8 * g + 8 <= n32) {
+                *reinterpret_cast<uint4*>(out + 8 * r * kThreads) = make_uint4(lo.x, lo.y, hi.x, hi.y);
             } else {
+                const uint32_t ge = e0 + 8 * g;
                 const uint32_t w[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
                 for (uint32_t i = 0; i < 8; i++)
