@@ -115,9 +115,136 @@ __global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const void* __r
     if (threadIdx.x == 0) *counter = 0;
 }
 
+// Histogram of a large input (a whole tensor): the warp-merged shared
+// histogram above spends most of its time in __match_any_sync, so for large
+// inputs each thread counts into a private column of 16-bit counters instead
+// (256 bins x kPrivThreads columns, 192 KB of shared memory, one CTA per SM).
+// A column's word bank depends only on the thread, so no two lanes of a warp
+// meet in a bank whatever exponents they hold. Values are counted in pairs:
+// both counters are read, the second corrected when the exponents are equal,
+// and both written back in order. Every 65,408 values per thread (before a
+// 16-bit counter can overflow) the block folds the columns into per-bin
+// totals and clears them. The next round's 16 loads per thread are issued
+// before the current round is counted. The last block ranks, as above.
+constexpr int kPrivThreads = 384;
+constexpr int kPrivLoads = 16;
+constexpr uint32_t kEpochValues = 65408;  // per thread between folds, + one tail value < 65536
+constexpr size_t kPrivSmem = (size_t)256 * kPrivThreads * sizeof(uint16_t);
+#ifndef UZIP_HIST_PRIVATE_FROM
+#define UZIP_HIST_PRIVATE_FROM (1u << 22)
+#endif
+constexpr uint64_t kPrivateFrom = UZIP_HIST_PRIVATE_FROM;  // inputs at least this long use it
+
+__device__ __forceinline__ void count_pair(uint16_t* col, uint32_t e0, uint32_t e1) {
+    const uint32_t a0 = e0 * kPrivThreads, a1 = e1 * kPrivThreads;
+    const uint32_t c0 = col[a0];
+    const uint32_t c1 = col[a1] + (e0 == e1 ? 1u : 0u);
+    col[a0] = (uint16_t)(c0 + 1);
+    col[a1] = (uint16_t)(c1 + 1);
+}
+
+template <int kFmt>
+__global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(const void* __restrict__ xv, uint64_t n,
+                                                                            uint8_t* __restrict__ cb) {
+    constexpr uint32_t kPerVec = kFmt == kE5M2 ? 16 : 8;
+#ifdef UZIP_HIST_EPOCH_ROUNDS
+    constexpr uint32_t kRoundsPerEpoch = UZIP_HIST_EPOCH_ROUNDS;  // shorter epochs (tests of the fold)
+    static_assert(kRoundsPerEpoch * kPrivLoads * kPerVec <= kEpochValues, "16-bit counters");
+#else
+    constexpr uint32_t kRoundsPerEpoch = kEpochValues / (kPrivLoads * kPerVec);
+#endif
+    extern __shared__ uint4 s_dyn[];
+    uint16_t* cnt = reinterpret_cast<uint16_t*>(s_dyn);  // [bin][thread]
+    __shared__ bool s_last;
+    unsigned long long* hist = reinterpret_cast<unsigned long long*>(cb + UZIP_CB_HIST);
+    unsigned int* counter = reinterpret_cast<unsigned int*>(cb + kCbCounter);
+    const int tid = threadIdx.x;
+    uint16_t* col = cnt + tid;
+    const uint8_t* x8 = static_cast<const uint8_t*>(xv);
+
+    auto clear = [&]() {
+        for (uint32_t i = tid; i < kPrivSmem / 16; i += kPrivThreads) s_dyn[i] = make_uint4(0, 0, 0, 0);
+    };
+    auto count_vec = [&](const uint4 v) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            if (kFmt == kE5M2) {
+                count_pair(col, (w[q] >> 2) & 0x1F, (w[q] >> 10) & 0x1F);
+                count_pair(col, (w[q] >> 18) & 0x1F, (w[q] >> 26) & 0x1F);
+            } else {
+                count_pair(col, (w[q] >> 7) & 0xFF, (w[q] >> 23) & 0xFF);
+            }
+        }
+    };
+    uint32_t total = 0;  // thread t < 256: bin t's block total
+    auto fold = [&]() {
+        __syncthreads();
+        if (tid < 256) {
+            const uint4* row = reinterpret_cast<const uint4*>(cnt + tid * kPrivThreads);
+            for (int k = 0; k < kPrivThreads / 8; k++) {
+                const uint4 r = row[k];
+                total += (r.x & 0xFFFF) + (r.x >> 16) + (r.y & 0xFFFF) + (r.y >> 16) + (r.z & 0xFFFF) + (r.z >> 16) +
+                         (r.w & 0xFFFF) + (r.w >> 16);
+            }
+        }
+        __syncthreads();
+    };
+
+    clear();
+    __syncthreads();
+    const uint64_t groups = n / kPerVec;
+    if (blockIdx.x == 0 && (uint64_t)tid < n - groups * kPerVec) {  // ragged tail: one value per thread
+        const uint64_t i = groups * kPerVec + tid;
+        const uint32_t e = kFmt == kE5M2 ? (x8[i] >> 2) & 0x1F : (static_cast<const uint16_t*>(xv)[i] >> 7) & 0xFF;
+        col[e * kPrivThreads] += 1;
+    }
+    const uint64_t per_round = (uint64_t)gridDim.x * kPrivThreads * kPrivLoads;
+    const uint64_t rounds = (groups + per_round - 1) / per_round;
+    auto load_round = [&](uint64_t r, uint4* v) {
+        const uint64_t base = (r * gridDim.x + blockIdx.x) * (uint64_t)kPrivThreads * kPrivLoads + tid;
+#pragma unroll
+        for (int j = 0; j < kPrivLoads; j++) {
+            const uint64_t g = base + (uint64_t)j * kPrivThreads;
+            v[j] = g < groups ? ld_stream_v4(x8 + 16 * g) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    uint4 v[kPrivLoads], nv[kPrivLoads];
+    if (rounds) load_round(0, v);
+    for (uint64_t r0 = 0; r0 < rounds; r0 += kRoundsPerEpoch) {
+        const uint64_t r1 = min(rounds, r0 + kRoundsPerEpoch);
+        for (uint64_t r = r0; r < r1; r++) {
+            if (r + 1 < rounds) load_round(r + 1, nv);
+            const uint64_t base = (r * gridDim.x + blockIdx.x) * (uint64_t)kPrivThreads * kPrivLoads + tid;
+#pragma unroll
+            for (int j = 0; j < kPrivLoads; j++)
+                if (base + (uint64_t)j * kPrivThreads < groups) count_vec(v[j]);
+#pragma unroll
+            for (int j = 0; j < kPrivLoads; j++) v[j] = nv[j];
+        }
+        if (r1 < rounds) {  // fold before a counter can overflow
+            fold();
+            clear();
+            __syncthreads();
+        }
+    }
+    fold();
+    if (tid < 256 && total) atomicAdd(&hist[tid], (unsigned long long)total);
+    // The last block ranks the totals.
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(counter, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    rank_and_write(cb, n);
+    if (tid == 0) *counter = 0;
+}
+
 // Tables from exps[16] (shared memory), written by a 256-thread CTA.
 __device__ void write_tables(const uint8_t* exps, uint8_t* cb, uint64_t n_sample) {
     const int t = threadIdx.x;
+    if (t >= 256) return;
     uint8_t code = 0, esc = 1;
 #pragma unroll
     for (int k = 0; k < 16; k++)
@@ -139,22 +266,24 @@ __device__ void write_tables(const uint8_t* exps, uint8_t* cb, uint64_t n_sample
 }
 
 // Rank the blob's 256 totals (count descending, exponent ascending) and write
-// the codebook; one 256-thread CTA, totals read from L2.
+// the codebook; the first 256 threads of the CTA, totals read from L2.
 __device__ void rank_and_write(uint8_t* cb, uint64_t n_sample) {
     __shared__ unsigned long long cnt[256];
     __shared__ uint8_t exps[16];
     const int t = threadIdx.x;
     const unsigned long long* hist = reinterpret_cast<const unsigned long long*>(cb + UZIP_CB_HIST);
-    cnt[t] = __ldcg(hist + t);
+    if (t < 256) cnt[t] = __ldcg(hist + t);
     __syncthreads();
-    const unsigned long long mine = cnt[t];
-    int rank = 0;
+    if (t < 256) {
+        const unsigned long long mine = cnt[t];
+        int rank = 0;
 #pragma unroll 8
-    for (int i = 0; i < 256; i++) {
-        const unsigned long long c = cnt[i];
-        rank += (c > mine) || (c == mine && i < t);
+        for (int i = 0; i < 256; i++) {
+            const unsigned long long c = cnt[i];
+            rank += (c > mine) || (c == mine && i < t);
+        }
+        if (rank < 16) exps[rank] = (uint8_t)t;
     }
-    if (rank < 16) exps[rank] = (uint8_t)t;
     __syncthreads();
     write_tables(exps, cb, n_sample);
 }
@@ -188,6 +317,13 @@ int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
     int dev = 0, sms = 0, per_sm = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
     UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (n_sample >= kPrivateFrom) {  // a large input: private-column histogram, one CTA per SM
+        auto* pk = fmt == kE5M2 ? histogram_private_kernel<kE5M2> : histogram_private_kernel<kBF16>;
+        UZIP_CUDA_TRY(cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrivSmem));
+        pk<<<(unsigned)sms, kPrivThreads, kPrivSmem, s>>>(d_sample_bf16, n_sample, cb);
+        UZIP_CUDA_TRY(cudaGetLastError());
+        return UZIP_OK;
+    }
     auto* kernel = fmt == kE5M2 ? calibrate_kernel<kE5M2> : calibrate_kernel<kBF16>;
     UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kHistThreads, 0));
     // One block per kHistThreads * kLoadsPerThread 16-byte loads, up to a

@@ -49,14 +49,6 @@ struct Params {
     uint32_t* status;
 };
 
-// Four codes (nibbles of c16, value i in nibble i) -> four exponent bytes.
-__device__ __forceinline__ uint32_t lookup4(uint32_t c16, uint32_t d0, uint32_t d1, uint32_t d2, uint32_t d3) {
-    const uint32_t sel = c16 & 0x7777u;
-    const uint32_t lo = prmt(d0, d1, sel);  // codes 0..7
-    const uint32_t hi = prmt(d2, d3, sel);  // codes 8..15
-    return prmt(lo, hi, 0x3210u | ((c16 & 0x8888u) >> 1));
-}
-
 // Eight codes (nibbles of a code word) -> eight exponent bytes (e_lo: values
 // 0..3, e_hi: values 4..7). The selectors of both halves are formed once for
 // the whole word; prmt reads only the low 16 bits of a selector.
@@ -331,9 +323,11 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
             uint32_t o[8];
 #pragma unroll
             for (int q = 0; q < 4; q++) {
+                uint32_t e8[2];
+                lookup8(cw[q], d0, d1, d2, d3, e8[0], e8[1]);
 #pragma unroll
                 for (int hh = 0; hh < 2; hh++) {
-                    uint32_t e4 = lookup4((cw[q] >> (16 * hh)) & 0xFFFF, d0, d1, d2, d3);
+                    uint32_t e4 = e8[hh];
                     const uint32_t bits = (fix >> (8 * q + 4 * hh)) & 0xF;
                     if (bits) {
 #pragma unroll
@@ -569,8 +563,8 @@ __global__ void __launch_bounds__(kThreads, UZIP_SDEC_MIN_BLOCKS) decode_sentine
         for (int r = 0; r < kGroupsPerThread; r++) {
             const uint32_t g = tid + r * kThreads;
             if (g >= tgroups) continue;
-            uint32_t e_lo = lookup4(cv[r] & 0xFFFF, d0, d1, d2, d3);
-            uint32_t e_hi = lookup4(cv[r] >> 16, d0, d1, d2, d3);
+            uint32_t e_lo, e_hi;
+            lookup8(cv[r], d0, d1, d2, d3, e_lo, e_hi);
             uint32_t bits = sb[r];
             if (bits) {
                 const uint32_t own = r == 0 ? (own01 & 0xFFFF) : r == 1 ? (own01 >> 16) + row1

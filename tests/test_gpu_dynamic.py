@@ -66,3 +66,37 @@ def test_dynamic_full_kv(uz, orc):
     check_dynamic(uz, orc, x, 1024)
     del x
     torch.cuda.empty_cache()
+
+
+LARGE = [(1 << 22) - 1, 1 << 22, (1 << 22) + 13, 3 * (1 << 22) + 7, 20_000_005]
+
+
+@pytest.mark.parametrize("law", ["gaussian", "one exponent", "random bits"])
+def test_histogram_of_large_inputs(uz, orc, law):
+    """Inputs of 4 Mi values and more are counted by the private-column
+    histogram (one CTA per SM, 16-bit counters per thread): histogram and
+    codebook equal the oracle's, at and around the size where it takes over,
+    with ragged tails and inputs spanning several rounds of loads."""
+    rng = np.random.default_rng(len(law))
+    for n in LARGE:
+        if law == "gaussian":
+            xh = (rng.standard_normal(n).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        elif law == "one exponent":  # every pair of counts hits one counter
+            xh = np.full(n, 0x3F85, np.uint16)
+            xh[::1001] = 0x4005
+        else:
+            xh = rng.integers(0, 65536, n, dtype=np.uint16)
+        x = torch.from_numpy(xh.view(np.int16)).cuda().view(torch.bfloat16)
+        cb = uz.calibrate(x)
+        assert uz.codebook_histogram(cb) == [int(v) for v in orc.histogram(xh)], n
+        assert uz.codebook_exps(cb) == orc.calibrate(xh).tolist(), n
+
+
+def test_e5m2_histogram_of_large_inputs(uz, orc):
+    rng = np.random.default_rng(9)
+    for n in LARGE:
+        xh = rng.integers(0, 256, n, dtype=np.uint8)
+        xh[: n // 3] = 0x3C  # a dominant exponent
+        cb = uz.e5m2_calibrate(torch.from_numpy(xh).cuda())
+        assert uz.codebook_histogram(cb) == [int(v) for v in orc.e5m2_histogram(xh)], n
+        assert uz.codebook_exps(cb) == orc.e5m2_calibrate(xh).tolist(), n
