@@ -117,30 +117,28 @@ __global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const void* __r
 
 // Histogram of a large input (a whole tensor): the warp-merged shared
 // histogram above spends most of its time in __match_any_sync, so for large
-// inputs each thread counts into a private column of 16-bit counters instead
-// (256 bins x kPrivThreads columns, 192 KB of shared memory, one CTA per SM).
-// A column's word bank depends only on the thread, so no two lanes of a warp
-// meet in a bank whatever exponents they hold. Values are counted in pairs:
-// both counters are read, the second corrected when the exponents are equal,
-// and both written back in order. Every 65,408 values per thread (before a
-// 16-bit counter can overflow) the block folds the columns into per-bin
-// totals and clears them. The next round's 16 loads per thread are issued
-// before the current round is counted. The last block ranks, as above.
+// inputs each thread counts into private 16-bit counters instead: thread t
+// owns word (e >> 1) * kPrivThreads + t for bins e and e ^ 1 (low and high
+// half), 192 KB of shared memory for 384 threads, one CTA per SM. Every
+// access of a lane falls in bank t mod 32, so no two lanes of a warp meet in
+// a bank whatever exponents they hold, and no two threads share a word. A
+// value adds 1 to its half with a shared-memory atomic whose result is not
+// used, so counting is never a read-modify-write chain through the shared
+// memory's latency. Every 65,408 values per thread (before a half can carry
+// into the other) the block folds the counters into per-bin totals and
+// clears them. The next round's 16 loads per thread are issued before the
+// current round is counted. The last block ranks, as above.
 constexpr int kPrivThreads = 384;
 constexpr int kPrivLoads = 16;
 constexpr uint32_t kEpochValues = 65408;  // per thread between folds, + one tail value < 65536
-constexpr size_t kPrivSmem = (size_t)256 * kPrivThreads * sizeof(uint16_t);
+constexpr size_t kPrivSmem = (size_t)128 * kPrivThreads * sizeof(uint32_t);
 #ifndef UZIP_HIST_PRIVATE_FROM
 #define UZIP_HIST_PRIVATE_FROM (1u << 22)
 #endif
 constexpr uint64_t kPrivateFrom = UZIP_HIST_PRIVATE_FROM;  // inputs at least this long use it
 
-__device__ __forceinline__ void count_pair(uint16_t* col, uint32_t e0, uint32_t e1) {
-    const uint32_t a0 = e0 * kPrivThreads, a1 = e1 * kPrivThreads;
-    const uint32_t c0 = col[a0];
-    const uint32_t c1 = col[a1] + (e0 == e1 ? 1u : 0u);
-    col[a0] = (uint16_t)(c0 + 1);
-    col[a1] = (uint16_t)(c1 + 1);
+__device__ __forceinline__ void count_one(uint32_t* col, uint32_t e) {
+    atomicAdd(col + (e >> 1) * kPrivThreads, 1u << (16 * (e & 1)));
 }
 
 template <int kFmt>
@@ -154,12 +152,12 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
     constexpr uint32_t kRoundsPerEpoch = kEpochValues / (kPrivLoads * kPerVec);
 #endif
     extern __shared__ uint4 s_dyn[];
-    uint16_t* cnt = reinterpret_cast<uint16_t*>(s_dyn);  // [bin][thread]
+    const uint32_t* cnt = reinterpret_cast<const uint32_t*>(s_dyn);  // [bin pair][thread]
     __shared__ bool s_last;
     unsigned long long* hist = reinterpret_cast<unsigned long long*>(cb + UZIP_CB_HIST);
     unsigned int* counter = reinterpret_cast<unsigned int*>(cb + kCbCounter);
     const int tid = threadIdx.x;
-    uint16_t* col = cnt + tid;
+    uint32_t* col = reinterpret_cast<uint32_t*>(s_dyn) + tid;
     const uint8_t* x8 = static_cast<const uint8_t*>(xv);
 
     auto clear = [&]() {
@@ -170,22 +168,24 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             if (kFmt == kE5M2) {
-                count_pair(col, (w[q] >> 2) & 0x1F, (w[q] >> 10) & 0x1F);
-                count_pair(col, (w[q] >> 18) & 0x1F, (w[q] >> 26) & 0x1F);
+#pragma unroll
+                for (int b = 0; b < 4; b++) count_one(col, (w[q] >> (8 * b + 2)) & 0x1F);
             } else {
-                count_pair(col, (w[q] >> 7) & 0xFF, (w[q] >> 23) & 0xFF);
+                count_one(col, (w[q] >> 7) & 0xFF);
+                count_one(col, (w[q] >> 23) & 0xFF);
             }
         }
     };
     uint32_t total = 0;  // thread t < 256: bin t's block total
     auto fold = [&]() {
         __syncthreads();
-        if (tid < 256) {
-            const uint4* row = reinterpret_cast<const uint4*>(cnt + tid * kPrivThreads);
-            for (int k = 0; k < kPrivThreads / 8; k++) {
-                const uint4 r = row[k];
-                total += (r.x & 0xFFFF) + (r.x >> 16) + (r.y & 0xFFFF) + (r.y >> 16) + (r.z & 0xFFFF) + (r.z >> 16) +
-                         (r.w & 0xFFFF) + (r.w >> 16);
+        if (tid < 256) {  // bin tid: half tid & 1 of row tid >> 1, read from a rotated start (no bank meets twice)
+            const uint32_t* row = cnt + (tid >> 1) * kPrivThreads;
+            const uint32_t sh = 16 * (tid & 1);
+            uint32_t j = tid % kPrivThreads;
+            for (int k = 0; k < kPrivThreads; k++) {
+                total += (row[j] >> sh) & 0xFFFF;
+                j = j + 1 == kPrivThreads ? 0 : j + 1;
             }
         }
         __syncthreads();
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
     if (blockIdx.x == 0 && (uint64_t)tid < n - groups * kPerVec) {  // ragged tail: one value per thread
         const uint64_t i = groups * kPerVec + tid;
         const uint32_t e = kFmt == kE5M2 ? (x8[i] >> 2) & 0x1F : (static_cast<const uint16_t*>(xv)[i] >> 7) & 0xFF;
-        col[e * kPrivThreads] += 1;
+        count_one(col, e);
     }
     const uint64_t per_round = (uint64_t)gridDim.x * kPrivThreads * kPrivLoads;
     const uint64_t rounds = (groups + per_round - 1) / per_round;
