@@ -224,14 +224,21 @@ __device__ __forceinline__ uint32_t spread_fields4(uint32_t f12) {
     return ((lo & 7) | ((lo & 0x38) << 5)) | (((hi & 7) | ((hi & 0x38) << 5)) << 16);
 }
 
-// Decoder for FP8 E5M2 streams (page §4.2 / appendix C): tiles of 8192
-// values as in decode_kernel, each thread taking 32 consecutive values (12
-// bytes of packed sign-mantissa fields, 16 bytes of codes, 32 bytes out);
-// the escape fix-up goes through shared memory as for BF16.
+// Decoder for FP8 E5M2 streams (page §4.2 / appendix C): tiles of
+// 256 * 32 * kE5Slots values, each thread taking kE5Slots slots of 32
+// consecutive values (slot s = tid + 256 j: 12 bytes of packed sign-mantissa
+// fields and 16 bytes of codes in, 32 bytes out), so a thread has
+// 28 * kE5Slots bytes of loads in flight per tile; the escape fix-up goes
+// through shared memory as for BF16.
+#ifndef UZIP_E5_SLOTS
+#define UZIP_E5_SLOTS 2
+#endif
+constexpr int kE5Slots = UZIP_E5_SLOTS;
+constexpr uint32_t kE5Tile = kThreads * 32 * kE5Slots;
+
 __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_kernel(const Params p) {
-    static_assert(kTile == kThreads * 32, "one 32-value slot per thread");
-    __shared__ uint32_t s_mask[2][kTile / 32];
-    __shared__ uint8_t s_val[kTile];
+    __shared__ uint32_t s_mask[2][kE5Tile / 32];
+    __shared__ uint8_t s_val[kE5Tile];
     __shared__ int s_bad;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -260,30 +267,34 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
     const uint8_t* D = p.s + L.off_d;
     uint8_t* out8 = reinterpret_cast<uint8_t*>(p.out);
     const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;
-    const uint32_t tiles = (n32 + kTile - 1) / kTile;
+    const uint32_t tiles = (n32 + kE5Tile - 1) / kE5Tile;
 
-    for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[0][i] = 0;
+    for (uint32_t i = tid; i < kE5Tile / 32; i += kThreads) s_mask[0][i] = 0;
     if (tid == 0) s_bad = 0;
     __syncthreads();
 
     int par = 0;
     for (uint32_t t = blockIdx.x; t < tiles; t += gridDim.x, par ^= 1) {
-        const uint32_t e0 = t * kTile;
-        const uint32_t tlen = min(kTile, n32 - e0);
-        const uint32_t v0 = 32 * tid;  // this thread's values e0 + v0 .. + 31
-        const bool mine = v0 < tlen;
-        // 1. dense loads (the padded sections keep a whole slot inside the stream)
-        uint32_t f[3] = {0, 0, 0};
-        uint4 cv = make_uint4(0, 0, 0, 0);
-        if (mine) {
-            const uint32_t* fa = reinterpret_cast<const uint32_t*>(A + (e0 / 8) * 3 + 12 * tid);
-            f[0] = __ldg(fa);
-            f[1] = __ldg(fa + 1);
-            f[2] = __ldg(fa + 2);
-            cv = __ldg(reinterpret_cast<const uint4*>(B + e0 / 2 + 16 * tid));
+        const uint32_t e0 = t * kE5Tile;
+        const uint32_t tlen = min(kE5Tile, n32 - e0);
+        // 1. dense loads of every slot (the padded sections keep a whole slot inside the stream)
+        uint32_t f[kE5Slots][3];
+        uint4 cv[kE5Slots];
+#pragma unroll
+        for (int j = 0; j < kE5Slots; j++) {
+            const uint32_t sl = tid + j * kThreads, v0 = 32 * sl;
+            f[j][0] = f[j][1] = f[j][2] = 0;
+            cv[j] = make_uint4(0, 0, 0, 0);
+            if (v0 < tlen) {
+                const uint32_t* fa = reinterpret_cast<const uint32_t*>(A + (e0 / 8) * 3 + 12 * sl);
+                f[j][0] = __ldg(fa);
+                f[j][1] = __ldg(fa + 1);
+                f[j][2] = __ldg(fa + 2);
+                cv[j] = ld_stream_v4(B + e0 / 2 + 16 * sl);
+            }
         }
         // 2. escapes of the chunks overlapping the tile -> shared memory
-        for (uint32_t i = tid; i < kTile / 32; i += kThreads) s_mask[par ^ 1][i] = 0;
+        for (uint32_t i = tid; i < kE5Tile / 32; i += kThreads) s_mask[par ^ 1][i] = 0;
         const uint32_t c_first = e0 / chunk, c_last = (e0 + tlen - 1) / chunk;
         bool bad = false;
         for (uint32_t c = c_first + warp; c <= c_last; c += kThreads / 32) {
@@ -297,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
             }
             const uint32_t k = o1 - o;
             const uint8_t* blk = D + 3ull * o;
-            for (uint32_t j = lane; j < k; j += 32) {
-                const uint32_t pos = (uint32_t)blk[2 * j] | ((uint32_t)blk[2 * j + 1] << 8);
+            for (uint32_t jj = lane; jj < k; jj += 32) {
+                const uint32_t pos = (uint32_t)blk[2 * jj] | ((uint32_t)blk[2 * jj + 1] << 8);
                 if (pos >= clen) {
                     bad = true;
                     continue;
@@ -306,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
                 const uint32_t el = cbase + pos;
                 if (el >= e0 && el < e0 + tlen) {
                     const uint32_t li = el - e0;
-                    s_val[li] = blk[2 * k + j];
+                    s_val[li] = blk[2 * k + jj];
                     atomicOr(&s_mask[par][li >> 5], 1u << (li & 31));
                 }
             }
@@ -314,12 +325,15 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
         if (bad) s_bad = 1;
         __syncthreads();
 
-        // 3. decode the slot's 32 values, patch, store
-        if (mine) {
-            const uint32_t fix = s_mask[par][tid];
-            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
-            const uint32_t g24[4] = {f[0] & 0xFFFFFF, ((f[0] >> 24) | (f[1] << 8)) & 0xFFFFFF,
-                                     ((f[1] >> 16) | (f[2] << 16)) & 0xFFFFFF, f[2] >> 8};
+        // 3. decode each slot's 32 values, patch, store
+#pragma unroll
+        for (int j = 0; j < kE5Slots; j++) {
+            const uint32_t sl = tid + j * kThreads, v0 = 32 * sl;
+            if (v0 >= tlen) continue;
+            const uint32_t fix = s_mask[par][sl];
+            const uint32_t cw[4] = {cv[j].x, cv[j].y, cv[j].z, cv[j].w};
+            const uint32_t g24[4] = {f[j][0] & 0xFFFFFF, ((f[j][0] >> 24) | (f[j][1] << 8)) & 0xFFFFFF,
+                                     ((f[j][1] >> 16) | (f[j][2] << 16)) & 0xFFFFFF, f[j][2] >> 8};
             uint32_t o[8];
 #pragma unroll
             for (int q = 0; q < 4; q++) {
@@ -611,7 +625,7 @@ using namespace uzip;
 namespace {
 
 int decode_launch(void (*kernel)(Params), const void* d_stream, size_t stream_bytes, void* d_out, size_t n,
-                  uint32_t* d_status, uzip_stream_t stream) {
+                  uint32_t* d_status, uzip_stream_t stream, uint32_t tile = kTile) {
     if (!d_stream || (n > 0 && !d_out) || n > UZIP_MAX_N) return UZIP_ERR_ARG;
     if (!aligned16(d_stream) || (n > 0 && !aligned16(d_out)) ||
         (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3)))
@@ -630,7 +644,7 @@ int decode_launch(void (*kernel)(Params), const void* d_stream, size_t stream_by
     UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0));
     if (per_sm < 1) return UZIP_ERR_CUDA;
-    const uint64_t tiles = (n + kTile - 1) / kTile;
+    const uint64_t tiles = (n + tile - 1) / tile;
     const uint64_t grid = std::max<uint64_t>(1, std::min<uint64_t>(tiles, (uint64_t)sms * per_sm));
     kernel<<<(unsigned)grid, kThreads, 0, s>>>(p);
     UZIP_CUDA_TRY(cudaGetLastError());
@@ -651,5 +665,5 @@ extern "C" UZIP_API int uzip_sentinel_decode(const void* d_stream, size_t stream
 
 extern "C" UZIP_API int uzip_e5m2_decode(const void* d_stream, size_t stream_bytes, void* d_out_e5m2, size_t n,
                                          uint32_t* d_status, uzip_stream_t stream) {
-    return decode_launch(decode_e5m2_kernel, d_stream, stream_bytes, d_out_e5m2, n, d_status, stream);
+    return decode_launch(decode_e5m2_kernel, d_stream, stream_bytes, d_out_e5m2, n, d_status, stream, kE5Tile);
 }

@@ -380,11 +380,12 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
         const bool full = ulen == kUnit;
         uint32_t cnt = 0;
         uint32_t mwords[2] = {0, 0};
+        // both rows' loads first: a lane has 64 bytes in flight per unit
+        uint32_t wall[2][8];
 #pragma unroll
         for (int it = 0; it < 2; it++) {
-            const uint32_t slot = it * 32 + lane;
-            const uint32_t v0 = 32 * slot;  // this lane's values v0 .. v0 + 31 of the unit
-            uint32_t w[8];
+            const uint32_t v0 = 32 * (it * 32 + lane);
+            uint32_t* w = wall[it];
             if (full || v0 + 32 <= ulen) {
                 const uint4 x0 = ld_stream_v4(src + v0), x1 = ld_stream_v4(src + v0 + 16);
                 w[0] = x0.x, w[1] = x0.y, w[2] = x0.z, w[3] = x0.w;
@@ -396,6 +397,12 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
                 for (uint32_t i = 0; i < 32; i++)
                     if (v0 + i < ulen) w[i / 4] |= (uint32_t)src[v0 + i] << (8 * (i & 3));
             }
+        }
+#pragma unroll
+        for (int it = 0; it < 2; it++) {
+            const uint32_t slot = it * 32 + lane;
+            const uint32_t v0 = 32 * slot;  // this lane's values v0 .. v0 + 31 of the unit
+            const uint32_t* w = wall[it];
             uint32_t codes[4], fields[4], ex[8];
             uint32_t emask = 0;
 #pragma unroll
