@@ -824,15 +824,165 @@ def run_sentinel(args):
     }
 
 
+def _timed_calls(fn, reps, flush, st):
+    """Device time of each of ``reps`` calls of fn, L2 flushed before each
+    (the flush is outside the timed events). Returns the median in ms."""
+    import statistics as stats
+
+    import torch
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in evs:
+        flush.fill_(1)
+        a.record(st)
+        fn()
+        b.record(st)
+    torch.cuda.synchronize()
+    return stats.median(a.elapsed_time(b) for a, b in evs)
+
+
+def run_sweep(args):
+    """Message-size sweep: N(0,1) BF16 buffers of 4 KiB .. 1 GiB (powers of
+    two) with chunks of 256, 1024 and 4096 values, the transfer-sized
+    messages of a KV-cache hand-off. Per call: device time of encode and of
+    decode (median, L2 flushed before every call, so no message is served
+    from L2 by its previous call) and the host time a call takes to enqueue.
+    Every point is checked bit-exact first."""
+    import torch
+
+    import lossless_bf16_exponent_gb300 as uz
+    import lossless_bf16_exponent_gb300.workloads as W
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist("nccl")
+    uz.load()
+    st = torch.cuda.current_stream(dev)
+    cb = uz.calibrate(W.sweep_sample(dev))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # twice the L2
+    rows = []
+    for chunk in W.SWEEP_CHUNKS:
+        for nbytes in W.SWEEP_BYTES:
+            x = W.sweep(nbytes, dev)
+            n = x.numel()
+            out = torch.empty(uz.max_compressed_size(n, chunk), dtype=torch.uint8, device=dev)
+            wsb = torch.empty(uz.workspace_bytes(n, chunk), dtype=torch.uint8, device=dev)
+            y = torch.empty_like(x)
+            _, sb = uz.encode(x, cb, chunk, out=out, workspace=wsb)
+            uz.decode(out, n, out=y, stream_bytes=sb)
+            assert torch.equal(y.view(torch.int16), x.view(torch.int16)), f"{nbytes} B, chunk {chunk}: not bit-exact"
+            reps = 30 if nbytes <= (64 << 20) else 10
+            for _ in range(args.warmup):
+                uz.encode(x, cb, chunk, out=out, workspace=wsb, sync=False)
+                uz.decode(out, n, out=y, stream_bytes=sb)
+            te = _timed_calls(lambda: uz.encode(x, cb, chunk, out=out, workspace=wsb, sync=False), reps, flush, st)
+            td = _timed_calls(lambda: uz.decode(out, n, out=y, stream_bytes=sb), reps, flush, st)
+            host_us = None
+            if nbytes <= (1 << 20):  # enqueue cost per call, back to back, no synchronisation
+                torch.cuda.synchronize()
+                t = time.perf_counter()
+                for _ in range(200):
+                    uz.encode(x, cb, chunk, out=out, workspace=wsb, sync=False)
+                    uz.decode(out, n, out=y, stream_bytes=sb)
+                host_us = round((time.perf_counter() - t) / 200 * 1e6, 2)
+                torch.cuda.synchronize()
+            rows.append({"bytes": nbytes, "chunk": chunk, "ratio": round(nbytes / sb, 5),
+                         "encode_us": round(te * 1e3, 2), "decode_us": round(td * 1e3, 2),
+                         "encode_gbs_raw": round(nbytes / (te * 1e-3) / 1e9, 2),
+                         "decode_gbs_raw": round(nbytes / (td * 1e-3) / 1e9, 2),
+                         "host_us_per_encode_decode": host_us})
+            del x, out, wsb, y
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return None
+    big = next(r for r in rows if r["bytes"] == W.SWEEP_BYTES[-1] and r["chunk"] == CHUNK)
+    small = next(r for r in rows if r["bytes"] == W.SWEEP_BYTES[0] and r["chunk"] == CHUNK)
+    return {"mode": "sweep", "metric": "per-call encode/decode latency (us) and GB/s (raw BF16) vs message size",
+            "value": round(small["encode_us"] + small["decode_us"], 2), "unit": "us", "n_gpus": ws,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
+            "config": {"workload": "N(0,1) BF16, 4 KiB .. 1 GiB x chunk {256, 1024, 4096}",
+                       "value": "encode + decode device time of a 4 KiB message at chunk 1024",
+                       "l2": "flushed (256 MiB write) before every timed call"},
+            "largest": {"bytes": big["bytes"], "encode_gbs_raw": big["encode_gbs_raw"],
+                        "decode_gbs_raw": big["decode_gbs_raw"]},
+            "rows": rows}
+
+
+def run_workloads(args):
+    """The other full-size workloads through the same calibrate -> encode ->
+    decode path: rows of log-uniform scale (8192 x 128), the heavy-tailed
+    escape stress (64 Mi values), the gradient-like buffer (1 Gi values, 10 %
+    zeros, 1 % subnormals; encode then decode in one stream) and the KV cache
+    for comparison. Device time per op (median; inputs of 128 MiB and more
+    exceed L2, the 2 MiB one is flushed from L2 before every call)."""
+    import torch
+
+    import lossless_bf16_exponent_gb300 as uz
+    import lossless_bf16_exponent_gb300.workloads as W
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist("nccl")
+    uz.load()
+    st = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    names = {1: "rows_lognormal_scale 8192x128", 2: "kv_cache 256M", 3: "heavy_tailed 64M (escape stress)",
+             5: "gradient_like 1G"}
+    peak, peak_src = measured_peak()
+    res = {}
+    for k in (1, 2, 3, 5):
+        x, sample = W.workload(k, device=dev)
+        n = x.numel()
+        raw = 2 * n
+        cb = uz.calibrate(sample)
+        out = torch.empty(uz.max_compressed_size(n, CHUNK), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(uz.workspace_bytes(n, CHUNK), dtype=torch.uint8, device=dev)
+        y = torch.empty_like(x)
+        _, sb = uz.encode(x, cb, CHUNK, out=out, workspace=wsb)
+        info = uz.stream_info(out, sb)
+        uz.decode(out, n, out=y, stream_bytes=sb)
+        assert torch.equal(y.view(torch.int16), x.view(torch.int16)), f"workload {k}: not bit-exact"
+        for _ in range(args.warmup):
+            uz.encode(x, cb, CHUNK, out=out, workspace=wsb, sync=False)
+            uz.decode(out, n, out=y, stream_bytes=sb)
+        reps = 20 if k != 5 else 10
+        te = _timed_calls(lambda: uz.encode(x, cb, CHUNK, out=out, workspace=wsb, sync=False), reps, flush, st)
+        td = _timed_calls(lambda: uz.decode(out, n, out=y, stream_bytes=sb), reps, flush, st)
+        m = int(info["escapes"])
+        res[names[k]] = {"n": n, "escape_rate": round(m / n, 6), "ratio": round(raw / sb, 5),
+                         "encode_us": round(te * 1e3, 2), "decode_us": round(td * 1e3, 2),
+                         "encode_gbs_raw": round(raw / (te * 1e-3) / 1e9, 1),
+                         "decode_gbs_raw": round(raw / (td * 1e-3) / 1e9, 1),
+                         "encode_frac": round((raw + sb) / (te * 1e-3) / 1e9 / peak, 4),
+                         "decode_frac": round((raw + sb) / (td * 1e-3) / 1e9 / peak, 4)}
+        del x, sample, out, wsb, y
+        torch.cuda.empty_cache()
+    if rank != 0:
+        return None
+    g = res[names[5]]
+    return {"mode": "workloads", "metric": "encode/decode GB/s (raw BF16 bytes) and ratio per workload",
+            "value": round(2 * g["n"] / ((g["encode_us"] + g["decode_us"]) * 1e-6) / 1e9, 1), "unit": "GB/s",
+            "n_gpus": ws, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+            "data": "synthetic",
+            "config": {"workload": "rows 8192x128, kv_cache 256M, heavy_tailed 64M, gradient_like 1G; chunk 1024",
+                       "value": "gradient_like 1G: raw bytes / (encode + decode time), one stream",
+                       "peak_gbs": peak, "peak_source": peak_src},
+            "workloads": res}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["codec", "dynamic", "pipeline", "chunks", "e5m2", "sentinel"], default="codec",
+    ap.add_argument("--mode", choices=["codec", "dynamic", "pipeline", "chunks", "e5m2", "sentinel", "sweep", "workloads"],
+                    default="codec",
                     help="codec = the benchmark step; dynamic = per-input codebook encode; "
-                         "pipeline = streamed compressed transfer (next rows)")
+                         "pipeline = streamed compressed transfer; chunks / e5m2 / sentinel = the page's "
+                         "variants; sweep = message sizes 4 KiB .. 1 GiB; workloads = the other full-size laws")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--tokens", type=int, default=2048,
@@ -852,6 +1002,10 @@ def main(argv=None):
         line = run_e5m2(args)
     elif args.mode == "sentinel":
         line = run_sentinel(args)
+    elif args.mode == "sweep":
+        line = run_sweep(args)
+    elif args.mode == "workloads":
+        line = run_workloads(args)
     else:
         line = run_ours(args)
     if line is not None:

@@ -6,19 +6,22 @@
 // §3.4: all 16 codes are real exponents; an escape gets a dummy code (0 here).
 //
 // Kernels:
-//   calibrate_kernel  one CTA per SM at most: every thread issues its 16-byte
-//                     loads of the sample first, then counts; one 256-bin
-//                     shared-memory histogram per warp, where equal exponents
-//                     inside a warp are merged with __match_any_sync so a
-//                     concentrated distribution does not serialise on one bin;
-//                     per-block totals are added to the blob's u64 histogram.
-//                     The last block to finish (a fence and a counter, no
-//                     waiting) ranks the 256 bins -- thread j ranks bin j
-//                     against all counts (count descending, exponent
-//                     ascending) -- and the 16 lowest ranks become the
-//                     codebook; then it writes the three tables.
+//   calibrate_kernel  a sample of up to 4 Mi values: blocks of 256 threads,
+//                     each thread issuing its two 16-byte loads first, then
+//                     counting into its warp's 256-bin shared histogram (BF16:
+//                     one shared atomic per value; E5M2, whose values crowd
+//                     onto a few of 32 bins: equal exponents of a warp merged
+//                     with __match_any_sync first); per-block totals are added
+//                     to the blob's u64 histogram. The last block to finish (a
+//                     fence and a counter, no waiting) compacts the bins seen,
+//                     ranks each against the others (count descending, exponent
+//                     ascending; unseen bins follow in exponent order), keeps
+//                     the 16 lowest ranks as the codebook and writes the three
+//                     tables.
+//   histogram_private_kernel  larger inputs (whole tensors), below.
 //   luts_kernel       the same tables from 16 caller-given exponents.
 #include <algorithm>
+#include <atomic>
 
 #include "uzip_internal.cuh"
 
@@ -28,14 +31,22 @@ namespace {
 constexpr int kHistThreads = 256;
 constexpr int kHistWarps = kHistThreads / 32;
 
+// One value into the warp's shared histogram. BF16 (256 bins): a plain
+// shared-memory atomic per value (measured faster than merging equal
+// exponents first). E5M2 (32 bins, values crowd onto a few of them): lanes
+// holding the same exponent add once, with their count.
+template <int kFmt>
 __device__ __forceinline__ void warp_hist_add(uint32_t* h, uint32_t e, bool valid) {
-    // Lanes holding the same exponent add once, with their count.
+    if (kFmt != kE5M2) {
+        if (valid) atomicAdd(&h[e], 1u);
+        return;
+    }
     const uint32_t key = valid ? e : (0x100u | (threadIdx.x & 31));
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
     if (valid && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&h[e], __popc(peers));
 }
 
-constexpr int kLoadsPerThread = 4;  // 16-byte loads in flight per thread
+constexpr int kLoadsPerThread = 2;  // 16-byte loads in flight per thread
 
 // Block-done counter of calibrate_kernel, in the blob's reserved bytes after
 // the histogram; cleared with the histogram before each launch.
@@ -79,10 +90,10 @@ __global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const void* __r
             for (int q = 0; q < 4; q++) {
                 if (kFmt == kE5M2) {
 #pragma unroll
-                    for (int b = 0; b < 4; b++) warp_hist_add(h, (w[q] >> (8 * b + 2)) & 0x1F, valid[j]);
+                    for (int b = 0; b < 4; b++) warp_hist_add<kFmt>(h, (w[q] >> (8 * b + 2)) & 0x1F, valid[j]);
                 } else {
-                    warp_hist_add(h, (w[q] >> 7) & 0xFF, valid[j]);
-                    warp_hist_add(h, (w[q] >> 23) & 0xFF, valid[j]);
+                    warp_hist_add<kFmt>(h, (w[q] >> 7) & 0xFF, valid[j]);
+                    warp_hist_add<kFmt>(h, (w[q] >> 23) & 0xFF, valid[j]);
                 }
             }
         }
@@ -95,7 +106,7 @@ __global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const void* __r
         if (valid)
             e = kFmt == kE5M2 ? (static_cast<const uint8_t*>(xv)[i] >> 2) & 0x1F
                               : (static_cast<const uint16_t*>(xv)[i] >> 7) & 0xFF;
-        warp_hist_add(h, e, valid);
+        warp_hist_add<kFmt>(h, e, valid);
     }
     __syncthreads();
     for (int b = threadIdx.x; b < 256; b += kHistThreads) {
@@ -266,21 +277,39 @@ __device__ void write_tables(const uint8_t* exps, uint8_t* cb, uint64_t n_sample
 }
 
 // Rank the blob's 256 totals (count descending, exponent ascending) and write
-// the codebook; the first 256 threads of the CTA, totals read from L2.
+// the codebook; the first 256 threads of the CTA, totals read from L2. The
+// bins with a nonzero count are compacted first (in exponent order), so each
+// of them is ranked against the nonzero bins only; a bin never seen ranks
+// after all of them, in exponent order.
 __device__ void rank_and_write(uint8_t* cb, uint64_t n_sample) {
-    __shared__ unsigned long long cnt[256];
+    __shared__ unsigned long long nz_cnt[256];
+    __shared__ uint32_t s_nz[8];
     __shared__ uint8_t exps[16];
     const int t = threadIdx.x;
     const unsigned long long* hist = reinterpret_cast<const unsigned long long*>(cb + UZIP_CB_HIST);
-    if (t < 256) cnt[t] = __ldcg(hist + t);
+    const unsigned long long mine = t < 256 ? __ldcg(hist + t) : 0ull;
+    const uint32_t lane = t & 31, warp = t >> 5;
+    const uint32_t nzb = __ballot_sync(0xffffffffu, mine != 0);
+    if (t < 256 && lane == 0) s_nz[warp] = __popc(nzb);
+    __syncthreads();
+    uint32_t pos = __popc(nzb & ((1u << lane) - 1)), nnz = 0;
+#pragma unroll
+    for (int w = 0; w < 8; w++) {
+        pos += w < (int)warp ? s_nz[w] : 0u;
+        nnz += s_nz[w];
+    }
+    if (t < 256 && mine) nz_cnt[pos] = mine;
     __syncthreads();
     if (t < 256) {
-        const unsigned long long mine = cnt[t];
-        int rank = 0;
-#pragma unroll 8
-        for (int i = 0; i < 256; i++) {
-            const unsigned long long c = cnt[i];
-            rank += (c > mine) || (c == mine && i < t);
+        uint32_t rank;
+        if (mine) {
+            rank = 0;
+            for (uint32_t k = 0; k < nnz; k++) {
+                const unsigned long long c = nz_cnt[k];
+                rank += (c > mine) || (c == mine && k < pos);
+            }
+        } else {
+            rank = nnz + ((uint32_t)t - pos);  // unseen: after every seen bin, in exponent order
         }
         if (rank < 16) exps[rank] = (uint8_t)t;
     }
@@ -307,6 +336,15 @@ __global__ void __launch_bounds__(256) luts_kernel(Exps16 in, uint8_t* __restric
 using namespace uzip;
 
 namespace uzip {
+namespace {
+
+// SM count and the histogram kernel's residency (BF16, E5M2) per device,
+// looked up on the first call on that device (0 = not yet).
+constexpr int kMaxCachedDevices = 64;
+std::atomic<int> g_sms[kMaxCachedDevices];
+std::atomic<int> g_per_sm[kMaxCachedDevices][2];
+
+}  // namespace
 
 int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook, cudaStream_t s, uint32_t fmt) {
     if (!d_codebook || (n_sample > 0 && !d_sample_bf16)) return UZIP_ERR_ARG;
@@ -314,9 +352,15 @@ int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
     uint8_t* cb = static_cast<uint8_t*>(d_codebook);
     // Histogram totals and the block counter start at zero.
     UZIP_CUDA_TRY(cudaMemsetAsync(cb + UZIP_CB_HIST, 0, kCbCounter + 16 - UZIP_CB_HIST, s));
-    int dev = 0, sms = 0, per_sm = 0;
+    int dev = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
-    UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    const bool cached = dev < kMaxCachedDevices;
+    const int slot = fmt == kE5M2 ? 1 : 0;
+    int sms = cached ? g_sms[dev].load() : 0, per_sm = cached ? g_per_sm[dev][slot].load() : 0;
+    if (sms < 1) {
+        UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        if (cached) g_sms[dev].store(sms);
+    }
     if (n_sample >= kPrivateFrom) {  // a large input: private-column histogram, one CTA per SM
         auto* pk = fmt == kE5M2 ? histogram_private_kernel<kE5M2> : histogram_private_kernel<kBF16>;
         UZIP_CUDA_TRY(cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrivSmem));
@@ -325,7 +369,10 @@ int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
         return UZIP_OK;
     }
     auto* kernel = fmt == kE5M2 ? calibrate_kernel<kE5M2> : calibrate_kernel<kBF16>;
-    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kHistThreads, 0));
+    if (per_sm < 1) {
+        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kHistThreads, 0));
+        if (cached && per_sm > 0) g_per_sm[dev][slot].store(per_sm);
+    }
     // One block per kHistThreads * kLoadsPerThread 16-byte loads, up to a
     // full resident wave: a small sample is a latency chain, a whole tensor
     // is read at HBM speed.

@@ -21,6 +21,8 @@
 // data that point outside their chunk are skipped and reported.
 #include <algorithm>
 
+#include <atomic>
+
 #include "uzip_internal.cuh"
 
 namespace uzip {
@@ -624,8 +626,14 @@ using namespace uzip;
 
 namespace {
 
-int decode_launch(void (*kernel)(Params), const void* d_stream, size_t stream_bytes, void* d_out, size_t n,
-                  uint32_t* d_status, uzip_stream_t stream, uint32_t tile = kTile) {
+// SM count and each decoder's residency per device, looked up on the first
+// call on that device (0 = not yet).
+constexpr int kMaxCachedDevices = 64;
+std::atomic<int> g_sms[kMaxCachedDevices];
+std::atomic<int> g_per_sm[kMaxCachedDevices][3];
+
+int decode_launch(void (*kernel)(Params), int slot, const void* d_stream, size_t stream_bytes, void* d_out,
+                  size_t n, uint32_t* d_status, uzip_stream_t stream, uint32_t tile = kTile) {
     if (!d_stream || (n > 0 && !d_out) || n > UZIP_MAX_N) return UZIP_ERR_ARG;
     if (!aligned16(d_stream) || (n > 0 && !aligned16(d_out)) ||
         (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3)))
@@ -639,11 +647,19 @@ int decode_launch(void (*kernel)(Params), const void* d_stream, size_t stream_by
     p.out = static_cast<uint16_t*>(d_out);
     p.n = n;
     p.status = d_status;
-    int dev = 0, sms = 0, per_sm = 0;
+    int dev = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
-    UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0));
-    if (per_sm < 1) return UZIP_ERR_CUDA;
+    const bool cached = dev < kMaxCachedDevices;
+    int sms = cached ? g_sms[dev].load() : 0, per_sm = cached ? g_per_sm[dev][slot].load() : 0;
+    if (sms < 1) {
+        UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+        if (cached) g_sms[dev].store(sms);
+    }
+    if (per_sm < 1) {
+        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kThreads, 0));
+        if (per_sm < 1) return UZIP_ERR_CUDA;
+        if (cached) g_per_sm[dev][slot].store(per_sm);
+    }
     const uint64_t tiles = (n + tile - 1) / tile;
     const uint64_t grid = std::max<uint64_t>(1, std::min<uint64_t>(tiles, (uint64_t)sms * per_sm));
     kernel<<<(unsigned)grid, kThreads, 0, s>>>(p);
@@ -655,15 +671,15 @@ int decode_launch(void (*kernel)(Params), const void* d_stream, size_t stream_by
 
 extern "C" UZIP_API int uzip_decode(const void* d_stream, size_t stream_bytes, void* d_out_bf16, size_t n,
                                     uint32_t* d_status, uzip_stream_t stream) {
-    return decode_launch(decode_kernel, d_stream, stream_bytes, d_out_bf16, n, d_status, stream);
+    return decode_launch(decode_kernel, 0, d_stream, stream_bytes, d_out_bf16, n, d_status, stream);
 }
 
 extern "C" UZIP_API int uzip_sentinel_decode(const void* d_stream, size_t stream_bytes, void* d_out_bf16, size_t n,
                                              uint32_t* d_status, uzip_stream_t stream) {
-    return decode_launch(decode_sentinel_kernel, d_stream, stream_bytes, d_out_bf16, n, d_status, stream);
+    return decode_launch(decode_sentinel_kernel, 1, d_stream, stream_bytes, d_out_bf16, n, d_status, stream);
 }
 
 extern "C" UZIP_API int uzip_e5m2_decode(const void* d_stream, size_t stream_bytes, void* d_out_e5m2, size_t n,
                                          uint32_t* d_status, uzip_stream_t stream) {
-    return decode_launch(decode_e5m2_kernel, d_stream, stream_bytes, d_out_e5m2, n, d_status, stream, kE5Tile);
+    return decode_launch(decode_e5m2_kernel, 2, d_stream, stream_bytes, d_out_e5m2, n, d_status, stream, kE5Tile);
 }

@@ -958,11 +958,14 @@ namespace {
 // Per-device launch facts, looked up on the first call on each device (the
 // results are the same whichever thread gets there first).
 struct DeviceFacts {
-    int sms, per_sm1, per_sm1e;
+    int dev, sms, per_sm1, per_sm1e;
 };
 constexpr int kMaxFactDevices = 64;
 std::atomic<int> g_facts_ready[kMaxFactDevices];
 DeviceFacts g_facts[kMaxFactDevices];
+// Escape-kernel residency per device, variant (one or two rounds) and
+// largest chunk table (0 = not looked up yet).
+std::atomic<int> g_escape_per_sm[kMaxFactDevices][2][kMaxRangeChunks + 1];
 
 size_t escape_smem(uint32_t range_chunks, int rounds) {
     return (size_t)kWarps * (kStageBytes + 4ull * rounds * kHeadEntries * 32 + 4ull * (range_chunks + 1));
@@ -975,6 +978,7 @@ int device_facts(DeviceFacts& f) {
         f = g_facts[dev];
         return UZIP_OK;
     }
+    f.dev = dev;
     UZIP_CUDA_TRY(cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev));
     UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm1, encode_dense_kernel, kThreads, 0));
     UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm1e, encode_dense_e5m2_kernel, kThreads, 0));
@@ -1045,17 +1049,23 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         const uint32_t rc_max =
             std::max<uint32_t>(1, std::min<uint32_t>(kMaxRangeChunks, kMaxRangeUnits * kUnit / chunk));
         // Residency at the largest chunk table this chunk size can need.
-        int per_sm2 = 0;
-        UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &per_sm2, two_rounds ? encode_escape_kernel<2> : encode_escape_kernel<1>, kThreads,
-            escape_smem(rc_max, two_rounds + 1)));
+        int per_sm2 = f.dev < kMaxFactDevices ? g_escape_per_sm[f.dev][two_rounds][rc_max].load() : 0;
+        if (per_sm2 < 1) {
+            UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &per_sm2, two_rounds ? encode_escape_kernel<2> : encode_escape_kernel<1>, kThreads,
+                escape_smem(rc_max, two_rounds + 1)));
+            if (per_sm2 > 0 && f.dev < kMaxFactDevices) g_escape_per_sm[f.dev][two_rounds][rc_max].store(per_sm2);
+        }
         if (per_sm2 < 1) return UZIP_ERR_CUDA;
         const uint64_t warps2 = (uint64_t)f.sms * per_sm2 * kWarps;
         p.range_chunks = (uint32_t)std::min<uint64_t>(rc_max, std::max<uint64_t>(1, (L.nc + warps2 - 1) / warps2));
         p.ranges = (L.nc + p.range_chunks - 1) / p.range_chunks;
         const uint64_t grid2 = std::min<uint64_t>((p.ranges + kWarps - 1) / kWarps, (uint64_t)f.sms * per_sm2);
 
-        UZIP_CUDA_TRY(cudaMemsetAsync(p.segs, 0, 4ull * g.nseg, s));  // segment totals
+        // Segment totals start at zero; the last segment's is never read (no
+        // escape lies after it), so a single-segment input (up to 64 units)
+        // needs no clearing.
+        if (g.nseg > 1) UZIP_CUDA_TRY(cudaMemsetAsync(p.segs, 0, 4ull * (g.nseg - 1), s));
         if (fmt == kE5M2)
             encode_dense_e5m2_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
         else

@@ -81,7 +81,7 @@ def test_sweep_small(uz, orc, chunk):
 
 # ----------------------------------------------------------------- edge sizes
 
-EDGE_CHUNKS = [8, 24, 256, 1000, 1024, 4096, 8192, 8200, 16384, 63496, 64008, 65528, 65536]
+EDGE_CHUNKS = [8, 24, 256, 512, 1000, 1024, 2048, 4096, 8192, 8200, 16384, 32768, 63496, 64008, 65528, 65536]
 
 
 @pytest.mark.parametrize("chunk", EDGE_CHUNKS)
@@ -116,7 +116,7 @@ def test_empty_input(uz, orc):
         assert int(status.item()) == 0
 
 
-@pytest.mark.parametrize("chunk", [8, 1024, 65536])
+@pytest.mark.parametrize("chunk", [8, 256, 512, 1024, 2048, 4096, 65536])
 def test_degenerate_inputs(uz, orc, chunk):
     n = 3 * 65536 + 11
     cases = {
