@@ -24,7 +24,9 @@
 //                  unit with more escapes stores its escape-mask bytes instead.
 //                  It stores the unit's escape count and adds it to its
 //                  segment's total (64 or more units per segment; the totals
-//                  are cleared before the launch).
+//                  are zeroed by a one-block kernel launched just before,
+//                  behind which the dense kernel launches at once and which
+//                  it waits for only before its first total update).
 //   escape kernel  launched as a programmatic dependent of the dense kernel (its
 //                  launch overlaps the dense tail; it waits for the dense
 //                  results before touching them). Each warp takes a range of
@@ -217,6 +219,13 @@ __device__ __forceinline__ uint32_t div_chunk(const Params& p, uint32_t x) {
     return p.chunk_shift < 32 ? x >> p.chunk_shift : x / p.chunk;
 }
 
+// Zero the segment totals. Its dependent (the dense kernel) may start at
+// once: it waits for this grid only before its first total update.
+__global__ void __launch_bounds__(256) clear_segments_kernel(uint32_t* segs, uint32_t words) {
+    allow_dependent_launch();
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < words; i += gridDim.x * blockDim.x) segs[i] = 0;
+}
+
 // ------------------------------------------------------------ dense kernel
 
 __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_kernel(const Params p) {
@@ -229,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t stride = (uint64_t)gridDim.x * kWarps;
     const uint64_t keep = l2_policy_evict_last();  // counts, lists, masks: read by the escape kernel
+    bool cleared = false;
     for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride) {
         const uint64_t ubase = u * kUnit;
         const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
@@ -315,9 +325,18 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
         }
         if (lane == 0) {
             st_u32_keep(p.counts + u, cnt, keep);
-            if (cnt) atomicAdd(&p.segs[u / p.seg_units], cnt);
+            if (cnt) {
+                if (!cleared) {  // the segment totals are zeroed by the launch before this one
+                    wait_for_prerequisite();
+                    cleared = true;
+                }
+                atomicAdd(&p.segs[u / p.seg_units], cnt);
+            }
         }
     }
+    // The grid completes only after the clearing launch has (the escape
+    // pass, which waits for this grid, reads the totals).
+    if (threadIdx.x == 0) wait_for_prerequisite();
 }
 
 // ------------------------------------------------------- FP8 E5M2 dense kernel
@@ -370,6 +389,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t stride = (uint64_t)gridDim.x * kWarps;
     const uint64_t keep = l2_policy_evict_last();
+    bool cleared = false;
     for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride) {
         const uint64_t ubase = u * kUnit;
         const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
@@ -470,9 +490,18 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
         }
         if (lane == 0) {
             st_u32_keep(p.counts + u, cnt, keep);
-            if (cnt) atomicAdd(&p.segs[u / p.seg_units], cnt);
+            if (cnt) {
+                if (!cleared) {  // the segment totals are zeroed by the launch before this one
+                    wait_for_prerequisite();
+                    cleared = true;
+                }
+                atomicAdd(&p.segs[u / p.seg_units], cnt);
+            }
         }
     }
+    // The grid completes only after the clearing launch has (the escape
+    // pass, which waits for this grid, reads the totals).
+    if (threadIdx.x == 0) wait_for_prerequisite();
 }
 
 // ----------------------------------------------------------- escape kernel
@@ -1064,13 +1093,22 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
 
         // Segment totals start at zero; the last segment's is never read (no
         // escape lies after it), so a single-segment input (up to 64 units)
-        // needs no clearing.
-        if (g.nseg > 1) UZIP_CUDA_TRY(cudaMemsetAsync(p.segs, 0, 4ull * (g.nseg - 1), s));
-        if (fmt == kE5M2)
-            encode_dense_e5m2_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
-        else
-            encode_dense_kernel<<<(unsigned)grid1, kThreads, 0, s>>>(p);
-        UZIP_CUDA_TRY(cudaGetLastError());
+        // needs no clearing. The clearing kernel lets the dense kernel
+        // launch behind it at once (programmatic dependent launch).
+        cudaLaunchAttribute pdl[1];
+        pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pdl[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg1 = {};
+        cfg1.gridDim = dim3((unsigned)grid1);
+        cfg1.blockDim = dim3(kThreads);
+        cfg1.stream = s;
+        if (g.nseg > 1) {
+            clear_segments_kernel<<<1, 256, 0, s>>>(p.segs, g.nseg - 1);
+            UZIP_CUDA_TRY(cudaGetLastError());
+            cfg1.attrs = pdl;
+            cfg1.numAttrs = 1;
+        }
+        UZIP_CUDA_TRY(cudaLaunchKernelEx(&cfg1, fmt == kE5M2 ? encode_dense_e5m2_kernel : encode_dense_kernel, p));
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)grid2);
         cfg.blockDim = dim3(kThreads);
