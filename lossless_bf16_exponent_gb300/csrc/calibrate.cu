@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const void* __r
         warp_hist_add<kFmt>(h, e, valid);
     }
     __syncthreads();
+    pdl_wait();  // the blob's totals and counter are zeroed by the launch before this one
     for (int b = threadIdx.x; b < 256; b += kHistThreads) {
         uint32_t s = 0;
 #pragma unroll
@@ -240,6 +241,7 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
         }
     }
     fold();
+    pdl_wait();  // the blob's totals and counter are zeroed by the launch before this one
     if (tid < 256 && total) atomicAdd(&hist[tid], (unsigned long long)total);
     // The last block ranks the totals.
     __threadfence();
@@ -250,6 +252,16 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
     __threadfence();
     rank_and_write(cb, n);
     if (tid == 0) *counter = 0;
+}
+
+// Zero the blob's histogram totals and block counter. Its dependent (the
+// histogram kernel) may launch at once: it waits for this grid only before
+// its first update of the totals.
+__global__ void __launch_bounds__(256) clear_hist_kernel(uint8_t* __restrict__ cb) {
+    pdl_launch_dependents();
+    uint4* z = reinterpret_cast<uint4*>(cb + UZIP_CB_HIST);
+    for (uint32_t i = threadIdx.x; i < (kCbCounter + 16 - UZIP_CB_HIST) / 16; i += blockDim.x)
+        z[i] = make_uint4(0, 0, 0, 0);
 }
 
 // Tables from exps[16] (shared memory), written by a 256-thread CTA.
@@ -350,8 +362,17 @@ int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
     if (!d_codebook || (n_sample > 0 && !d_sample_bf16)) return UZIP_ERR_ARG;
     if (!aligned16(d_codebook) || (n_sample > 0 && !aligned16(d_sample_bf16))) return UZIP_ERR_ALIGN;
     uint8_t* cb = static_cast<uint8_t*>(d_codebook);
-    // Histogram totals and the block counter start at zero.
-    UZIP_CUDA_TRY(cudaMemsetAsync(cb + UZIP_CB_HIST, 0, kCbCounter + 16 - UZIP_CB_HIST, s));
+    // Histogram totals and the block counter start at zero: a one-block
+    // kernel clears them and the histogram kernel launches behind it at once.
+    clear_hist_kernel<<<1, 256, 0, s>>>(cb);
+    UZIP_CUDA_TRY(cudaGetLastError());
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
     int dev = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
     const bool cached = dev < kMaxCachedDevices;
@@ -364,8 +385,10 @@ int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
     if (n_sample >= kPrivateFrom) {  // a large input: private-column histogram, one CTA per SM
         auto* pk = fmt == kE5M2 ? histogram_private_kernel<kE5M2> : histogram_private_kernel<kBF16>;
         UZIP_CUDA_TRY(cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrivSmem));
-        pk<<<(unsigned)sms, kPrivThreads, kPrivSmem, s>>>(d_sample_bf16, n_sample, cb);
-        UZIP_CUDA_TRY(cudaGetLastError());
+        cfg.gridDim = dim3((unsigned)sms);
+        cfg.blockDim = dim3(kPrivThreads);
+        cfg.dynamicSmemBytes = kPrivSmem;
+        UZIP_CUDA_TRY(cudaLaunchKernelEx(&cfg, pk, d_sample_bf16, (uint64_t)n_sample, cb));
         return UZIP_OK;
     }
     auto* kernel = fmt == kE5M2 ? calibrate_kernel<kE5M2> : calibrate_kernel<kBF16>;
@@ -380,8 +403,9 @@ int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook,
     uint64_t blocks = (n_sample + per_block - 1) / per_block;
     blocks = std::min<uint64_t>(blocks, (uint64_t)sms * std::max(per_sm, 1));
     if (blocks == 0) blocks = 1;
-    kernel<<<(unsigned)blocks, kHistThreads, 0, s>>>(d_sample_bf16, n_sample, cb);
-    UZIP_CUDA_TRY(cudaGetLastError());
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kHistThreads);
+    UZIP_CUDA_TRY(cudaLaunchKernelEx(&cfg, kernel, d_sample_bf16, (uint64_t)n_sample, cb));
     return UZIP_OK;
 }
 
