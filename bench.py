@@ -36,11 +36,11 @@ METRIC = "encode/decode GB/s (raw BF16 bytes) @256M elems; ratio; % of HBM peak"
 WORKLOAD = "kv_cache [64,2,8,2048,128] bf16 = 268,435,456 values, chunk 1024, calibration sample 1 Mi values"
 CHUNK = 1024
 FALLBACK_HBM_GBS = 6800.0
-# Kernels one step launches: calibrate (one kernel: histogram, then Top-16
-# selection by its last block), encode (dense pass, escape pass), decode (one
-# kernel). The two clears of small device arrays (histogram bins, segment
-# totals) are driver memsets.
-KERNELS_PER_STEP = 4
+# Kernels one step launches: calibrate (a one-block clear of the histogram
+# totals, then the histogram kernel whose last block selects the Top-16),
+# encode (a one-block clear of the segment totals, dense pass, escape pass),
+# decode (one kernel).
+KERNELS_PER_STEP = 6
 
 
 # ------------------------------------------------------------- distributed

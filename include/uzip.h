@@ -139,8 +139,11 @@ UZIP_API size_t uzip_encode_workspace_bytes(size_t n, uint32_t chunk);
 /* Encode n BF16 values (§3.2), reading the input from HBM once: a dense kernel
  * (sign-mantissa bytes, packed codes, per-unit escape lists and counts) and an
  * escape kernel (chunk offsets from the escape-count prefix, escape blocks in
- * ascending element order, header). Each call launches a small memset and the
- * two kernels on `stream`.
+ * ascending element order, header). Each call launches, on `stream`, a
+ * one-block kernel that clears the per-segment escape totals (inputs of more
+ * than 64 units of 2048 values only) and the two kernels; the later launches
+ * start early (programmatic dependent launch) and wait on the device for the
+ * data they need.
  *   d_in_bf16      n BF16 values (may be NULL when n == 0).
  *   chunk          escape-position chunk, a multiple of 8 in [8, 65536].
  *   d_codebook     from uzip_calibrate / uzip_codebook_from_exps.
