@@ -12,22 +12,36 @@ from . import _lib
 from ._lib import CODEBOOK_BYTES, HEADER_BYTES, UzipError, check
 
 
-def _sp(device=None) -> ctypes.c_void_p:
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+# The current stream's raw handle without building a Stream object (a few
+# microseconds per call otherwise); the public API where this is missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
-def _p(t: torch.Tensor | None) -> ctypes.c_void_p:
-    return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
+def _sp(device=None) -> int:
+    """Raw handle of the current CUDA stream of ``device`` (default: current device)."""
+    if _raw_stream is not None:
+        if isinstance(device, torch.device):
+            idx = device.index
+        else:
+            idx = device
+        return _raw_stream(torch.cuda.current_device() if idx is None else idx)
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _p(t: torch.Tensor | None):
+    return t.data_ptr() if t is not None else None
 
 
 def _flat16(x: torch.Tensor) -> torch.Tensor:
+    """Check a tensor of 16-bit values for the C ABI (CUDA, contiguous); the
+    tensor itself is returned (the ABI takes its pointer and element count)."""
     if not x.is_cuda:
         raise ValueError("expected a CUDA tensor")
     if x.element_size() != 2:
         raise ValueError(f"expected 16-bit values, got {x.dtype}")
     if not x.is_contiguous():
         raise ValueError("expected a contiguous tensor")
-    return x.reshape(-1)
+    return x
 
 
 def load():
@@ -161,7 +175,7 @@ def stream_info(stream: torch.Tensor, stream_bytes: int | None = None) -> dict:
 def roundtrip_ok(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024) -> bool:
     s, nb = encode(x, codebook, chunk)
     y = decode(s, x.numel(), stream_bytes=nb, dtype=x.dtype)
-    return bool(torch.equal(y.view(torch.int16), _flat16(x).view(torch.int16)))
+    return bool(torch.equal(y.view(torch.int16), _flat16(x).reshape(-1).view(torch.int16)))
 
 
 __all__ = [

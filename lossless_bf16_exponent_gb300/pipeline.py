@@ -82,10 +82,10 @@ def send_compressed(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, 
     tensor (bit-identical to ``x``) and the device-timed transfer."""
     if link not in ("host", "d2d"):
         raise ValueError("link must be 'host' or 'd2d'")
-    v = _flat16(x)
+    v = _flat16(x).reshape(-1)
     dev = v.device
     n = v.numel()
-    y = torch.empty_like(v) if out is None else _flat16(out)
+    y = torch.empty_like(v) if out is None else _flat16(out).reshape(-1)
     parts = split_points(n, pieces)
     L = load()
     st = _Streams(dev)
@@ -162,10 +162,10 @@ def send_compressed(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, 
 
 def send_raw(x: torch.Tensor, pieces: int = 16, link: str = "host", out: torch.Tensor | None = None):
     """The same pipeline without the codec: each raw piece crosses the link."""
-    v = _flat16(x)
+    v = _flat16(x).reshape(-1)
     dev = v.device
     n = v.numel()
-    y = torch.empty_like(v) if out is None else _flat16(out)
+    y = torch.empty_like(v) if out is None else _flat16(out).reshape(-1)
     parts = split_points(n, pieces)
     st = _Streams(dev)
     host = torch.empty(n, dtype=v.dtype, pin_memory=True) if link == "host" else None
