@@ -104,6 +104,7 @@ struct Params {
     uint64_t n;
     uint32_t chunk;
     uint32_t seg_units;   // units per segment
+    uint32_t seg_shift;   // log2(seg_units)
     uint32_t nseg;        // segments
     uint32_t range_chunks;
     uint32_t chunk_shift;  // log2(chunk) when chunk is a power of two, else 32
@@ -330,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
                     wait_for_prerequisite();
                     cleared = true;
                 }
-                atomicAdd(&p.segs[u / p.seg_units], cnt);
+                atomicAdd(&p.segs[u >> p.seg_shift], cnt);
             }
         }
     }
@@ -495,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
                     wait_for_prerequisite();
                     cleared = true;
                 }
-                atomicAdd(&p.segs[u / p.seg_units], cnt);
+                atomicAdd(&p.segs[u >> p.seg_shift], cnt);
             }
         }
     }
@@ -556,7 +557,7 @@ __device__ __forceinline__ void load_range(const Params& p, uint64_t r, uint32_t
     rl.e = (uint32_t)min((uint64_t)c1 * C, p.n);
     rl.u0 = rl.s / kUnit;
     rl.nu = (rl.e - 1) / kUnit - rl.u0 + 1;
-    rl.seg = rl.u0 / p.seg_units;
+    rl.seg = rl.u0 >> p.seg_shift;
 #pragma unroll
     for (int rr = 0; rr < kRounds; rr++) {
         const uint32_t u = rl.u0 + 32 * rr + lane;
@@ -943,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ESC_MIN_BLOCKS) encode_escape_k
         // first unit (a block-wide sum of at most kMaxSegments totals).
         const uint64_t r = rb + warp;
         const bool active = r < p.ranges;
-        const uint32_t seg_first = (uint32_t)(rb * p.range_chunks * p.chunk / kUnit) / p.seg_units;
+        const uint32_t seg_first = (uint32_t)(rb * p.range_chunks * p.chunk / kUnit) >> p.seg_shift;
         RangeLoads<kRounds> rl;
         __syncwarp();  // the previous range's list entries are no longer read
         if (active) load_range(p, r, seg_first, rl, s_head);
@@ -1056,6 +1057,7 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
     p.cap = out_capacity;
     p.L = L;
     p.seg_units = g.seg_units;
+    p.seg_shift = (uint32_t)__builtin_ctz(g.seg_units);
     p.nseg = g.nseg;
     p.segs = reinterpret_cast<uint32_t*>(ws + g.off_segs);
     p.counts = reinterpret_cast<uint32_t*>(ws + g.off_counts);
