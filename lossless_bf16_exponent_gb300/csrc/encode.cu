@@ -342,37 +342,39 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
 
 // ------------------------------------------------------- FP8 E5M2 dense kernel
 
+// E5M2 exponents have 5 bits, so a table of every exponent pair fits in
+// 2 KB of shared memory: entry (ea | eb << 5) = code(ea) | code(eb) << 4 (the
+// packed code byte of two neighbouring values) | esc(ea) << 8 | esc(eb) << 9.
+// One lookup then encodes two values.
+constexpr uint32_t kPairEntries = 1024;
+
 // Eight E5M2 values (w0, w1: value i in byte i) -> their 8 codes (one word,
 // value i in nibble i), their 3-bit sign-mantissa fields (24 bits, value i at
-// bits 3i), the escape flags (bit 7 of byte i of esc_lo / esc_hi for value i /
-// i + 4) and the exponents (bytes of e_lo / e_hi).
-__device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, const uint8_t* tab, uint32_t& codes,
-                                                  uint32_t& fields, uint32_t& esc_lo, uint32_t& esc_hi,
-                                                  uint32_t& e_lo, uint32_t& e_hi) {
+// bits 3i) and their escape flags (byte k: bit 0 for value 2k, bit 1 for
+// value 2k + 1).
+__device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, const uint16_t* pair, uint32_t& codes,
+                                                  uint32_t& fields, uint32_t& escs) {
     const uint32_t w[2] = {w0, w1};
-    uint32_t packed[2], esc[2], ex[2], f[2];
+    uint32_t t[4], f[2];
 #pragma unroll
     for (int h = 0; h < 2; h++) {
-        const uint32_t e4 = (w[h] >> 2) & 0x1F1F1F1Fu;                      // exponent bytes
         const uint32_t a4 = ((w[h] >> 5) & 0x04040404u) | (w[h] & 0x03030303u);  // sign << 2 | mantissa
         const uint32_t pr = a4 | (a4 >> 5);  // bits 0..5: a0 | a1 << 3; bits 16..21: a2 | a3 << 3
         f[h] = (pr & 0x3Fu) | ((pr >> 10) & 0xFC0u);
-        ex[h] = e4;
-        const uint32_t t0 = tab[e4 & 0xFF];
-        const uint32_t t1 = tab[prmt(e4, 0, 0x4441)];
-        const uint32_t t2 = tab[prmt(e4, 0, 0x4442)];
-        const uint32_t t3 = tab[e4 >> 24];
-        const uint32_t t4 = prmt(prmt(t0, t1, 0x0040), prmt(t2, t3, 0x0040), 0x5410);
-        const uint32_t c = t4 & 0x0F0F0F0Fu;
-        packed[h] = c | (c >> 4);
-        esc[h] = t4 & 0x80808080u;
+        t[2 * h] = pair[((w[h] >> 2) & 0x1Fu) | ((w[h] >> 5) & 0x3E0u)];         // values 0, 1 of the word
+        t[2 * h + 1] = pair[((w[h] >> 18) & 0x1Fu) | ((w[h] >> 21) & 0x3E0u)];  // values 2, 3
     }
-    codes = prmt(packed[0], packed[1], 0x6420);
+    const uint32_t x = prmt(t[0], t[1], 0x5140), y = prmt(t[2], t[3], 0x5140);
+    codes = prmt(x, y, 0x5410);
+    escs = prmt(x, y, 0x7632);
     fields = f[0] | (f[1] << 12);
-    esc_lo = esc[0];
-    esc_hi = esc[1];
-    e_lo = ex[0];
-    e_hi = ex[1];
+}
+
+// Escape flags of encode_group_e5m2 (pair k's two bits in byte k) -> 8-bit
+// mask, value i at bit i: the multiply moves byte k's bits to 18 + 2k, and no
+// two of its shifted copies overlap or carry into that window.
+__device__ __forceinline__ uint32_t escape_mask_pairs(uint32_t escs) {
+    return (((escs & 0x03030303u) * 0x41041u) >> 18) & 0xFFu;
 }
 
 // The dense pass for E5M2 input: as encode_dense_kernel, one warp per unit
@@ -381,9 +383,15 @@ __device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, cons
 // of codes stored), so a row of the warp covers 1024 values in ascending
 // lane order and its escapes are ranked with one scan.
 __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5m2_kernel(const Params p) {
-    __shared__ uint32_t s_tab_words[64];
-    uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_tab_words);
-    s_tab[threadIdx.x] = p.cb[UZIP_CB_ENC + threadIdx.x] | (p.cb[UZIP_CB_ESC + threadIdx.x] ? 0x80 : 0);
+    __shared__ uint8_t s_tab[32];
+    __shared__ uint16_t s_pair[kPairEntries];
+    if (threadIdx.x < 32)
+        s_tab[threadIdx.x] = p.cb[UZIP_CB_ENC + threadIdx.x] | (p.cb[UZIP_CB_ESC + threadIdx.x] ? 0x80 : 0);
+    __syncthreads();
+    for (uint32_t i = threadIdx.x; i < kPairEntries; i += kThreads) {
+        const uint32_t ta = s_tab[i & 31], tb = s_tab[i >> 5];
+        s_pair[i] = (uint16_t)((ta & 0xF) | ((tb & 0xF) << 4) | ((ta >> 7) << 8) | ((tb >> 7) << 9));
+    }
     __syncthreads();
     allow_dependent_launch();
 
@@ -424,18 +432,15 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
             const uint32_t slot = it * 32 + lane;
             const uint32_t v0 = 32 * slot;  // this lane's values v0 .. v0 + 31 of the unit
             const uint32_t* w = wall[it];
-            uint32_t codes[4], fields[4], ex[8];
-            uint32_t emask = 0;
+            uint32_t codes[4], fields[4], escs[4];
+            uint32_t escany = 0;
 #pragma unroll
             for (int q = 0; q < 4; q++) {
-                uint32_t esc_lo, esc_hi;
-                encode_group_e5m2(w[2 * q], w[2 * q + 1], s_tab, codes[q], fields[q], esc_lo, esc_hi, ex[2 * q],
-                                  ex[2 * q + 1]);
-                emask |= escape_mask(esc_lo, esc_hi) << (8 * q);
+                encode_group_e5m2(w[2 * q], w[2 * q + 1], s_pair, codes[q], fields[q], escs[q]);
+                escany |= escs[q];
             }
             const uint32_t valid = ulen > v0 ? min(ulen - v0, 32u) : 0u;
-            if (valid < 32) {  // only real values have codes, fields and escapes
-                emask &= (1u << valid) - 1;
+            if (valid < 32) {  // only real values have codes and fields (escapes: masked below)
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     const uint32_t vq = valid > 8u * q ? min(valid - 8u * q, 8u) : 0u;
@@ -463,7 +468,11 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
                     if (b < 3 * gv) dst_a[12 * slot + b] = (uint8_t)((b < 4 ? f0 : b < 8 ? f1 : f2) >> (8 * (b & 3)));
             }
             // Escapes of this row (1024 values, lane-major): one scan ranks them.
-            if (__any_sync(0xffffffffu, emask != 0)) {
+            if (__any_sync(0xffffffffu, (escany & 0x03030303u) != 0)) {
+                uint32_t emask = 0;
+#pragma unroll
+                for (int q = 0; q < 4; q++) emask |= escape_mask_pairs(escs[q]) << (8 * q);
+                if (valid < 32) emask &= (1u << valid) - 1;  // (valid == 0: no bits)
                 const uint32_t c = __popc(emask);
                 uint32_t incl = c;
 #pragma unroll
@@ -474,10 +483,10 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
                 uint32_t j = cnt + incl - c;
                 for (uint32_t bits = emask; bits; bits &= bits - 1, j++) {
                     const uint32_t b = __ffs(bits) - 1;
-                    const uint32_t k = b >> 2;  // exponent word of value b, chosen in registers
-                    const uint32_t lo = (k & 2) ? ((k & 1) ? ex[3] : ex[2]) : ((k & 1) ? ex[1] : ex[0]);
-                    const uint32_t hi = (k & 2) ? ((k & 1) ? ex[7] : ex[6]) : ((k & 1) ? ex[5] : ex[4]);
-                    const uint32_t e = (((k & 4) ? hi : lo) >> (8 * (b & 3))) & 0x1F;
+                    const uint32_t k = b >> 2;  // input word of value b, chosen in registers
+                    const uint32_t lo = (k & 2) ? ((k & 1) ? w[3] : w[2]) : ((k & 1) ? w[1] : w[0]);
+                    const uint32_t hi = (k & 2) ? ((k & 1) ? w[7] : w[6]) : ((k & 1) ? w[5] : w[4]);
+                    const uint32_t e = (((k & 4) ? hi : lo) >> (8 * (b & 3) + 2)) & 0x1F;
                     if (j < kListCap) st_u32_keep(list + j, (v0 + b) | (e << 16), keep);
                 }
                 cnt += __shfl_sync(0xffffffffu, incl, 31);
