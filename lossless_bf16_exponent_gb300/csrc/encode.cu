@@ -53,6 +53,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr uint32_t kMaxSegments = 2048;       // segment totals (a block sums up to all of them)
 constexpr uint32_t kListCap = 64;             // escape entries a unit keeps in its list
 constexpr uint32_t kHeadEntries = 32;         // list entries a unit keeps in shared memory during the escape pass
+static_assert(kHeadEntries == 32, "head_slot: eight 16-byte chunks per lane row");
 constexpr uint32_t kMaxRangeUnits = 31;       // a range covers at most 31 units of values (32 overlapped)
 constexpr uint32_t kStageBytes = 2560;        // per-warp staging of a range's escape blocks (853 escapes)
 constexpr uint32_t kMaxRangeChunks = 256;     // bounds the per-warp chunk table
@@ -200,11 +201,12 @@ __device__ void zero_words(uint8_t* out, uint64_t from, uint64_t to) {
 
 __device__ __forceinline__ uint32_t warp_sum(uint32_t v) { return __reduce_add_sync(0xffffffffu, v); }
 
-// Shared-memory slot of list entry j of lane L's unit (round rr): each lane
-// owns a 128-byte row of eight 16-byte chunks, chunk c stored at c ^ (L & 7)
-// so that lanes reading the same entry spread over the banks.
+// Shared-memory slot of list entry j (< kHeadEntries) of lane L's unit (round
+// rr): each lane owns a 128-byte row of eight 16-byte chunks, chunk c stored
+// at c ^ (L & 7) so that lanes reading the same entry spread over the banks;
+// for j < 32 that is entry j ^ ((L & 7) << 2) of the row.
 __device__ __forceinline__ uint32_t head_slot(int rr, uint32_t L, uint32_t j) {
-    return (uint32_t)rr * (kHeadEntries * 32) + L * kHeadEntries + ((((j >> 2) ^ (L & 7)) << 2) | (j & 3));
+    return (uint32_t)rr * (kHeadEntries * 32) + L * kHeadEntries + (j ^ ((L & 7) << 2));
 }
 
 // 16-byte asynchronous global -> shared copy (cp.async) and its wait.
@@ -842,6 +844,40 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
                 uint32_t i = n_lo[rr];
                 const uint32_t iend = i + n_in[rr];
                 uint32_t rank = first[rr];
+                if (staged && !sent && iend <= kHeadEntries) {
+                    // The common case, specialised: every entry in shared
+                    // memory, every byte into the stage.
+                    const uint32_t* hrow = s_head + (uint32_t)rr * (kHeadEntries * 32) + lane * kHeadEntries;
+                    const uint32_t hsw = (lane & 7) << 2;  // entry j of the row is hrow[j ^ hsw]
+                    uint32_t ent = hrow[i ^ hsw];
+                    uint32_t off = u.ubase + (ent & 0xFFFF) - s;
+                    for (;;) {
+                        const uint32_t q = div_chunk(p, off);
+                        const uint32_t qbeg = q * C;
+                        const uint32_t cstart = s_cp[q];
+                        const uint32_t k = s_cp[q + 1] - cstart;
+                        uint8_t* sp = stage + lead + 3 * cstart + 2 * (rank - cstart);
+                        uint8_t* sv = stage + lead + 3 * cstart + 2 * k + (rank - cstart);
+                        bool more;
+                        for (;;) {
+                            const uint32_t pos = off - qbeg, expo = ent >> 16;
+                            i++;
+                            rank++;
+                            more = i < iend;
+                            if (more) ent = hrow[i ^ hsw];
+                            sp[0] = (uint8_t)(pos & 0xFF);
+                            sp[1] = (uint8_t)(pos >> 8);
+                            *sv = (uint8_t)expo;
+                            sp += 2;
+                            sv += 1;
+                            if (!more) break;
+                            off = u.ubase + (ent & 0xFFFF) - s;
+                            if (off >= qbeg + C) break;  // the next escape opens another chunk
+                        }
+                        if (!more) break;
+                    }
+                    continue;
+                }
                 uint32_t ent = entry(rr, u.ubase, i);
                 uint32_t off = u.ubase + (ent & 0xFFFF) - s;
                 for (;;) {
