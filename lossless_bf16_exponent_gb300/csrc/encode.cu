@@ -709,7 +709,9 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
             uint32_t i = n_lo[rr];
             const uint32_t iend = n_lo[rr] + n_in[rr];
             while (q < nq && x < u.phi) {
-                uint32_t hi = iend;  // first entry at or past x: binary search (the list is ascending)
+                // First entry at or past x: binary search (the list is ascending;
+                // entries from n_lo on are at or past plo, so none is needed there).
+                uint32_t hi = x > u.plo ? iend : i;
                 while (i < hi) {
                     const uint32_t mid = (i + hi) >> 1;
                     if ((entry(rr, u.ubase, mid) & 0xFFFF) < x) i = mid + 1;
