@@ -155,16 +155,25 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "of fallback"
 
 
+def source_code_hash(path: str) -> str:
+    """First 16 hex digits of the SHA-256 of a CUDA source with its comments
+    and whitespace removed: the code a profile was taken on, unaffected by
+    edits to comments."""
+    text = open(path, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return hashlib.sha256("".join(text.split()).encode()).hexdigest()[:16]
+
+
 def profile_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (else None)."""
+    the current kernel code (else None)."""
     src = {"encode": "encode.cu", "decode": "decode.cu"}[kernel]
     path = os.path.join(ROOT, "profiles", f"{kernel}_kv_cache.md")
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(os.path.join(ROOT, "lossless_bf16_exponent_gb300", "csrc", src), "rb")
-                             .read()).hexdigest()[:16]
-        m_sha = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
+        sha = source_code_hash(os.path.join(ROOT, "lossless_bf16_exponent_gb300", "csrc", src))
+        m_sha = re.search(r"code_sha256_16:\s*([0-9a-f]+)", text)
         m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9]+)", text)
         if m_sha and m_b and m_sha.group(1) == sha:
             return int(m_b.group(1))

@@ -1,4 +1,5 @@
-// encode.cu -- SplitZip encoder for sm_103a: one pass over the input, two kernels.
+// encode.cu -- SplitZip encoder for sm_103a: one pass over the input (a one-block
+// clear of the segment totals, a dense kernel, an escape kernel).
 //
 // SplitZip review page, §3.2: encoding is (1) a dense transform -- split each
 // BF16 value into its exponent and sign-mantissa byte, store the latter
@@ -37,7 +38,9 @@
 //                  element order, bounds-checked against out_capacity. The warp
 //                  that owns the last range writes the tail and the header.
 // The input is read from HBM once; the escape lists cost about 4 bytes per
-// escape written and read.
+// escape written and read. FP8 E5M2 input (page §4.2) has its own dense
+// kernel (one lookup per exponent pair, 32 values per lane and step) and
+// shares the escape kernel.
 #include <algorithm>
 #include <atomic>
 
