@@ -1,0 +1,43 @@
+"""Concurrent use: the library keeps no device state between calls, so calls
+on different CUDA streams, each with its own output, workspace and codebook,
+may run at the same time on the GPU. Two tensors are encoded and decoded on
+two streams at once; each stream must equal, byte for byte, the stream the
+same call produces alone on the default stream, and each round trip must be
+bit-exact."""
+import pytest
+import torch
+
+import lossless_bf16_exponent_gb300.workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def test_two_streams_at_once_match_sequential_calls(uz):
+    dev = torch.device("cuda")
+    shape = (8, 2, 8, 256, 128)  # 4 Mi values each: enough blocks for the two to overlap
+    xs = [W.kv_cache(shape, seed=21, device=dev).reshape(-1), W.heavy_tailed(1 << 22, seed=22, device=dev)]
+    samples = [W.kv_cache_sample(device=dev), W.gaussian(1 << 16, seed=23, device=dev)]
+    chunks = [1024, 256]
+    cbs = [uz.calibrate(s) for s in samples]
+    want = [uz.encode(x, cb, c) for x, cb, c in zip(xs, cbs, chunks)]
+    torch.cuda.synchronize()
+
+    streams = [torch.cuda.Stream(dev) for _ in xs]
+    outs = [torch.empty(uz.max_compressed_size(x.numel(), c), dtype=torch.uint8, device=dev)
+            for x, c in zip(xs, chunks)]
+    wss = [torch.empty(uz.workspace_bytes(x.numel(), c), dtype=torch.uint8, device=dev) for x, c in zip(xs, chunks)]
+    ys = [torch.empty_like(x) for x in xs]
+    for rep in range(3):
+        for o in outs:
+            o.fill_(0xAB)
+        torch.cuda.synchronize()
+        for k, st in enumerate(streams):
+            with torch.cuda.stream(st):
+                uz.encode(xs[k], cbs[k], chunks[k], out=outs[k], workspace=wss[k], sync=False)
+                uz.decode(outs[k], xs[k].numel(), out=ys[k])
+        torch.cuda.synchronize()
+        for k in range(len(xs)):
+            stream, nbytes = want[k]
+            assert torch.equal(outs[k][:nbytes], stream[:nbytes]), f"stream {k} differs (rep {rep})"
+            assert torch.all(outs[k][nbytes:] == 0xAB), f"stream {k}: bytes past its end written (rep {rep})"
+            assert torch.equal(ys[k].view(torch.int16), xs[k].view(torch.int16)), f"round trip {k} (rep {rep})"
