@@ -366,8 +366,12 @@ __device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, cons
         const uint32_t a4 = ((w[h] >> 5) & 0x04040404u) | (w[h] & 0x03030303u);  // sign << 2 | mantissa
         const uint32_t pr = a4 | (a4 >> 5);  // bits 0..5: a0 | a1 << 3; bits 16..21: a2 | a3 << 3
         f[h] = (pr & 0x3Fu) | ((pr >> 10) & 0xFC0u);
-        t[2 * h] = pair[((w[h] >> 2) & 0x1Fu) | ((w[h] >> 5) & 0x3E0u)];         // values 0, 1 of the word
-        t[2 * h + 1] = pair[((w[h] >> 18) & 0x1Fu) | ((w[h] >> 21) & 0x3E0u)];  // values 2, 3
+        // Exponent bytes e0..e3 -> e0 | e1 << 5 in bits 0..9 and e2 | e3 << 5 in
+        // bits 16..25 (bits 13..15 pick up e2's low bits and are not used).
+        const uint32_t e4 = (w[h] >> 2) & 0x1F1F1F1Fu;
+        const uint32_t ix = (e4 & 0x001F001Fu) | ((e4 >> 3) & 0xFFE0FFE0u);
+        t[2 * h] = pair[ix & 0x3FFu];  // values 0, 1 of the word
+        t[2 * h + 1] = pair[ix >> 16];  // values 2, 3
     }
     const uint32_t x = prmt(t[0], t[1], 0x5140), y = prmt(t[2], t[3], 0x5140);
     codes = prmt(x, y, 0x5410);
