@@ -155,14 +155,25 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "of fallback"
 
 
-def source_code_hash(path: str) -> str:
-    """First 16 hex digits of the SHA-256 of a CUDA source with its comments
-    and whitespace removed: the code a profile was taken on, unaffected by
-    edits to comments."""
-    text = open(path, encoding="utf-8").read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    text = re.sub(r"//[^\n]*", "", text)
-    return hashlib.sha256("".join(text.split()).encode()).hexdigest()[:16]
+def source_code_hash(*paths: str) -> str:
+    """First 16 hex digits of the SHA-256 of CUDA sources (in order) with
+    their comments and whitespace removed: the code a profile was taken on,
+    unaffected by edits to comments."""
+    h = hashlib.sha256()
+    for path in paths:
+        text = open(path, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("".join(text.split()).encode())
+    return h.hexdigest()[:16]
+
+
+def kernel_code_hash(source: str) -> str:
+    """Code hash of one kernel source of the library together with the two
+    headers every kernel source includes."""
+    return source_code_hash(os.path.join(ROOT, "lossless_bf16_exponent_gb300", "csrc", source),
+                            os.path.join(ROOT, "lossless_bf16_exponent_gb300", "csrc", "uzip_internal.cuh"),
+                            os.path.join(ROOT, "include", "uzip.h"))
 
 
 def profile_traffic(kernel: str):
@@ -172,7 +183,7 @@ def profile_traffic(kernel: str):
     path = os.path.join(ROOT, "profiles", f"{kernel}_kv_cache.md")
     try:
         text = open(path).read()
-        sha = source_code_hash(os.path.join(ROOT, "lossless_bf16_exponent_gb300", "csrc", src))
+        sha = kernel_code_hash(src)
         m_sha = re.search(r"code_sha256_16:\s*([0-9a-f]+)", text)
         m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9]+)", text)
         if m_sha and m_b and m_sha.group(1) == sha:

@@ -377,7 +377,9 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
 // ------------------------------------------------------ Top-15 + sentinel
 
 // Sentinel (code 15) flags of eight codes: bit 4i set when nibble i is 15.
-__device__ __forceinline__ uint32_t sentinel_bits(uint32_t w) { return w & (w >> 1) & (w >> 2) & (w >> 3) & 0x11111111u; }
+__device__ __forceinline__ uint32_t sentinel_bits(uint32_t w) {
+    return w & (w >> 1) & (w >> 2) & (w >> 3) & 0x11111111u;
+}
 
 // 16-byte asynchronous global -> shared copy (cp.async) and its wait.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {

@@ -127,7 +127,9 @@ struct Params {
 // Programmatic dependent launch (PTX griddepcontrol): the dense kernel lets
 // the escape kernel be scheduled early; the escape kernel waits until the
 // dense grid has completed and its writes are visible.
-__device__ __forceinline__ void allow_dependent_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ void wait_for_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Eight values -> 8 sign-mantissa bytes (a_lo, a_hi), 8 packed codes (one
@@ -327,7 +329,8 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
 #pragma unroll
             for (int it = 0; it < 2; it++)
 #pragma unroll
-                for (int r = 0; r < 4; r++) st_u8_keep(gmask + it * 128 + r * 32 + lane, (mbytes[it] >> (8 * r)) & 0xFF, keep);
+                for (int r = 0; r < 4; r++)
+                    st_u8_keep(gmask + it * 128 + r * 32 + lane, (mbytes[it] >> (8 * r)) & 0xFF, keep);
         }
         if (lane == 0) {
             st_u32_keep(p.counts + u, cnt, keep);
@@ -617,7 +620,8 @@ __device__ __forceinline__ void escape_range(const Params& p, const RangeLoads<k
         if (32 * rr + lane < nu && rl.cnt[rr] > 8) {
             const uint32_t c = min(rl.cnt[rr], kListCap);
             const uint32_t* list = p.lists + (uint64_t)(u0 + 32 * rr + lane) * kListCap;
-            for (uint32_t j = 8; j < min(c, kHeadEntries); j += 4) cp_async16(s_head + head_slot(rr, lane, j), list + j);
+            for (uint32_t j = 8; j < min(c, kHeadEntries); j += 4)
+                cp_async16(s_head + head_slot(rr, lane, j), list + j);
             for (uint32_t j = kHeadEntries; j < c; j += 8) prefetch_l1(list + j);  // one 32-byte sector each
         }
     }

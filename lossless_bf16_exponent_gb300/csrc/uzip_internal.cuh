@@ -91,7 +91,9 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // Programmatic dependent launch (PTX griddepcontrol): let the next kernel of
 // the stream launch now / wait until the previous kernel has completed and
 // its writes are visible (a no-op when not launched as a dependent).
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // 16-byte streaming load through the non-coherent path (data read once).

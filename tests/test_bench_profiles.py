@@ -1,6 +1,7 @@
 """bench.py reports a kernel's DRAM traffic from a committed ncu summary only
 while the kernel code that summary was taken on is unchanged: the check
-hashes the CUDA source with comments and whitespace removed."""
+hashes the kernel's CUDA source and the headers it includes, with comments
+and whitespace removed."""
 import os
 import sys
 
@@ -35,9 +36,15 @@ def test_traffic_needs_a_matching_summary(tmp_path, monkeypatch):
     (prof / "encode_kv_cache.md").write_text("dram_bytes_per_full_launch: 123\ncode_sha256_16: 0000000000000000\n")
     csrc = tmp_path / "lossless_bf16_exponent_gb300" / "csrc"
     csrc.mkdir(parents=True)
+    (tmp_path / "include").mkdir()
     (csrc / "encode.cu").write_text("int f() { return 0; }\n")
+    (csrc / "uzip_internal.cuh").write_text("#pragma once\n")
+    (tmp_path / "include" / "uzip.h").write_text("#define UZIP_VERSION 1\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.profile_traffic("encode") is None
-    good = bench.source_code_hash(str(csrc / "encode.cu"))
+    good = bench.kernel_code_hash("encode.cu")
     (prof / "encode_kv_cache.md").write_text(f"dram_bytes_per_full_launch: 123\ncode_sha256_16: {good}\n")
     assert bench.profile_traffic("encode") == 123
+    # a change in an included header is a change of the kernel code
+    (csrc / "uzip_internal.cuh").write_text("#pragma once\nconstexpr int k = 1;\n")
+    assert bench.profile_traffic("encode") is None
