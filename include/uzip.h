@@ -230,8 +230,9 @@ UZIP_API int uzip_decode(const void *d_stream, size_t stream_bytes, void *d_out_
  *                  that receives the bytes copied (0 when nothing was).
  * When either end is host memory the copy uses a small grid that fills the
  * host link and leaves the SMs to concurrent codec kernels.
- * Returns UZIP_ERR_ARG / UZIP_ERR_ALIGN / UZIP_ERR_CAPACITY / UZIP_ERR_CUDA,
- * else UZIP_OK. Async. */
+ * Returns UZIP_ERR_ARG (a NULL end, or an end or d_copied in pageable host
+ * memory or at an address CUDA does not know; nothing is launched) /
+ * UZIP_ERR_ALIGN / UZIP_ERR_CAPACITY / UZIP_ERR_CUDA, else UZIP_OK. Async. */
 UZIP_API int uzip_stream_copy(const void *src_stream, void *dst, size_t capacity,
                               unsigned long long *d_copied, uzip_stream_t stream);
 

@@ -45,13 +45,19 @@ __global__ void __launch_bounds__(kCopyThreads) stream_copy_kernel(const uint8_t
     if (blockIdx.x == 0 && threadIdx.x < total % 16) dst[vecs * 16 + threadIdx.x] = src[vecs * 16 + threadIdx.x];
 }
 
-bool is_host_memory(const void* p) {
+// Where a pointer lives: kDevice (device or managed memory), kPinned (page-
+// locked host memory, which a kernel reaches over the host link) or kOther
+// (pageable host memory or an unknown address: no kernel may touch it).
+enum Where { kDevice, kPinned, kOther };
+
+Where where_is(const void* p) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-        cudaGetLastError();  // unregistered host memory: clear the error
-        return true;
+        cudaGetLastError();  // clear the error
+        return kOther;
     }
-    return a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered;
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return kDevice;
+    return a.type == cudaMemoryTypeHost ? kPinned : kOther;
 }
 
 }  // namespace
@@ -67,7 +73,9 @@ extern "C" UZIP_API int uzip_stream_copy(const void* src_stream, void* dst, size
     int dev = 0, sms = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
     UZIP_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    const bool host_end = is_host_memory(src_stream) || is_host_memory(dst);
+    const Where ws = where_is(src_stream), wd = where_is(dst);
+    if (ws == kOther || wd == kOther || (d_copied && where_is(d_copied) == kOther)) return UZIP_ERR_ARG;
+    const bool host_end = ws == kPinned || wd == kPinned;
     const uint64_t per_cta = (uint64_t)kCopyThreads * kCopyUnroll * 16;
     const uint64_t want = std::max<uint64_t>(1, (capacity + per_cta - 1) / per_cta);
     const uint64_t grid = std::min<uint64_t>(want, host_end ? 32 : (uint64_t)sms * 4);

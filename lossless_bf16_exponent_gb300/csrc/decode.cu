@@ -111,13 +111,15 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
         if (blockIdx.x == 0 && tid == 0 && p.status) *p.status = UZIP_ERR_CORRUPT;
         return;
     }
-    const uint32_t n32 = (uint32_t)p.n;  // n < 2^32
+    // n < 2^32; sums that can pass n (a tile count, the end of a group or
+    // chunk) are taken in 64 bits or relative to the tile.
+    const uint32_t n32 = (uint32_t)p.n;
     const uint8_t* A = p.s + L.off_a;
     const uint8_t* B = p.s + L.off_b;
     const uint8_t* C = p.s + L.off_c;
     const uint8_t* D = p.s + L.off_d;
     const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;  // decode table: code k -> byte k
-    const uint32_t tiles = (n32 + kTile - 1) / kTile;
+    const uint32_t tiles = (uint32_t)(((uint64_t)n32 + kTile - 1) / kTile);
 
     s_mask[0][tid] = 0;
     if (tid == 0) s_bad = 0;
@@ -202,14 +204,14 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
             }
             const uint2 lo = rebuild4(e_lo, av[r].x);
             const uint2 hi = rebuild4(e_hi, av[r].y);
-            if (full || e0 + 8 * g + 8 <= n32) {
+            if (full || 8 * g + 8 <= tlen) {
                 *reinterpret_cast<uint4*>(out + 8 * r * kThreads) = make_uint4(lo.x, lo.y, hi.x, hi.y);
             } else {
                 const uint32_t ge = e0 + 8 * g;
                 const uint32_t w[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
                 for (uint32_t i = 0; i < 8; i++)
-                    if (ge + i < n32) p.out[ge + i] = (uint16_t)(w[i / 2] >> (16 * (i & 1)));
+                    if (8 * g + i < tlen) p.out[ge + i] = (uint16_t)(w[i / 2] >> (16 * (i & 1)));
             }
         }
         __syncthreads();  // s_val and this bitmap are rewritten by the next tile
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
     const uint8_t* D = p.s + L.off_d;
     uint8_t* out8 = reinterpret_cast<uint8_t*>(p.out);
     const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;
-    const uint32_t tiles = (n32 + kE5Tile - 1) / kE5Tile;
+    const uint32_t tiles = (uint32_t)(((uint64_t)n32 + kE5Tile - 1) / kE5Tile);
 
     for (uint32_t i = tid; i < kE5Tile / 32; i += kThreads) s_mask[0][i] = 0;
     if (tid == 0) s_bad = 0;
@@ -359,14 +361,14 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
                 }
             }
             const uint32_t ge = e0 + v0;
-            if (ge + 32 <= n32) {
+            if (v0 + 32 <= tlen) {
                 uint4* dst = reinterpret_cast<uint4*>(out8 + ge);
                 dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
                 dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
             } else {
 #pragma unroll
                 for (uint32_t i = 0; i < 32; i++)
-                    if (ge + i < n32) out8[ge + i] = (uint8_t)(o[i / 4] >> (8 * (i & 3)));
+                    if (v0 + i < tlen) out8[ge + i] = (uint8_t)(o[i / 4] >> (8 * (i & 3)));
             }
         }
         __syncthreads();  // s_val and this bitmap are rewritten by the next tile
@@ -458,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_SDEC_MIN_BLOCKS) decode_sentine
     const uint8_t* D = p.s + L.off_d;
     const uint64_t d_room = p.stream_bytes - L.off_d;  // readable bytes from D on
     const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;
-    const uint32_t tiles = (n32 + kTile - 1) / kTile;
+    const uint32_t tiles = (uint32_t)(((uint64_t)n32 + kTile - 1) / kTile);
     const uint32_t t_begin = (uint32_t)((uint64_t)tiles * blockIdx.x / gridDim.x);
     const uint32_t t_end = (uint32_t)((uint64_t)tiles * (blockIdx.x + 1) / gridDim.x);
     if (tid == 0) s_bad = 0;
@@ -569,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_SDEC_MIN_BLOCKS) decode_sentine
         // every chunk ending in the tile: its end offset against the code 15s before it
         for (uint32_t k = tid; k <= c_last - c_first; k += kThreads) {
             const uint32_t c = c_first + k;
-            const uint32_t ce = min((c + 1) * chunk, n32);
+            const uint32_t ce = (uint32_t)min((uint64_t)(c + 1) * chunk, (uint64_t)n32);
             const uint32_t o1 = s_off[par][k + 1];
             if (ce <= e0 + tlen && g0 + before(ce - e0) != o1) s_bad = 1;
             if ((c == 0 && s_off[par][k] != 0) || (c + 1 == nc && o1 != m32)) s_bad = 1;
@@ -606,13 +608,13 @@ __global__ void __launch_bounds__(kThreads, UZIP_SDEC_MIN_BLOCKS) decode_sentine
             const uint2 lo = rebuild4(e_lo, av[r].x);
             const uint2 hi = rebuild4(e_hi, av[r].y);
             const uint32_t ge = e0 + 8 * g;
-            if (ge + 8 <= n32) {
+            if (8 * g + 8 <= tlen) {
                 *reinterpret_cast<uint4*>(p.out + ge) = make_uint4(lo.x, lo.y, hi.x, hi.y);
             } else {
                 const uint32_t wv[4] = {lo.x, lo.y, hi.x, hi.y};
 #pragma unroll
                 for (uint32_t i = 0; i < 8; i++)
-                    if (ge + i < n32) p.out[ge + i] = (uint16_t)(wv[i / 2] >> (16 * (i & 1)));
+                    if (8 * g + i < tlen) p.out[ge + i] = (uint16_t)(wv[i / 2] >> (16 * (i & 1)));
             }
         }
         g0 += tile_total;

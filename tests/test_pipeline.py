@@ -7,6 +7,7 @@ import pytest
 import torch
 
 import lossless_bf16_exponent_gb300.workloads as W
+from lossless_bf16_exponent_gb300 import _lib
 from lossless_bf16_exponent_gb300 import pipeline as PL
 
 
@@ -94,3 +95,25 @@ def test_stream_copy_refuses_non_streams(uz):
     uz.stream_copy(stream, dst, nbytes - 1, copied=copied)  # capacity below the stream's total
     torch.cuda.synchronize()
     assert int(copied.item()) == 0 and torch.all(dst == 7)
+
+
+@pytest.mark.gpu
+def test_stream_copy_refuses_pageable_memory(uz):
+    """A kernel may touch device or pinned host memory only: pageable host
+    buffers (either end, or the byte-count word) are refused on the host,
+    before anything is launched."""
+    x = torch.randn(10_000, device="cuda").bfloat16()
+    stream, nbytes = uz.encode(x, uz.calibrate(x), 1024)
+    cap = stream.numel()
+    dst = torch.zeros(cap, dtype=torch.uint8, device="cuda")
+    pageable = torch.zeros(cap, dtype=torch.uint8)
+    assert not pageable.is_pinned()
+    for src, to in ((stream, pageable), (pageable, dst)):
+        with pytest.raises(_lib.UzipError) as e:
+            uz.stream_copy(src, to, cap)
+        assert e.value.code == _lib.ERR_ARG
+    with pytest.raises(_lib.UzipError) as e:
+        uz.stream_copy(stream, dst, cap, copied=torch.zeros(1, dtype=torch.int64))
+    assert e.value.code == _lib.ERR_ARG
+    torch.cuda.synchronize()
+    assert torch.all(dst == 0) and torch.all(pageable == 0)
