@@ -267,6 +267,8 @@ def run_ours(args):
     cal_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     enc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    median_us = {op: round(statistics.median(e[i].elapsed_time(e[i + 1]) for e in evs) * 1e3, 2)
+                 for i, op in enumerate(("calibrate", "encode", "decode"))}
     max_ms = max_over_ranks(elapsed_ms, dev)
     total_raw = sum_over_ranks(raw * args.steps, dev)
 
@@ -277,7 +279,7 @@ def run_ours(args):
 
     cpu = cpu_baseline(x, sample) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
     return report(args, ws, rank, n, raw, nbytes, m, max_ms, total_raw, cal_ms, enc_ms, dec_ms, e2e, cpu,
-                  clocks, sample)
+                  clocks, sample, median_us)
 
 
 def e2e_measure(args, x, sample, cb, out, wsb, y, n, raw, stream, dev):
@@ -353,7 +355,10 @@ def e2e_measure(args, x, sample, cb, out, wsb, y, n, raw, stream, dev):
 
 
 def report(args, ws, rank, n, raw, nbytes, m, max_ms, total_raw, cal_ms, enc_ms, dec_ms, e2e, cpu, clocks,
-           sample):
+           sample, median_us=None):
+    """The JSON line. Per-op times (calibrate_us, encode_us, decode_us and
+    the rates and fractions derived from them) are means over the timed
+    steps, as the page reports them; ``median_us`` holds the medians."""
     if rank != 0:
         return None
     peak, peak_src = measured_peak()
@@ -385,6 +390,7 @@ def report(args, ws, rank, n, raw, nbytes, m, max_ms, total_raw, cal_ms, enc_ms,
         "calibrate_us": round(cal_ms * 1e3, 2),
         "encode_us": round(enc_ms * 1e3, 2),
         "decode_us": round(dec_ms * 1e3, 2),
+        "median_us": median_us,
         "ratio": round(raw / nbytes, 5),
         "ratio_payload": round(raw / (n + (n + 1) // 2 + 3 * m), 5),
         "escape_rate": m / n,
