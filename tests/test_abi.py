@@ -136,3 +136,13 @@ def test_calibrate_and_codebook_validation(lib):
     ok = (ctypes.c_uint8 * 16)(*range(16))
     assert lib.uzip_codebook_from_exps(ok, MIS, None) == _lib.ERR_ALIGN
     assert lib.uzip_codebook_from_exps(None, A16, None) == _lib.ERR_ARG
+
+
+def test_stream_copy_argument_validation(lib):
+    # Checked on the host before the memory kinds are looked up or anything is launched.
+    assert lib.uzip_stream_copy(None, A16, 4096, None, None) == _lib.ERR_ARG
+    assert lib.uzip_stream_copy(A16, None, 4096, None, None) == _lib.ERR_ARG
+    assert lib.uzip_stream_copy(MIS, A16, 4096, None, None) == _lib.ERR_ALIGN
+    assert lib.uzip_stream_copy(A16, MIS, 4096, None, None) == _lib.ERR_ALIGN
+    assert lib.uzip_stream_copy(A16, A16, 4096, ctypes.c_void_p(0x10004), None) == _lib.ERR_ALIGN
+    assert lib.uzip_stream_copy(A16, A16, 63, None, None) == _lib.ERR_CAPACITY
