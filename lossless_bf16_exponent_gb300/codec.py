@@ -44,6 +44,56 @@ def _flat16(x: torch.Tensor) -> torch.Tensor:
     return x
 
 
+def _nbytes(t: torch.Tensor) -> int:
+    return t.numel() * t.element_size()
+
+
+def _dev(t: torch.Tensor, what: str, nbytes: int = 0) -> torch.Tensor:
+    """Check a caller-given device buffer: a contiguous CUDA tensor of at
+    least ``nbytes`` bytes (the C ABI takes only its address, so its extent
+    is checked here)."""
+    if not t.is_cuda:
+        raise ValueError(f"{what}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{what}: expected a contiguous tensor")
+    if _nbytes(t) < nbytes:
+        raise ValueError(f"{what}: holds {_nbytes(t)} bytes, needs {nbytes}")
+    return t
+
+
+def _cb(codebook: torch.Tensor) -> torch.Tensor:
+    return _dev(codebook, "codebook", CODEBOOK_BYTES)
+
+
+def _status(status: torch.Tensor | None):
+    """The decoders' status word: one int32 in device (or pinned host) memory."""
+    if status is None:
+        return None
+    if (status.dtype != torch.int32 or status.numel() < 1 or not status.is_contiguous()
+            or not (status.is_cuda or status.is_pinned())):
+        raise ValueError("status: expected a contiguous int32 CUDA (or pinned host) tensor of one element")
+    return _p(status)
+
+
+def _stream_nbytes(stream: torch.Tensor, stream_bytes: int | None) -> int:
+    """Readable bytes of a stream tensor: all of it, or the first ``stream_bytes``."""
+    if not stream.is_contiguous():
+        raise ValueError("stream: expected a contiguous tensor")
+    if stream_bytes is None:
+        return _nbytes(stream)
+    if not 0 <= stream_bytes <= _nbytes(stream):
+        raise ValueError(f"stream_bytes {stream_bytes} outside the stream tensor ({_nbytes(stream)} bytes)")
+    return int(stream_bytes)
+
+
+def _out_values(out: torch.Tensor, n: int, flat) -> torch.Tensor:
+    """A caller-given output of n values (``flat`` checks the element size)."""
+    o = flat(out)
+    if o.numel() < n:
+        raise ValueError(f"out: holds {o.numel()} values, needs {n}")
+    return o
+
+
 def load():
     return _lib.load()
 
@@ -58,7 +108,7 @@ def calibrate(sample: torch.Tensor, codebook: torch.Tensor | None = None) -> tor
     """Top-16 codebook from the exponent histogram of ``sample`` (offline
     calibration, SplitZip §3.3). Returns the 4096-byte device codebook."""
     s = _flat16(sample)
-    cb = new_codebook(s.device) if codebook is None else codebook
+    cb = new_codebook(s.device) if codebook is None else _cb(codebook)
     check(load().uzip_calibrate(_p(s), s.numel(), _p(cb), _sp(s.device)), "uzip_calibrate")
     return cb
 
@@ -68,7 +118,7 @@ def codebook_from_exps(exps, device="cuda", codebook: torch.Tensor | None = None
     if len(vals) != 16:
         raise ValueError("need 16 exponents")
     arr = (ctypes.c_uint8 * 16)(*vals)
-    cb = new_codebook(device) if codebook is None else codebook
+    cb = new_codebook(device) if codebook is None else _cb(codebook)
     check(load().uzip_codebook_from_exps(arr, _p(cb), _sp(cb.device)), "uzip_codebook_from_exps")
     return cb
 
@@ -112,8 +162,8 @@ def encode(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, out: torc
         workspace = torch.empty(max(16, workspace_bytes(n, chunk)), dtype=torch.uint8, device=v.device)
     nbytes = ctypes.c_size_t(0)
     L = load()
-    args = (_p(v), n, chunk, _p(codebook), _p(out), out.numel(), _p(workspace), workspace.numel(),
-            ctypes.byref(nbytes) if sync else None)
+    args = (_p(v), n, chunk, _p(_cb(codebook)), _p(_dev(out, "out")), _nbytes(out),
+            _p(_dev(workspace, "workspace")), _nbytes(workspace), ctypes.byref(nbytes) if sync else None)
     check(L.uzip_encode(*args, _sp(v.device)), "uzip_encode")
     return out, (nbytes.value if sync else None)
 
@@ -124,14 +174,14 @@ def encode_dynamic(x: torch.Tensor, chunk: int = 1024, codebook: torch.Tensor | 
     Table 7). Returns ``(stream, nbytes, codebook)``."""
     v = _flat16(x)
     n = v.numel()
-    cb = new_codebook(v.device) if codebook is None else codebook
+    cb = new_codebook(v.device) if codebook is None else _cb(codebook)
     if out is None:
         out = torch.empty(max_compressed_size(n, chunk), dtype=torch.uint8, device=v.device)
     if workspace is None:
         workspace = torch.empty(max(16, workspace_bytes(n, chunk)), dtype=torch.uint8, device=v.device)
     nbytes = ctypes.c_size_t(0)
-    args = (_p(v), n, chunk, _p(cb), _p(out), out.numel(), _p(workspace), workspace.numel(),
-            ctypes.byref(nbytes) if sync else None)
+    args = (_p(v), n, chunk, _p(cb), _p(_dev(out, "out")), _nbytes(out), _p(_dev(workspace, "workspace")),
+            _nbytes(workspace), ctypes.byref(nbytes) if sync else None)
     check(load().uzip_encode_dynamic(*args, _sp(v.device)), "uzip_encode_dynamic")
     return out, (nbytes.value if sync else None), cb
 
@@ -142,9 +192,9 @@ def decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = None, status
     land in ``status`` (a 1-element int32 CUDA tensor) when given."""
     if out is None:
         out = torch.empty(n, dtype=dtype, device=stream.device)
-    o = _flat16(out) if n else out
-    nb = stream.numel() if stream_bytes is None else stream_bytes
-    check(load().uzip_decode(_p(stream), nb, _p(o) if n else None, n, _p(status), _sp(stream.device)),
+    o = _out_values(out, n, _flat16) if n else out
+    nb = _stream_nbytes(stream, stream_bytes)
+    check(load().uzip_decode(_p(stream), nb, _p(o) if n else None, n, _status(status), _sp(stream.device)),
           "uzip_decode")
     return out
 
@@ -155,7 +205,15 @@ def stream_copy(src: torch.Tensor, dst: torch.Tensor, capacity: int | None = Non
     ``dst``; either may be pinned host memory. ``copied`` (one int64 element,
     device or pinned host) receives the byte count. Asynchronous on ``stream``
     (default: the current stream of the device)."""
-    cap = min(src.numel(), dst.numel()) if capacity is None else capacity
+    for t, what in ((src, "src"), (dst, "dst")):
+        if not t.is_contiguous():
+            raise ValueError(f"{what}: expected a contiguous tensor")
+    room = min(_nbytes(src), _nbytes(dst))
+    cap = room if capacity is None else int(capacity)
+    if not 0 <= cap <= room:
+        raise ValueError(f"capacity {cap} beyond src or dst ({room} bytes)")
+    if copied is not None and (copied.dtype != torch.int64 or copied.numel() < 1 or not copied.is_contiguous()):
+        raise ValueError("copied: expected a contiguous int64 tensor of one element")
     dev = src.device if src.is_cuda else dst.device
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     check(load().uzip_stream_copy(_p(src), _p(dst), cap, _p(copied), ctypes.c_void_p(s.cuda_stream)),
@@ -164,7 +222,7 @@ def stream_copy(src: torch.Tensor, dst: torch.Tensor, capacity: int | None = Non
 
 def stream_info(stream: torch.Tensor, stream_bytes: int | None = None) -> dict:
     info = _lib.Info()
-    nb = stream.numel() if stream_bytes is None else stream_bytes
+    nb = _stream_nbytes(stream, stream_bytes)
     rc = load().uzip_stream_info(_p(stream), nb, ctypes.byref(info), _sp(stream.device))
     d = {f: getattr(info, f) for f, _ in _lib.Info._fields_ if f != "exps"}
     d["exps"] = list(info.exps)
@@ -200,7 +258,7 @@ def _flat8(x: torch.Tensor) -> torch.Tensor:
 def e5m2_calibrate(sample: torch.Tensor, codebook: torch.Tensor | None = None) -> torch.Tensor:
     """Codebook from E5M2 values (SplitZip §4.2 / appendix C)."""
     s = _flat8(sample)
-    cb = new_codebook(s.device) if codebook is None else codebook
+    cb = new_codebook(s.device) if codebook is None else _cb(codebook)
     check(load().uzip_e5m2_calibrate(_p(s), s.numel(), _p(cb), _sp(s.device)), "uzip_e5m2_calibrate")
     return cb
 
@@ -219,8 +277,8 @@ def e5m2_encode(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, out:
     if workspace is None:
         workspace = torch.empty(max(16, workspace_bytes(n, chunk)), dtype=torch.uint8, device=v.device)
     nbytes = ctypes.c_size_t(0)
-    args = (_p(v), n, chunk, _p(codebook), _p(out), out.numel(), _p(workspace), workspace.numel(),
-            ctypes.byref(nbytes) if sync else None)
+    args = (_p(v), n, chunk, _p(_cb(codebook)), _p(_dev(out, "out")), _nbytes(out),
+            _p(_dev(workspace, "workspace")), _nbytes(workspace), ctypes.byref(nbytes) if sync else None)
     check(load().uzip_e5m2_encode(*args, _sp(v.device)), "uzip_e5m2_encode")
     return out, (nbytes.value if sync else None)
 
@@ -230,9 +288,9 @@ def e5m2_decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = None, s
     """Decode an E5M2 stream into ``n`` bytes (uint8 bit patterns)."""
     if out is None:
         out = torch.empty(max(n, 1), dtype=torch.uint8, device=stream.device)[:n]
-    o = _flat8(out) if n else out
-    nb = stream.numel() if stream_bytes is None else stream_bytes
-    check(load().uzip_e5m2_decode(_p(stream), nb, _p(o) if n else None, n, _p(status), _sp(stream.device)),
+    o = _out_values(out, n, _flat8) if n else out
+    nb = _stream_nbytes(stream, stream_bytes)
+    check(load().uzip_e5m2_decode(_p(stream), nb, _p(o) if n else None, n, _status(status), _sp(stream.device)),
           "uzip_e5m2_decode")
     return out
 
@@ -242,7 +300,7 @@ def e5m2_decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = None, s
 def make_sentinel(codebook: torch.Tensor) -> torch.Tensor:
     """Turn a codebook into the Top-15 + sentinel codebook of its first 15
     exponents, in place (SplitZip §3.4, Table 6)."""
-    check(load().uzip_codebook_make_sentinel(_p(codebook), _sp(codebook.device)), "uzip_codebook_make_sentinel")
+    check(load().uzip_codebook_make_sentinel(_p(_cb(codebook)), _sp(codebook.device)), "uzip_codebook_make_sentinel")
     return codebook
 
 
@@ -260,8 +318,8 @@ def sentinel_encode(x: torch.Tensor, codebook: torch.Tensor, chunk: int = 1024, 
     if workspace is None:
         workspace = torch.empty(max(16, workspace_bytes(n, chunk)), dtype=torch.uint8, device=v.device)
     nbytes = ctypes.c_size_t(0)
-    args = (_p(v), n, chunk, _p(codebook), _p(out), out.numel(), _p(workspace), workspace.numel(),
-            ctypes.byref(nbytes) if sync else None)
+    args = (_p(v), n, chunk, _p(_cb(codebook)), _p(_dev(out, "out")), _nbytes(out),
+            _p(_dev(workspace, "workspace")), _nbytes(workspace), ctypes.byref(nbytes) if sync else None)
     check(load().uzip_sentinel_encode(*args, _sp(v.device)), "uzip_sentinel_encode")
     return out, (nbytes.value if sync else None)
 
@@ -271,8 +329,9 @@ def sentinel_decode(stream: torch.Tensor, n: int, out: torch.Tensor | None = Non
     """Decode a Top-15 + sentinel stream into ``n`` BF16 values."""
     if out is None:
         out = torch.empty(max(n, 1), dtype=torch.bfloat16, device=stream.device)[:n]
-    o = _flat16(out) if n else out
-    nb = stream.numel() if stream_bytes is None else stream_bytes
-    check(load().uzip_sentinel_decode(_p(stream), nb, _p(o) if n else None, n, _p(status), _sp(stream.device)),
+    o = _out_values(out, n, _flat16) if n else out
+    nb = _stream_nbytes(stream, stream_bytes)
+    check(load().uzip_sentinel_decode(_p(stream), nb, _p(o) if n else None, n, _status(status),
+                                      _sp(stream.device)),
           "uzip_sentinel_decode")
     return out

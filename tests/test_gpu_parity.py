@@ -25,8 +25,10 @@ def u16(x):
 
 
 def check_codebook(uz, orc, cb, sample_u16):
-    exps = np.array(uz.codebook_exps(cb), np.uint8)
-    assert exps.tolist() == orc.calibrate(sample_u16).tolist()
+    """The GPU codebook against the oracle's; returns the oracle's exponents
+    (the oracle's inputs never come from the CUDA path)."""
+    exps = orc.calibrate(sample_u16)
+    assert uz.codebook_exps(cb) == exps.tolist()
     assert uz.codebook_histogram(cb) == [int(v) for v in orc.histogram(sample_u16)]
     enc, dec, esc = orc.luts(exps)
     host = cb.cpu().numpy()

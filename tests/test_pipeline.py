@@ -40,7 +40,8 @@ def test_b_hide_and_model():
 def test_pipeline_round_trip_and_piece_streams(uz, orc, link):
     x, s = W.workload(1, device="cuda")  # 1,048,576 values
     cb = uz.calibrate(s)
-    exps = np.array(uz.codebook_exps(cb), np.uint8)
+    exps = orc.calibrate(W.as_u16(s))
+    assert uz.codebook_exps(cb) == exps.tolist()
     y, tr = PL.send_compressed(x, cb, chunk=1024, pieces=6, link=link)
     assert torch.equal(y.view(torch.int16), x.view(torch.int16))
     xh = W.as_u16(x)
@@ -92,6 +93,7 @@ def test_stream_copy_refuses_non_streams(uz):
     assert int(copied.item()) == 0 and torch.all(dst == 7)
     x = torch.randn(10_000, device="cuda").bfloat16()
     stream, nbytes = uz.encode(x, uz.calibrate(x), 1024)
+    dst = torch.full((stream.numel(),), 7, dtype=torch.uint8, device="cuda")
     uz.stream_copy(stream, dst, nbytes - 1, copied=copied)  # capacity below the stream's total
     torch.cuda.synchronize()
     assert int(copied.item()) == 0 and torch.all(dst == 7)
