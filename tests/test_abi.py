@@ -7,7 +7,6 @@ import re
 
 import pytest
 
-import oracle
 from lossless_bf16_exponent_gb300 import _lib, build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
