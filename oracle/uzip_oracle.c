@@ -37,6 +37,9 @@
  *     starts at byte 3 * offsets[c] of the escape section, where offsets[] is
  *     the exclusive prefix sum of the per-chunk escape counts (u32, nc + 1
  *     entries, offsets[nc] = M);
+ *   - so a decoder accepts only offsets that rise from 0 to M and blocks whose
+ *     positions lie inside their chunk and rise strictly (one entry per
+ *     escape: a repeated or falling position is not a stream of this format);
  *   - the stream is: a 64-byte header, then the sign-mantissa bytes, the packed
  *     codes, the chunk offsets and the escape blocks, each of the first four
  *     parts padded with zero bytes to a multiple of 16 bytes.
@@ -314,6 +317,9 @@ int orc_decode(const uint8_t *in, uint64_t in_bytes, uint16_t *x, uint64_t n)
         for (uint64_t j = 0; j < k; j++) {
             uint64_t pos = get_u16(block + 2 * j);
             if (pos >= len) return ORC_ERR_CORRUPT;
+            /* Escapes are stored in ascending element order, one entry each:
+             * a position that does not rise past the one before is corrupt. */
+            if (j > 0 && pos <= get_u16(block + 2 * (j - 1))) return ORC_ERR_CORRUPT;
             x[start + pos] = rebuild(A[start + pos], block[2 * k + j]);
         }
     }
@@ -503,6 +509,7 @@ int orc_e5m2_decode(const uint8_t *in, uint64_t in_bytes, uint8_t *x, uint64_t n
         for (uint64_t j = 0; j < k; j++) {
             uint64_t pos = get_u16(block + 2 * j);
             if (pos >= len) return ORC_ERR_CORRUPT;
+            if (j > 0 && pos <= get_u16(block + 2 * (j - 1))) return ORC_ERR_CORRUPT; /* ascending, as for BF16 */
             x[start + pos] = (uint8_t)((x[start + pos] & 0x83) | ((block[2 * k + j] & 0x1F) << 2));
         }
     }

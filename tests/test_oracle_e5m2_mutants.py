@@ -30,6 +30,10 @@ MUTANTS = {
     "escape fix-up keeps the old exponent": ("x[start + pos] = (uint8_t)((x[start + pos] & 0x83) | ((block[2 * k + j] & 0x1F) << 2));",
                                              "x[start + pos] = (uint8_t)(x[start + pos] | ((block[2 * k + j] & 0x1F) << 2));"),
     "magic": ('memcpy(out, "UZE1", 4);', 'memcpy(out, "UZP1", 4);'),
+    "repeated positions accepted": ("if (j > 0 && pos <= get_u16(block + 2 * (j - 1))) return ORC_ERR_CORRUPT;",
+                                    "if (j > 0 && pos < get_u16(block + 2 * (j - 1))) return ORC_ERR_CORRUPT;"),
+    "offsets not checked": ("if (get_u32(C) != 0 || get_u32(C + 4 * nc) != m) return ORC_ERR_CORRUPT;",
+                            "if (get_u32(C) > m) return ORC_ERR_CORRUPT;"),
 }
 
 BATTERY = r"""

@@ -198,6 +198,13 @@ def test_corrupt_streams_are_refused(orc):
     bad = good.copy()
     bad[112] = 9  # escape position past its chunk of 8
     assert orc.e5m2_decode(bad, x.size)[0] == oracle.ERR_CORRUPT
+    # offsets (at 96) must run from 0 to M; chunk 0's positions (4, 5 at 112)
+    # must rise strictly, one entry per escape
+    for edits in ({96: 1}, {104: 2}, {114: 4}, {112: 5, 114: 4}):
+        bad = good.copy()
+        for k, v in edits.items():
+            bad[k] = v
+        assert orc.e5m2_decode(bad, x.size)[0] == oracle.ERR_CORRUPT, edits
     assert orc.e5m2_decode(good, x.size - 1)[0] == oracle.ERR_CORRUPT
     # a BF16 stream is not an E5M2 stream
     assert orc.e5m2_decode(orc.encode(np.zeros(10, np.uint16), np.arange(16), 8)[1], 10)[0] == oracle.ERR_CORRUPT

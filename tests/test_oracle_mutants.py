@@ -33,6 +33,14 @@ MUTANTS = {
                               "x[start + pos] = x[start + pos];"),
     "section padding": ("return (v + 15) / 16 * 16;", "return (v + 7) / 8 * 8;"),
     "chunk count": ("L.nc = (n + chunk - 1) / chunk;", "L.nc = n / chunk + 1;"),
+    "first offset not checked": ("if (get_u32(C) != 0 || get_u32(C + 4 * nc) != m) return ORC_ERR_CORRUPT;",
+                                 "if (get_u32(C + 4 * nc) != m) return ORC_ERR_CORRUPT;"),
+    "last offset not checked": ("if (get_u32(C) != 0 || get_u32(C + 4 * nc) != m) return ORC_ERR_CORRUPT;",
+                                "if (get_u32(C) != 0) return ORC_ERR_CORRUPT;"),
+    "repeated positions accepted": ("if (j > 0 && pos <= get_u16(block + 2 * (j - 1))) return ORC_ERR_CORRUPT;",
+                                    "if (j > 0 && pos < get_u16(block + 2 * (j - 1))) return ORC_ERR_CORRUPT;"),
+    "falling positions accepted": ("if (j > 0 && pos <= get_u16(block + 2 * (j - 1))) return ORC_ERR_CORRUPT;",
+                                   "if (j > 0 && pos == get_u16(block + 2 * (j - 1))) return ORC_ERR_CORRUPT;"),
 }
 
 BATTERY = r"""
@@ -55,6 +63,7 @@ checks = [
     lambda: pins.test_brute_force_tiny_inputs(o, 1024),
     lambda: pins.test_all_patterns_tensor(o),
     lambda: pins.test_all_zero_reaches_four_thirds(o),
+    lambda: pins.test_decode_rejects_corrupt_streams(o),
 ]
 failed = []
 for i, c in enumerate(checks):

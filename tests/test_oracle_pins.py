@@ -364,6 +364,36 @@ def test_decode_rejects_corrupt_streams(orc):
     off_d = off_c + pad16(4 * (nc + 1))
     bad = s.copy(); bad[off_d:off_d + 2] = [0xFF, 0xFF]
     assert orc.decode(bad, 1000)[0] == oracle.ERR_CORRUPT         # position outside chunk
+    offs = s[off_c:off_c + 4 * (nc + 1)].view("<u4").astype(np.int64)
+    # Offsets must run from 0 to M. Two streams that break only that rule:
+    # one escape slot more in the header (M + 1, total + 3) with three spare
+    # bytes before every block and all offsets raised by one (offsets[0] = 1),
+    # or after the last block with the offsets unchanged (offsets[nc] = M).
+    def grown(offsets, lead):
+        m1 = int(offs[nc]) + 1
+        g = np.concatenate([s[:off_d], np.zeros(3, np.uint8) if lead else s[off_d:],
+                            s[off_d:] if lead else np.zeros(3, np.uint8)])
+        g[24:32] = np.frombuffer(np.uint64(m1).tobytes(), np.uint8)
+        g[48:56] = np.frombuffer(np.uint64(g.size).tobytes(), np.uint8)
+        g[off_c:off_c + 4 * (nc + 1)] = np.frombuffer(offsets.astype("<u4").tobytes(), np.uint8)
+        return g
+    assert orc.decode(grown(offs + 1, True), 1000)[0] == oracle.ERR_CORRUPT   # offsets[0] != 0
+    assert orc.decode(grown(offs, False), 1000)[0] == oracle.ERR_CORRUPT      # offsets[nc] != M
+    # Chunk 2's block: its first two positions made equal, then swapped.
+    # Escapes are stored one per entry in ascending order: neither is a stream.
+    blk = off_d + 3 * int(offs[2])
+    assert offs[3] - offs[2] >= 2
+    p0, p1 = bytes(s[blk:blk + 2]), bytes(s[blk + 2:blk + 4])
+    assert int.from_bytes(p0, "little") < int.from_bytes(p1, "little")
+    bad = s.copy(); bad[blk + 2:blk + 4] = list(p0)
+    assert orc.decode(bad, 1000)[0] == oracle.ERR_CORRUPT         # repeated position
+    bad = s.copy(); bad[blk:blk + 2] = list(p1); bad[blk + 2:blk + 4] = list(p0)
+    assert orc.decode(bad, 1000)[0] == oracle.ERR_CORRUPT         # falling positions
+    # Damage that leaves a valid stream is accepted: a code byte changes a
+    # value but breaks no rule of the format.
+    off_b = 64 + pad16(1000)
+    bad = s.copy(); bad[off_b + 7] ^= 0x11
+    assert orc.decode(bad, 1000)[0] == oracle.OK
 
 
 # ------------------------------------------------------------ plausibility
