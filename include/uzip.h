@@ -174,9 +174,11 @@ UZIP_API int uzip_encode(const void *d_in_bf16, size_t n, uint32_t chunk, const 
  *   The workspace is a device array built into the library, sized for at most
  *   UZIP_NOALLOC_MAX_N values (about 8.1 MiB, held on every GPU that loads the
  *   library until the process exits); n above that returns UZIP_ERR_CAPACITY
- *   before any CUDA call. Nothing is allocated: the first call on a device
- *   looks up the array's address with that device current (make that first
- *   call before any stream capture). All calls share the one array; the call
+ *   before any CUDA call. Nothing is allocated: each call looks up the
+ *   array's address for the device and context current at the call (so a
+ *   cudaDeviceReset between calls is harmless); the first call on a device
+ *   may load the library's device code, so make it before any stream
+ *   capture. All calls share the one array; the call
  *   clears what must start at zero, but calls that overlap on the GPU (other
  *   streams, other host threads) race on it and corrupt each other's output,
  *   so serialise them. Arguments, output and errors are otherwise those of
@@ -206,10 +208,14 @@ UZIP_API int uzip_encode_dynamic(const void *d_in_bf16, size_t n, uint32_t chunk
  *                  error code. The kernel checks the header (magic, version,
  *                  status flags, n, chunk, nc, M, total <= stream_bytes) before
  *                  it writes any output; with a bad header it writes no output
- *                  and stores UZIP_ERR_CORRUPT. Escape entries that point
- *                  outside their chunk or offsets that do not rise are skipped
- *                  and also give UZIP_ERR_CORRUPT (the output is then not
- *                  trustworthy). No read or write leaves the buffers.
+ *                  and stores UZIP_ERR_CORRUPT. The rest of the stream must
+ *                  follow the format: offsets[0] = 0, offsets[nc] = M, the
+ *                  offsets rising, no chunk holding more escapes than values,
+ *                  and in each block positions inside the chunk that rise
+ *                  strictly (one entry per escape). A stream that breaks any
+ *                  of these also gives UZIP_ERR_CORRUPT (its output is then
+ *                  not trustworthy); a stream that keeps every rule is
+ *                  accepted. No read or write leaves the buffers.
  * Returns host-detected errors only (UZIP_ERR_ARG, UZIP_ERR_ALIGN,
  * UZIP_ERR_CAPACITY if stream_bytes < 64, UZIP_ERR_CUDA). Async. */
 UZIP_API int uzip_decode(const void *d_stream, size_t stream_bytes, void *d_out_bf16, size_t n,

@@ -17,8 +17,10 @@
 //   3. each group is decoded with the 16-byte decode table held in four
 //      registers and selected by byte permutes (three PRMTs per four values),
 //      escapes are patched from shared memory, and 16 bytes are stored.
-// The header is validated by every CTA before any output is written; escape
-// data that point outside their chunk are skipped and reported.
+// The header is validated by every CTA before any output is written. The
+// rest of a stream is checked as the oracle checks it: offsets that do not
+// run from 0 to M or do not rise, and blocks whose positions leave their
+// chunk or do not rise strictly, are skipped and reported as corrupt.
 #include <algorithm>
 
 #include <atomic>
@@ -84,6 +86,21 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
     return v;
 }
 
+// The stream's offsets must run from 0 (offsets[0]) to M (offsets[nc]); that
+// they rise is checked chunk by chunk where each block is walked.
+__device__ __forceinline__ bool offsets_span_ok(const uint8_t* C, uint64_t nc, uint64_t m) {
+    return ld_u32_le(C) == 0 && ld_u32_le(C + 4 * nc) == m;
+}
+
+// Escape positions of a chunk's block rise strictly (one entry per escape,
+// ascending). Lane l holds entry j0 + l; its predecessor's position comes from
+// lane l - 1, or for lane 0 from `last` (entry j0 - 1, the previous step's
+// lane 31). Every lane of the warp must call it.
+__device__ __forceinline__ uint32_t rising_prev(uint32_t pos, uint32_t last, uint32_t lane) {
+    const uint32_t up = __shfl_up_sync(0xffffffffu, pos, 1);
+    return lane == 0 ? last : up;
+}
+
 __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(const Params p) {
     static_assert(kGroupsPerThread == 4, "one 32-bit escape word per thread");
     // escape bitmap, double-buffered by tile parity: word w holds the four groups w + r * threads, bit
@@ -122,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
     const uint32_t tiles = (uint32_t)(((uint64_t)n32 + kTile - 1) / kTile);
 
     s_mask[0][tid] = 0;
-    if (tid == 0) s_bad = 0;
+    if (tid == 0) s_bad = blockIdx.x == 0 && !offsets_span_ok(C, nc, m);
     __syncthreads();
 
     int par = 0;
@@ -164,9 +181,14 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
             }
             const uint32_t k = o1 - o;
             const uint8_t* blk = D + 3ull * o;
-            for (uint32_t j = lane; j < k; j += 32) {
-                const uint32_t pos = (uint32_t)blk[2 * j] | ((uint32_t)blk[2 * j + 1] << 8);
-                if (pos >= clen) {
+            uint32_t last = 0;  // position of entry j0 - 1 (read only when j0 > 0)
+            for (uint32_t j0 = 0; j0 < k; j0 += 32) {  // uniform across the warp
+                const uint32_t j = j0 + lane;
+                const uint32_t pos = j < k ? (uint32_t)blk[2 * j] | ((uint32_t)blk[2 * j + 1] << 8) : 0u;
+                const uint32_t prev = rising_prev(pos, last, lane);
+                last = __shfl_sync(0xffffffffu, pos, 31);
+                if (j >= k) continue;
+                if (pos >= clen || (j > 0 && pos <= prev)) {
                     bad = true;
                     continue;
                 }
@@ -275,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
     const uint32_t tiles = (uint32_t)(((uint64_t)n32 + kE5Tile - 1) / kE5Tile);
 
     for (uint32_t i = tid; i < kE5Tile / 32; i += kThreads) s_mask[0][i] = 0;
-    if (tid == 0) s_bad = 0;
+    if (tid == 0) s_bad = blockIdx.x == 0 && !offsets_span_ok(C, nc, m);
     __syncthreads();
 
     int par = 0;
@@ -313,9 +335,14 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
             }
             const uint32_t k = o1 - o;
             const uint8_t* blk = D + 3ull * o;
-            for (uint32_t jj = lane; jj < k; jj += 32) {
-                const uint32_t pos = (uint32_t)blk[2 * jj] | ((uint32_t)blk[2 * jj + 1] << 8);
-                if (pos >= clen) {
+            uint32_t last = 0;
+            for (uint32_t j0 = 0; j0 < k; j0 += 32) {  // uniform across the warp
+                const uint32_t jj = j0 + lane;
+                const uint32_t pos = jj < k ? (uint32_t)blk[2 * jj] | ((uint32_t)blk[2 * jj + 1] << 8) : 0u;
+                const uint32_t prev = rising_prev(pos, last, lane);
+                last = __shfl_sync(0xffffffffu, pos, 31);
+                if (jj >= k) continue;
+                if (pos >= clen || (jj > 0 && pos <= prev)) {
                     bad = true;
                     continue;
                 }
