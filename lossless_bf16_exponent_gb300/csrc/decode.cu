@@ -65,6 +65,12 @@ __device__ __forceinline__ void lookup8(uint32_t cw, uint32_t d0, uint32_t d1, u
     e_hi = prmt(prmt(d0, d1, sel_hi), prmt(d2, d3, sel_hi), pick_hi);
 }
 
+// Four flag bits -> four byte masks (bit i set -> byte i = 0xFF): the four
+// shifted copies of the multiply never overlap, and bit i lands at 8 i.
+__device__ __forceinline__ uint32_t byte_mask4(uint32_t bits4) {
+    return ((bits4 * 0x00204081u) & 0x01010101u) * 0xFFu;
+}
+
 // Four exponent bytes + four sign-mantissa bytes -> four BF16 values.
 __device__ __forceinline__ uint2 rebuild4(uint32_t e4, uint32_t a4) {
     const uint32_t hi = (a4 & 0x80808080u) | ((e4 >> 1) & 0x7F7F7F7Fu);  // sign | exponent bits 7..1
@@ -106,7 +112,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
     // escape bitmap, double-buffered by tile parity: word w holds the four groups w + r * threads, bit
     // 8 r + i for value i of group r, so each thread reads one word per tile
     __shared__ uint32_t s_mask[2][kThreads];
-    __shared__ uint8_t s_val[kTile];
+    __shared__ __align__(16) uint8_t s_val[kTile];
     __shared__ int s_bad;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -213,16 +219,11 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
             uint32_t e_lo, e_hi;
             lookup8(cv[r], d0, d1, d2, d3, e_lo, e_hi);
             const uint32_t fix = (fix_all >> (8 * r)) & 0xFF;
-            if (fix) {
-#pragma unroll
-                for (int i = 0; i < 8; i++) {
-                    if (fix & (1u << i)) {
-                        const uint32_t sh = 8 * (i & 3);
-                        const uint32_t v = (uint32_t)s_val[8 * g + i] << sh;
-                        if (i < 4) e_lo = (e_lo & ~(0xFFu << sh)) | v;
-                        else e_hi = (e_hi & ~(0xFFu << sh)) | v;
-                    }
-                }
+            if (fix) {  // the group's eight patch bytes at once; only the flagged ones are taken
+                const uint2 sv = *reinterpret_cast<const uint2*>(s_val + 8 * g);
+                const uint32_t m_lo = byte_mask4(fix & 0xF), m_hi = byte_mask4(fix >> 4);
+                e_lo = (e_lo & ~m_lo) | (sv.x & m_lo);
+                e_hi = (e_hi & ~m_hi) | (sv.y & m_hi);
             }
             const uint2 lo = rebuild4(e_lo, av[r].x);
             const uint2 hi = rebuild4(e_hi, av[r].y);
@@ -265,7 +266,7 @@ constexpr uint32_t kE5Tile = kThreads * 32 * kE5Slots;
 
 __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_kernel(const Params p) {
     __shared__ uint32_t s_mask[2][kE5Tile / 32];
-    __shared__ uint8_t s_val[kE5Tile];
+    __shared__ __align__(16) uint8_t s_val[kE5Tile];
     __shared__ int s_bad;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -375,13 +376,10 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
                 for (int hh = 0; hh < 2; hh++) {
                     uint32_t e4 = e8[hh];
                     const uint32_t bits = (fix >> (8 * q + 4 * hh)) & 0xF;
-                    if (bits) {
-#pragma unroll
-                        for (int i = 0; i < 4; i++)
-                            if (bits & (1u << i)) {
-                                const uint32_t sh = 8 * i;
-                                e4 = (e4 & ~(0xFFu << sh)) | ((uint32_t)s_val[v0 + 8 * q + 4 * hh + i] << sh);
-                            }
+                    if (bits) {  // four patch bytes at once; only the flagged ones are taken
+                        const uint32_t sv = *reinterpret_cast<const uint32_t*>(s_val + v0 + 8 * q + 4 * hh);
+                        const uint32_t mk = byte_mask4(bits);
+                        e4 = (e4 & ~mk) | (sv & mk);
                     }
                     const uint32_t a4 = spread_fields4((g24[q] >> (12 * hh)) & 0xFFF);
                     o[2 * q + hh] = ((a4 * 32u) & 0x80808080u) | ((e4 * 4u) & 0x7C7C7C7Cu) | (a4 & 0x03030303u);
