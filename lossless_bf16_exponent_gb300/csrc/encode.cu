@@ -1059,6 +1059,23 @@ size_t escape_smem(uint32_t range_chunks, int rounds) {
     return (size_t)kWarps * (kStageBytes + 4ull * rounds * kHeadEntries * 32 + 4ull * (range_chunks + 1));
 }
 
+// Let both escape-kernel variants take their largest dynamic shared memory.
+// A function attribute belongs to the current context, which a
+// cudaDeviceReset replaces, so it is set again before every launch that
+// needs it (a host-side call, no device work).
+cudaError_t allow_escape_smem() {
+    void (*esc[2])(Params) = {encode_escape_kernel<1>, encode_escape_kernel<2>};
+    for (int k = 0; k < 2; k++) {
+        const size_t smem_max = escape_smem(kMaxRangeChunks, k + 1);
+        if (smem_max > 48 * 1024) {
+            const cudaError_t e =
+                cudaFuncSetAttribute(esc[k], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
+}
+
 int device_facts(DeviceFacts& f) {
     int dev = 0;
     UZIP_CUDA_TRY(cudaGetDevice(&dev));
@@ -1070,12 +1087,7 @@ int device_facts(DeviceFacts& f) {
     UZIP_CUDA_TRY(cudaDeviceGetAttribute(&f.sms, cudaDevAttrMultiProcessorCount, dev));
     UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm1, encode_dense_kernel, kThreads, 0));
     UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm1e, encode_dense_e5m2_kernel, kThreads, 0));
-    void (*esc[2])(Params) = {encode_escape_kernel<1>, encode_escape_kernel<2>};
-    for (int k = 0; k < 2; k++) {
-        const size_t smem_max = escape_smem(kMaxRangeChunks, k + 1);
-        if (smem_max > 48 * 1024)
-            UZIP_CUDA_TRY(cudaFuncSetAttribute(esc[k], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_max));
-    }
+    UZIP_CUDA_TRY(allow_escape_smem());
     if (f.sms < 1 || f.per_sm1 < 1 || f.per_sm1e < 1) return UZIP_ERR_CUDA;
     if (dev < kMaxFactDevices) {
         g_facts[dev] = f;
@@ -1173,6 +1185,7 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         cfg.gridDim = dim3((unsigned)grid2);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = escape_smem(p.range_chunks, two_rounds + 1);
+        if (cfg.dynamicSmemBytes > 48 * 1024) UZIP_CUDA_TRY(allow_escape_smem());
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1257,9 +1270,11 @@ extern "C" UZIP_API int uzip_encode_dynamic(const void* d_in_bf16, size_t n, uin
 // workspace lives in a file-scope device array, fixed at load time: every GPU
 // that loads this library holds kNoAllocScratchBytes (about 8.1 MiB) of it
 // until the process exits. Host code cannot use the array's name as a device
-// address, so its address is looked up once per device with
-// cudaGetSymbolAddress (on the first call on that device, with the device
-// current) and passed to the same two kernels uzip_encode launches.
+// address, so every call looks the address up with cudaGetSymbolAddress, for
+// the device and context current at the call, and passes it to the same
+// kernels uzip_encode launches. The lookup is not cached: after a
+// cudaDeviceReset, or under another context, the module is loaded again and
+// the array may sit at another address.
 
 namespace uzip {
 namespace {
@@ -1269,9 +1284,6 @@ namespace {
 constexpr uint64_t workspace_bytes_for(uint64_t n) { return geometry_of(n).bytes; }
 
 constexpr uint64_t kNoAllocScratchBytes = workspace_bytes_for(UZIP_NOALLOC_MAX_N);
-
-constexpr int kMaxCachedDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxCachedDevices];
 
 }  // namespace
 }  // namespace uzip
@@ -1285,14 +1297,9 @@ extern "C" UZIP_API int uzip_encode_noalloc(const void* d_in_bf16, size_t n, uin
     if (!chunk_valid(chunk)) return UZIP_ERR_CHUNK;
     const uint64_t need = geometry_of(n).bytes;
     if (need > kNoAllocScratchBytes) return UZIP_ERR_CAPACITY;
-    int dev = 0;
-    UZIP_CUDA_TRY(cudaGetDevice(&dev));
-    void* scratch = dev < kMaxCachedDevices ? g_scratch_addr[dev].load(std::memory_order_acquire) : nullptr;
-    if (!scratch) {
-        UZIP_CUDA_TRY(cudaGetSymbolAddress(&scratch, g_noalloc_scratch));
-        if (!scratch) return UZIP_ERR_CUDA;
-        if (dev < kMaxCachedDevices) g_scratch_addr[dev].store(scratch, std::memory_order_release);
-    }
+    void* scratch = nullptr;
+    UZIP_CUDA_TRY(cudaGetSymbolAddress(&scratch, g_noalloc_scratch));
+    if (!scratch) return UZIP_ERR_CUDA;
     return encode_impl(d_in_bf16, n, chunk, d_codebook, d_out, out_capacity, scratch, (size_t)need, h_out_bytes,
                        stream);
 }

@@ -14,16 +14,16 @@ PKG = os.path.join(ROOT, "lossless_bf16_exponent_gb300")
 CUDA = "/usr/local/cuda"
 
 
-def _build(tmp_path):
+def _build(tmp_path, name="roundtrip"):
     from lossless_bf16_exponent_gb300 import build as B
 
     lib = B.build()
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
-    exe = str(tmp_path / "roundtrip")
+    exe = str(tmp_path / name)
     cmd = [cc, "-O2", "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
-           "-I", os.path.join(CUDA, "include"), os.path.join(ROOT, "tests", "c", "roundtrip.c"), "-o", exe,
+           "-I", os.path.join(CUDA, "include"), os.path.join(ROOT, "tests", "c", name + ".c"), "-o", exe,
            "-L", os.path.dirname(lib), "-luzip", "-L", os.path.join(CUDA, "lib64"), "-lcudart",
            f"-Wl,-rpath,{os.path.dirname(lib)}", f"-Wl,-rpath,{os.path.join(CUDA, 'lib64')}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -33,6 +33,7 @@ def _build(tmp_path):
 
 def test_c_client_compiles_and_links(tmp_path):
     assert os.path.exists(_build(tmp_path))
+    assert os.path.exists(_build(tmp_path, "noalloc_reset"))
 
 
 @pytest.mark.gpu
