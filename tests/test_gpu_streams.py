@@ -1,6 +1,8 @@
-"""Concurrent use: the library keeps no device state between calls, so calls
-on different CUDA streams, each with its own output, workspace and codebook,
-may run at the same time on the GPU. Two tensors are encoded and decoded on
+"""Concurrent use: the entry points that take the caller's buffers keep no
+device state between calls, so calls on different CUDA streams, each with its
+own output, workspace and codebook, may run at the same time on the GPU.
+(uzip_encode_noalloc is the exception: every call shares one built-in scratch
+array, so its calls must be serialised; it is not used here.) Two tensors are encoded and decoded on
 two streams at once; each stream must equal, byte for byte, the stream the
 same call produces alone on the default stream, and each round trip must be
 bit-exact."""
