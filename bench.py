@@ -193,8 +193,54 @@ def profile_traffic(kernel: str):
     return None
 
 
-def cpu_cores_used() -> int:
-    return 1  # the oracle is single-threaded C
+def host_threads() -> int:
+    """Host cores this process may run on (the chunk-parallel oracle uses one
+    thread per core)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
+def chunk_slices(n: int, parts: int, chunk: int = CHUNK):
+    """Cut [0, n) into at most `parts` slices at chunk boundaries."""
+    per = -(-n // parts)
+    per = -(-per // chunk) * chunk
+    return [(a, min(n, a + per)) for a in range(0, n, per)]
+
+
+def oracle_parallel(o, xh, exps, threads: int):
+    """The unchanged oracle on all host cores: the values cut at chunk
+    boundaries into one slice per thread, each slice encoded and decoded as a
+    stream of its own (as the pipeline's pieces are); ctypes releases the GIL
+    for the C calls. Returns the decoded slices (for the check afterwards)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    def work(ab):
+        a, b = ab
+        rc, s = o.encode(xh[a:b], exps, CHUNK)
+        rc2, y = o.decode(s, b - a)
+        assert rc == 0 and rc2 == 0
+        return y
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(work, chunk_slices(xh.size, threads)))
+
+
+def kv_input(args, dev):
+    """The KV-cache workload (tensor, calibration sample): the benchmark's
+    268,435,456 values at --tokens 2048, else a smaller cache of the same law
+    (profiling cases)."""
+    import lossless_bf16_exponent_gb300.workloads as W
+
+    if args.tokens == W.KV_SHAPE[3]:
+        return W.workload(2, device=dev)
+    shape = W.KV_SHAPE[:3] + (args.tokens,) + W.KV_SHAPE[4:]
+    return W.kv_cache(shape, device=dev).reshape(-1), W.kv_cache_sample(device=dev)
+
+
+def kv_label(args, n: int) -> str:
+    return WORKLOAD if n == 268435456 else f"kv_cache tokens={args.tokens} ({n} values), chunk {CHUNK}"
 
 
 # ------------------------------------------------------------ our (GPU) arm
@@ -217,11 +263,7 @@ def run_ours(args):
     barrier()
     uz.load()
 
-    if args.tokens == W.KV_SHAPE[3]:
-        x, sample = W.workload(2, device=dev)
-    else:  # a smaller cache of the same law (profiling cases)
-        shape = W.KV_SHAPE[:3] + (args.tokens,) + W.KV_SHAPE[4:]
-        x, sample = W.kv_cache(shape, device=dev).reshape(-1), W.kv_cache_sample(device=dev)
+    x, sample = kv_input(args, dev)
     n = x.numel()
     raw = 2 * n
     cb = uz.new_codebook(dev)
@@ -262,8 +304,24 @@ def run_ours(args):
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    clocks = sampler.stop() if rank == 0 else {}
     elapsed_ms = t0.elapsed_time(t1)
+    # The timed steps may be over before nvidia-smi samples once: the same
+    # step runs on for --clock-loop seconds more, still sampled, so the clock
+    # record covers these kernels under load (steps and ms_per_step are not
+    # touched).
+    loop_steps = int(args.clock_loop * 1e3 / max(elapsed_ms / args.steps, 1e-3))
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0.record(stream)
+    for _ in range(loop_steps):
+        step()
+    l1.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if rank == 0 else {}
+    if rank == 0 and clocks.get("samples") and loop_steps:
+        loop_ms = l0.elapsed_time(l1) / loop_steps
+        clocks["loaded_loop"] = {"steps": loop_steps, "seconds": round(loop_steps * loop_ms / 1e3, 2),
+                                 "ms_per_step": round(loop_ms, 4),
+                                 "ms_x_sm_mhz": round(loop_ms * clocks["sm_mhz"], 1)}
     cal_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     enc_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
     dec_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
@@ -381,7 +439,7 @@ def report(args, ws, rank, n, raw, nbytes, m, max_ms, total_raw, cal_ms, enc_ms,
         "vs_baseline": None,
         "dtype": "u16",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD if n == 268435456 else f"kv_cache tokens={args.tokens} ({n} values)",
+        "config": {"workload": kv_label(args, n),
                    "step": "calibrate + encode + decode",
                    "l2": "inputs larger than L2 (512 MiB BF16 tensor, 403 MB stream)",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
@@ -410,9 +468,11 @@ def report(args, ws, rank, n, raw, nbytes, m, max_ms, total_raw, cal_ms, enc_ms,
     return line
 
 
-def cpu_baseline(x, sample, budget_s: float = 12.0):
+def cpu_baseline(x, sample, budget_s: float = 8.0):
     """The oracle, as it stands, on the host: calibrate on the sample, encode
-    and decode the whole workload, repeated while the budget lasts."""
+    and decode the whole workload, repeated while the budget lasts -- on all
+    host cores (one chunk-aligned slice per thread, the unchanged oracle in
+    each) and, beside it, on one thread."""
     import numpy as np
 
     import lossless_bf16_exponent_gb300.workloads as W
@@ -420,25 +480,42 @@ def cpu_baseline(x, sample, budget_s: float = 12.0):
 
     o = oracle.Oracle()
     xh, sh = W.as_u16(x), W.as_u16(sample)
-    t_total, raw_total, reps = 0.0, 0, 0
-    while reps < 1 or (t_total < budget_s and reps < 5):
-        t = time.perf_counter()
-        exps = o.calibrate(sh)
-        rc, s = o.encode(xh, exps, CHUNK)
-        rc2, y = o.decode(s, xh.size)
-        t_total += time.perf_counter() - t
-        assert rc == 0 and rc2 == 0 and np.array_equal(y, xh)
-        raw_total += 2 * xh.size
-        reps += 1
-    return {"value": round(raw_total / t_total / 1e9, 4), "unit": "GB/s", "cores": cpu_cores_used(),
-            "kind": "oracle",
-            "sample": f"whole workload ({xh.size} values) x{reps}: calibrate 1 Mi sample + encode + decode, "
-                      f"{t_total:.1f} s"}
+    threads = host_threads()
+
+    def timed(parallel: bool):
+        t_total, raw_total, reps = 0.0, 0, 0
+        while reps < 1 or (t_total < budget_s and reps < 5):
+            t = time.perf_counter()
+            exps = o.calibrate(sh)
+            if parallel:
+                ys = oracle_parallel(o, xh, exps, threads)
+            else:
+                rc, s = o.encode(xh, exps, CHUNK)
+                rc2, y = o.decode(s, xh.size)
+                assert rc == 0 and rc2 == 0
+                ys = [y]
+            t_total += time.perf_counter() - t
+            assert np.array_equal(np.concatenate(ys), xh)
+            raw_total += 2 * xh.size
+            reps += 1
+        return raw_total / t_total / 1e9, reps, t_total
+
+    par, reps_p, t_p = timed(True)
+    one, reps_1, t_1 = timed(False)
+    return {"value": round(par, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"whole workload ({xh.size} values) x{reps_p}: calibrate 1 Mi sample, then encode + "
+                      f"decode of {threads} chunk-aligned slices on {threads} threads, {t_p:.1f} s",
+            "single_thread": {"value": round(one, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"whole workload x{reps_1} on one thread, {t_1:.1f} s"}}
 
 
 # ------------------------------------------------------ reference (oracle) arm
 
 def run_reference(args):
+    """The oracle alone on the host cores (all of them, one chunk-aligned
+    slice per thread), each step calibrating on the sample and encoding and
+    decoding a slice of the workload sized so the whole run stays within
+    about two minutes -- the whole workload when that fits."""
     import numpy as np
     import torch
 
@@ -449,42 +526,44 @@ def run_reference(args):
     if rank != 0:
         return None  # rank 0 alone runs the CPU reference
     o = oracle.Oracle()
+    threads = host_threads()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     x, sample = W.workload(2, device=dev)
     xh, sh = W.as_u16(x), W.as_u16(sample)
     del x
-    # Size each step's slice so the whole run stays within about two minutes.
-    probe = xh[: 1 << 22]
+    probe = xh[: 1 << 24]
     t = time.perf_counter()
-    rc, s = o.encode(probe, o.calibrate(sh), CHUNK)
-    o.decode(s, probe.size)
+    oracle_parallel(o, probe, o.calibrate(sh), threads)
     per_val = (time.perf_counter() - t) / probe.size
     steps_total = args.steps + args.warmup
     n_slice = int(min(xh.size, max(1 << 20, 110.0 / max(steps_total, 1) / per_val)))
-    n_slice -= n_slice % 8192
-    n_slice = max(n_slice, 8192)
+    if n_slice < xh.size:  # a slice of whole chunks, at chunk-aligned offsets
+        n_slice = max(8192, n_slice - n_slice % 8192)
     times = []
     for k in range(steps_total):
-        off = (k * n_slice) % (xh.size - n_slice + 1)
+        off = (k * n_slice) % (xh.size - n_slice + 1) // 8192 * 8192
         sl = xh[off:off + n_slice]
         t = time.perf_counter()
         exps = o.calibrate(sh)
-        rc, s = o.encode(sl, exps, CHUNK)
-        rc2, y = o.decode(s, sl.size)
+        ys = oracle_parallel(o, sl, exps, threads)
         dt = time.perf_counter() - t
-        assert rc == 0 and rc2 == 0 and np.array_equal(y, sl)
+        assert np.array_equal(np.concatenate(ys), sl)
         if k >= args.warmup:
             times.append(dt)
     elapsed = sum(times)
     value = 2 * n_slice * len(times) / elapsed / 1e9
-    sample_txt = (f"slice of {n_slice} values of the workload per step (calibrate 1 Mi sample + encode + "
-                  f"decode), single thread")
+    whole = n_slice == xh.size
+    what = "the whole workload" if whole else f"a slice of {n_slice} of its {xh.size} values"
+    sample_txt = (f"{what} per step (calibrate 1 Mi sample, then encode + decode of {threads} chunk-aligned "
+                  f"slices on {threads} threads)")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed / len(times) * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "step": "calibrate + encode + decode (CPU oracle, bounded slice)"},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cpu_cores_used(), "kind": "oracle",
+        "config": {"workload": WORKLOAD,
+                   "step": "calibrate + encode + decode (CPU oracle, " + ("whole workload" if whole else
+                                                                       "bounded slice") + ")"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample_txt},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -507,7 +586,7 @@ def run_dynamic(args):
     dev = torch.device("cuda", local)
     init_dist("nccl")
     uz.load()
-    x, sample = W.workload(2, device=dev)
+    x, sample = kv_input(args, dev)
     n = x.numel()
     raw = 2 * n
     cb = uz.new_codebook(dev)
@@ -549,7 +628,7 @@ def run_dynamic(args):
         "value": round(raw * ws / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "codebook": "Top-16 of the whole tensor, rebuilt every step"},
+        "config": {"workload": kv_label(args, n), "codebook": "Top-16 of the whole tensor, rebuilt every step"},
         "roofline": {"kernel": "calibrate + encode", "bound": "hbm", "achieved": round(alg / (ms * 1e-3) / 1e9, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(alg / (ms * 1e-3) / 1e9 / peak, 4),
                      "peak_source": peak_src, "algorithmic_bytes": alg},
@@ -578,7 +657,7 @@ def run_pipeline(args):
     dev = torch.device("cuda", local)
     init_dist("nccl")
     uz.load()
-    x, sample = W.workload(2, device=dev)
+    x, sample = kv_input(args, dev)
     n = x.numel()
     raw = 2 * n
     cb = uz.calibrate(sample)
@@ -632,7 +711,7 @@ def run_pipeline(args):
         "mode": "pipeline", "metric": "compressed transfer GB/s (raw BF16 bytes through encode -> link -> decode)",
         "value": links["host"]["compressed_pipeline_gbs"], "unit": "GB/s", "n_gpus": ws, "steps": runs,
         "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "pieces": pieces, "value_link": "host"},
+        "data": "synthetic", "config": {"workload": kv_label(args, n), "pieces": pieces, "value_link": "host"},
         "g_enc_gbs": round(g_enc / 1e9, 1), "g_dec_gbs": round(g_dec / 1e9, 1), "ratio": round(ratio, 5),
         "b_hide_gbs": round(PL.b_hide(g_enc, g_dec, ratio) / 1e9, 1), "links": links,
         "note": ("the stage model assumes independent resources; the host link is one (copy engines over "
@@ -659,7 +738,7 @@ def run_chunks(args):
     dev = torch.device("cuda", local)
     init_dist("nccl")
     uz.load()
-    x, sample = W.workload(2, device=dev)
+    x, sample = kv_input(args, dev)
     n = x.numel()
     raw = 2 * n
     cb = uz.calibrate(sample)
@@ -701,7 +780,7 @@ def run_chunks(args):
     return {"mode": "chunks", "metric": "encode/decode GB/s and ratio vs escape chunk size @256M elems",
             "value": best["decode_gbs_raw"], "unit": "GB/s", "n_gpus": ws, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "value": "decode GB/s at chunk 1024"}, "rows": rows}
+            "config": {"workload": kv_label(args, n), "value": "decode GB/s at chunk 1024"}, "rows": rows}
 
 
 def run_e5m2(args):
@@ -720,7 +799,9 @@ def run_e5m2(args):
     dev = torch.device("cuda", local)
     init_dist("nccl")
     uz.load()
-    x, sample = W.workload_e5m2(device=dev)
+    xb, sb = kv_input(args, dev)  # the KV law, quantised to E5M2 as an FP8 KV cache stores it
+    x, sample = W.to_e5m2_bits(xb), W.to_e5m2_bits(sb)
+    del xb
     n = x.numel()
     cb = uz.e5m2_calibrate(sample)
     out = torch.empty(uz.e5m2_compressed_size(n, n, CHUNK), dtype=torch.uint8, device=dev)
@@ -759,7 +840,7 @@ def run_e5m2(args):
         "value": round(n * ws / (step_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": ws, "steps": reps,
         "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u8", "data": "synthetic",
-        "config": {"workload": "kv_cache [64,2,8,2048,128] quantised to FP8 E5M2 = 268,435,456 values, chunk 1024",
+        "config": {"workload": kv_label(args, n) + ", quantised to FP8 E5M2",
                    "step": "encode + decode"},
         "encode_us": round(te * 1e3, 2), "decode_us": round(td * 1e3, 2),
         "encode_gbs_raw": round(n / (te * 1e-3) / 1e9, 1), "decode_gbs_raw": round(n / (td * 1e-3) / 1e9, 1),
@@ -786,7 +867,7 @@ def run_sentinel(args):
     dev = torch.device("cuda", local)
     init_dist("nccl")
     uz.load()
-    x, sample = W.workload(2, device=dev)
+    x, sample = kv_input(args, dev)
     n = x.numel()
     raw = 2 * n
     cb16 = uz.calibrate(sample)
@@ -842,7 +923,7 @@ def run_sentinel(args):
         "mode": "sentinel", "metric": "Top-15+sentinel vs Top-16 decode GB/s (raw BF16 bytes) and ratio @256M elems",
         "value": s15["decode_gbs_raw"], "unit": "GB/s", "n_gpus": ws, "steps": reps, "warmup": args.warmup,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "value": "Top-15 + sentinel decode GB/s", "peak_gbs": peak,
+        "config": {"workload": kv_label(args, n), "value": "Top-15 + sentinel decode GB/s", "peak_gbs": peak,
                    "peak_source": peak_src},
         "codecs": res,
         "decode_speed_top16_over_sentinel": round(res["top15_sentinel"]["decode_us"] / res["top16"]["decode_us"], 3),
@@ -958,8 +1039,12 @@ def run_workloads(args):
              5: "gradient_like 1G"}
     peak, peak_src = measured_peak()
     res = {}
-    for k in (1, 2, 3, 5):
+    for k in (args.only,) if args.only else (1, 2, 3, 5):
         x, sample = W.workload(k, device=dev)
+        if args.n and k == 3:  # a smaller instance of the law (profiling cases)
+            x = W.heavy_tailed(args.n, device=dev)
+        elif args.n and k == 5:
+            x = W.gradient_like(args.n, device=dev)
         n = x.numel()
         raw = 2 * n
         cb = uz.calibrate(sample)
@@ -987,6 +1072,14 @@ def run_workloads(args):
         torch.cuda.empty_cache()
     if rank != 0:
         return None
+    if args.only:
+        r = res[names[args.only]]
+        return {"mode": "workloads", "metric": "encode/decode GB/s (raw BF16 bytes) and ratio of one workload",
+                "value": round(2 * r["n"] / ((r["encode_us"] + r["decode_us"]) * 1e-6) / 1e9, 1), "unit": "GB/s",
+                "n_gpus": ws, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u16",
+                "data": "synthetic", "config": {"workload": f"{names[args.only]} ({r['n']} values), chunk 1024",
+                                                "peak_gbs": peak, "peak_source": peak_src},
+                "workloads": res}
     g = res[names[5]]
     return {"mode": "workloads", "metric": "encode/decode GB/s (raw BF16 bytes) and ratio per workload",
             "value": round(2 * g["n"] / ((g["encode_us"] + g["decode_us"]) * 1e-6) / 1e9, 1), "unit": "GB/s",
@@ -1013,6 +1106,12 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--tokens", type=int, default=2048,
                     help="tokens of the KV-cache workload (2048 = the benchmark; smaller for profiling)")
+    ap.add_argument("--clock-loop", type=float, default=1.5,
+                    help="seconds of sampled steps after the timed ones, for the clock record (0: none)")
+    ap.add_argument("--only", type=int, choices=[1, 2, 3, 5], default=0,
+                    help="workloads mode: run this workload alone")
+    ap.add_argument("--n", type=int, default=0,
+                    help="workloads mode: values of the heavy-tailed (3) or gradient-like (5) law")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

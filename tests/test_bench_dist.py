@@ -72,7 +72,9 @@ def test_reference_line_shape(monkeypatch):
     args = bench.argparse.Namespace(steps=3, warmup=3)
     line = bench.run_reference(args)
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == bench.host_threads()
+    # the tiny workload fits in a step: the line says it ran the whole of it
+    assert "whole workload" in line["config"]["step"] and "whole workload" in line["cpu_baseline"]["sample"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
     for k in ("metric", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling", "dtype",
               "data", "config"):

@@ -46,3 +46,26 @@ def test_roofline_is_the_slower_op():
         ms = enc_ms if kernel == "encode" else dec_ms
         assert abs(r["achieved"] - (raw + nbytes) / (ms * 1e-3) / 1e9) < 0.1
         assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-3
+
+
+def test_chunk_slices_cover_the_input_at_chunk_boundaries():
+    for n, parts in ((1, 4), (1024, 16), (3 * 1024 + 5, 2), (268435456, 16), (1000003, 72)):
+        sl = bench.chunk_slices(n, parts)
+        assert sl[0][0] == 0 and sl[-1][1] == n and len(sl) <= parts
+        for (a, b), (c, d) in zip(sl, sl[1:]):
+            assert b == c and a % bench.CHUNK == 0 and c % bench.CHUNK == 0 and a < b
+
+
+def test_chunk_parallel_oracle_round_trips():
+    """The all-cores CPU baseline runs the unchanged oracle on chunk-aligned
+    slices in threads; the slices decode back to the input."""
+    import numpy as np
+
+    import oracle
+
+    o = oracle.Oracle()
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(50_000).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    exps = o.calibrate(x[:4096])
+    ys = bench.oracle_parallel(o, x, exps, 4)
+    assert len(ys) == 4 and np.array_equal(np.concatenate(ys), x)
