@@ -244,10 +244,11 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
 
 // ------------------------------------------------------------ FP8 E5M2
 
-// Twelve bits of packed 3-bit fields (four values) -> four bytes, field i in
-// byte i. Fields 0 and 2 move by 0 and 10 bits, fields 1 and 3 by 5 and 15:
-// one multiply for each pair, whose two shifted copies never overlap (so no
-// carries), then a mask keeps the wanted copy of each field.
+// The low twelve bits of packed 3-bit fields (four values) -> four bytes,
+// field i in byte i (higher input bits are ignored). Fields 0 and 2 move by 0
+// and 10 bits, fields 1 and 3 by 5 and 15: one multiply for each pair, whose
+// two shifted copies never overlap (so no carries), then a mask keeps the
+// wanted copy of each field.
 __device__ __forceinline__ uint32_t spread_fields4(uint32_t f12) {
     return (((f12 & 0x1C7u) * 0x401u) & 0x00070007u) | (((f12 & 0xE38u) * 0x8020u) & 0x07000700u);
 }
@@ -294,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
     const uint8_t* C = p.s + L.off_c;
     const uint8_t* D = p.s + L.off_d;
     uint8_t* out8 = reinterpret_cast<uint8_t*>(p.out);
-    const uint32_t d0 = h2.x, d1 = h2.y, d2 = h2.z, d3 = h2.w;
+    // decode table: code k -> its 5-bit exponent already at bits 2..6 of an E5M2 byte
+    const uint32_t d0 = (h2.x << 2) & 0x7C7C7C7Cu, d1 = (h2.y << 2) & 0x7C7C7C7Cu;
+    const uint32_t d2 = (h2.z << 2) & 0x7C7C7C7Cu, d3 = (h2.w << 2) & 0x7C7C7C7Cu;
     const uint32_t tiles = (uint32_t)(((uint64_t)n32 + kE5Tile - 1) / kE5Tile);
 
     for (uint32_t i = tid; i < kE5Tile / 32; i += kThreads) s_mask[0][i] = 0;
@@ -365,24 +368,26 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
             if (v0 >= tlen) continue;
             const uint32_t fix = s_mask[par][sl];
             const uint32_t cw[4] = {cv[j].x, cv[j].y, cv[j].z, cv[j].w};
-            const uint32_t g24[4] = {f[j][0] & 0xFFFFFF, ((f[j][0] >> 24) | (f[j][1] << 8)) & 0xFFFFFF,
-                                     ((f[j][1] >> 16) | (f[j][2] << 16)) & 0xFFFFFF, f[j][2] >> 8};
+            // the 24 field bits of group q start at bit 0 of g24[q]; bits above
+            // 24 are the next group's, which spread_fields4 never reads
+            const uint32_t g24[4] = {f[j][0], (f[j][0] >> 24) | (f[j][1] << 8), (f[j][1] >> 16) | (f[j][2] << 16),
+                                     f[j][2] >> 8};
             uint32_t o[8];
 #pragma unroll
             for (int q = 0; q < 4; q++) {
                 uint32_t e8[2];
                 lookup8(cw[q], d0, d1, d2, d3, e8[0], e8[1]);
+                const uint32_t fq = (fix >> (8 * q)) & 0xFF;
+                if (fq) {  // the group's patch bytes at once; only the flagged ones are taken
+                    const uint2 sv = *reinterpret_cast<const uint2*>(s_val + v0 + 8 * q);
+                    const uint32_t m0 = byte_mask4(fq & 0xF), m1 = byte_mask4(fq >> 4);
+                    e8[0] = (e8[0] & ~m0) | ((sv.x << 2) & 0x7C7C7C7Cu & m0);
+                    e8[1] = (e8[1] & ~m1) | ((sv.y << 2) & 0x7C7C7C7Cu & m1);
+                }
 #pragma unroll
                 for (int hh = 0; hh < 2; hh++) {
-                    uint32_t e4 = e8[hh];
-                    const uint32_t bits = (fix >> (8 * q + 4 * hh)) & 0xF;
-                    if (bits) {  // four patch bytes at once; only the flagged ones are taken
-                        const uint32_t sv = *reinterpret_cast<const uint32_t*>(s_val + v0 + 8 * q + 4 * hh);
-                        const uint32_t mk = byte_mask4(bits);
-                        e4 = (e4 & ~mk) | (sv & mk);
-                    }
-                    const uint32_t a4 = spread_fields4((g24[q] >> (12 * hh)) & 0xFFF);
-                    o[2 * q + hh] = ((a4 * 32u) & 0x80808080u) | ((e4 * 4u) & 0x7C7C7C7Cu) | (a4 & 0x03030303u);
+                    const uint32_t a4 = spread_fields4(hh ? g24[q] >> 12 : g24[q]);
+                    o[2 * q + hh] = ((a4 << 5) & 0x80808080u) | (a4 & 0x03030303u) | e8[hh];
                 }
             }
             const uint32_t ge = e0 + v0;
