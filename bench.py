@@ -176,8 +176,9 @@ def kernel_code_hash(source: str) -> str:
                             os.path.join(ROOT, "include", "uzip.h"))
 
 
-def profile_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+def profile_traffic(kernel: str, key: str = "dram_bytes_per_full_launch"):
+    """DRAM bytes per launch (or, with key="dram_read_bytes_per_full_launch",
+    the read bytes alone) from the committed ncu summary, if it was taken on
     the current kernel code (else None)."""
     src = {"encode": "encode.cu", "decode": "decode.cu"}[kernel]
     path = os.path.join(ROOT, "profiles", f"{kernel}_kv_cache.md")
@@ -185,7 +186,7 @@ def profile_traffic(kernel: str):
         text = open(path).read()
         sha = kernel_code_hash(src)
         m_sha = re.search(r"code_sha256_16:\s*([0-9a-f]+)", text)
-        m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9]+)", text)
+        m_b = re.search(key + r":\s*([0-9]+)", text)
         if m_sha and m_b and m_sha.group(1) == sha:
             return int(m_b.group(1))
     except OSError:
@@ -459,7 +460,11 @@ def report(args, ws, rank, n, raw, nbytes, m, max_ms, total_raw, cal_ms, enc_ms,
         "roofline": {"kernel": dominant, "bound": "hbm", "achieved": round(dom_gbs, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(dom_gbs / peak, 4), "peak_source": peak_src,
                      "traffic": profile_traffic(dominant),
-                     "algorithmic_bytes": enc_bytes if dominant == "encode" else dec_bytes},
+                     "algorithmic_bytes": enc_bytes if dominant == "encode" else dec_bytes,
+                     # DRAM writes still in L2 when a kernel ends are not counted in its
+                     # traffic, so the reads are the check for wasted traffic
+                     "traffic_read": profile_traffic(dominant, "dram_read_bytes_per_full_launch"),
+                     "algorithmic_read_bytes": raw if dominant == "encode" else nbytes},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
