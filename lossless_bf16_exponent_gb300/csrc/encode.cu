@@ -379,7 +379,7 @@ __device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, cons
     const uint32_t x = prmt(t[0], t[1], 0x5140), y = prmt(t[2], t[3], 0x5140);
     codes = prmt(x, y, 0x5410);
     escs = prmt(x, y, 0x7632);
-    fields = f[0] | (f[1] << 12);
+    fields = f[1] * 4096u + f[0];  // f[0] < 2^12: the same as f[0] | f[1] << 12, on the multiply-add pipe
 }
 
 // Escape flags of encode_group_e5m2 (pair k's two bits in byte k) -> 8-bit
@@ -462,8 +462,9 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
                     }
                 }
             }
-            const uint32_t f0 = fields[0] | (fields[1] << 24), f1 = (fields[1] >> 8) | (fields[2] << 16),
-                           f2 = (fields[2] >> 16) | (fields[3] << 8);
+            // four 24-bit field words -> 12 bytes: one byte permute per 4 bytes
+            const uint32_t f0 = prmt(fields[0], fields[1], 0x4210), f1 = prmt(fields[1], fields[2], 0x5421),
+                           f2 = prmt(fields[2], fields[3], 0x6542);
             if (valid == 32) {
                 *reinterpret_cast<uint4*>(dst_b + 16 * slot) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
                 uint32_t* fa = reinterpret_cast<uint32_t*>(dst_a + 12 * slot);
