@@ -234,7 +234,132 @@ __global__ void __launch_bounds__(256) clear_segments_kernel(uint32_t* segs, uin
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < words; i += gridDim.x * blockDim.x) segs[i] = 0;
 }
 
+// Stores of a unit's escape list, mask bytes and mask words: to the global
+// workspace with an L2 evict-last policy (the escape kernel reads them back),
+// or, for the one-CTA encoder of short inputs, to shared memory.
+template <bool kSmem>
+__device__ __forceinline__ void put_u32(uint32_t* q, uint32_t v, uint64_t keep) {
+    if (kSmem) *q = v;
+    else st_u32_keep(q, v, keep);
+}
+template <bool kSmem>
+__device__ __forceinline__ void put_u8(uint8_t* q, uint32_t v, uint64_t keep) {
+    if (kSmem) *q = (uint8_t)v;
+    else st_u8_keep(q, v, keep);
+}
+
 // ------------------------------------------------------------ dense kernel
+
+// One unit of kUnit values, by the whole warp: sign-mantissa bytes and packed
+// codes to the stream; the unit's escapes, ascending, to `list` (up to
+// kListCap (position, exponent) entries), or, past kListCap of them, its
+// escape-mask bytes to `masks`. Returns the unit's escape count (the same in
+// every lane).
+template <bool kSmem>
+__device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u, const uint8_t* s_tab,
+                                                    uint32_t* list, uint8_t* masks, uint64_t keep) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t ubase = u * kUnit;
+    const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
+    const uint4* src = reinterpret_cast<const uint4*>(p.in + ubase);
+    uint8_t* dst_a = p.out + p.L.off_a + ubase;
+    uint8_t* dst_b = p.out + p.L.off_b + ubase / 2;
+    const bool full = ulen == kUnit;  // every unit but the tensor's last
+    uint32_t cnt = 0;                 // escapes so far in this unit (uniform across the warp)
+    uint32_t mbytes[2] = {0, 0};      // this lane's 8 mask bytes, in case the list overflows
+#pragma unroll kIterUnroll
+    for (int it = 0; it < 2; it++) {
+        uint4 v[4];
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const uint32_t g = it * 128 + r * 32 + lane;
+            v[r] = make_uint4(0, 0, 0, 0);
+            if (full || 8 * g + 8 <= ulen) {
+                v[r] = ld_stream_v4(src + g);
+            } else if (8 * g < ulen) {  // ragged tail of the tensor (< 8 values)
+                uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (uint32_t i = 0; i < 8; i++)
+                    if (8 * g + i < ulen) w[i / 2] |= (uint32_t)p.in[ubase + 8 * g + i] << (16 * (i & 1));
+                v[r] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const uint32_t g = it * 128 + r * 32 + lane;
+            uint32_t esc_lo = 0, esc_hi = 0, e_lo = 0, e_hi = 0;
+            if (full || 8 * g < ulen) {
+                uint32_t a_lo, a_hi, codes;
+                encode_group(v[r], s_tab, a_lo, a_hi, codes, esc_lo, esc_hi, e_lo, e_hi);
+                if (!full && 8 * g + 8 > ulen) {  // codes and escapes of real values only
+                    const uint32_t valid = ulen - 8 * g;
+                    const uint64_t keep = (1ull << (8 * valid)) - 1;
+                    esc_lo &= (uint32_t)keep;
+                    esc_hi &= (uint32_t)(keep >> 32);
+                    codes &= (1u << (4 * valid)) - 1;
+                }
+                *reinterpret_cast<uint2*>(dst_a + 8 * g) = make_uint2(a_lo, a_hi);
+                *reinterpret_cast<uint32_t*>(dst_b + 4 * g) = codes;
+            }
+            // Escapes are rare: the mask and the ranking run only for rows
+            // holding one. Groups g = it*128 + r*32 + lane come in
+            // ascending order per (it, r) row, so a warp scan ranks the
+            // row's escapes (the whole warp takes part).
+            if (__any_sync(0xffffffffu, (esc_lo | esc_hi) != 0)) {
+                const uint32_t mask = escape_mask(esc_lo, esc_hi);
+                const uint32_t c = __popc(mask);
+                uint32_t excl, total;
+                if (!__any_sync(0xffffffffu, c > 1)) {  // sparse row: one ballot ranks it
+                    const uint32_t b = __ballot_sync(0xffffffffu, c != 0);
+                    excl = __popc(b & ((1u << lane) - 1));
+                    total = __popc(b);
+                } else {
+                    uint32_t incl = c;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += t;
+                    }
+                    excl = incl - c;
+                    total = __shfl_sync(0xffffffffu, incl, 31);
+                }
+                uint32_t j = cnt + excl;
+                for (uint32_t bits = mask; bits; bits &= bits - 1, j++) {
+                    const uint32_t b = __ffs(bits) - 1;
+                    const uint32_t e = ((b < 4 ? e_lo : e_hi) >> (8 * (b & 3))) & 0xFF;
+                    if (j < kListCap) put_u32<kSmem>(list + j, (8 * g + b) | (e << 16), keep);
+                }
+                cnt += total;
+                mbytes[it] |= mask << (8 * r);
+            }
+        }
+    }
+    if (cnt > kListCap) {  // the list overflowed: keep the masks instead
+#pragma unroll
+        for (int it = 0; it < 2; it++)
+#pragma unroll
+            for (int r = 0; r < 4; r++)
+                put_u8<kSmem>(masks + it * 128 + r * 32 + lane, (mbytes[it] >> (8 * r)) & 0xFF, keep);
+    }
+    return cnt;
+}
+
+// Publish a unit for the escape kernel: its count, and its escapes added to
+// its segment's total (zeroed by the launch before the dense kernel, which
+// is waited for before the first total update).
+__device__ __forceinline__ void publish_unit(const Params& p, uint64_t u, uint32_t cnt, uint64_t keep,
+                                             bool& cleared) {
+    if ((threadIdx.x & 31) == 0) {
+        st_u32_keep(p.counts + u, cnt, keep);
+        if (cnt) {
+            if (!cleared) {
+                wait_for_prerequisite();
+                cleared = true;
+            }
+            atomicAdd(&p.segs[u >> p.seg_shift], cnt);
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_kernel(const Params p) {
     __shared__ uint32_t s_tab_words[64];
@@ -243,106 +368,12 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
     __syncthreads();
     allow_dependent_launch();
 
-    const uint32_t lane = threadIdx.x & 31;
     const uint64_t stride = (uint64_t)gridDim.x * kWarps;
     const uint64_t keep = l2_policy_evict_last();  // counts, lists, masks: read by the escape kernel
     bool cleared = false;
-    for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride) {
-        const uint64_t ubase = u * kUnit;
-        const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
-        const uint4* src = reinterpret_cast<const uint4*>(p.in + ubase);
-        uint8_t* dst_a = p.out + p.L.off_a + ubase;
-        uint8_t* dst_b = p.out + p.L.off_b + ubase / 2;
-        uint32_t* list = p.lists + u * kListCap;
-        const bool full = ulen == kUnit;  // every unit but the tensor's last
-        uint32_t cnt = 0;                 // escapes so far in this unit (uniform across the warp)
-        uint32_t mbytes[2] = {0, 0};      // this lane's 8 mask bytes, in case the list overflows
-#pragma unroll kIterUnroll
-        for (int it = 0; it < 2; it++) {
-            uint4 v[4];
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
-                const uint32_t g = it * 128 + r * 32 + lane;
-                v[r] = make_uint4(0, 0, 0, 0);
-                if (full || 8 * g + 8 <= ulen) {
-                    v[r] = ld_stream_v4(src + g);
-                } else if (8 * g < ulen) {  // ragged tail of the tensor (< 8 values)
-                    uint32_t w[4] = {0, 0, 0, 0};
-#pragma unroll
-                    for (uint32_t i = 0; i < 8; i++)
-                        if (8 * g + i < ulen) w[i / 2] |= (uint32_t)p.in[ubase + 8 * g + i] << (16 * (i & 1));
-                    v[r] = make_uint4(w[0], w[1], w[2], w[3]);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; r++) {
-                const uint32_t g = it * 128 + r * 32 + lane;
-                uint32_t esc_lo = 0, esc_hi = 0, e_lo = 0, e_hi = 0;
-                if (full || 8 * g < ulen) {
-                    uint32_t a_lo, a_hi, codes;
-                    encode_group(v[r], s_tab, a_lo, a_hi, codes, esc_lo, esc_hi, e_lo, e_hi);
-                    if (!full && 8 * g + 8 > ulen) {  // codes and escapes of real values only
-                        const uint32_t valid = ulen - 8 * g;
-                        const uint64_t keep = (1ull << (8 * valid)) - 1;
-                        esc_lo &= (uint32_t)keep;
-                        esc_hi &= (uint32_t)(keep >> 32);
-                        codes &= (1u << (4 * valid)) - 1;
-                    }
-                    *reinterpret_cast<uint2*>(dst_a + 8 * g) = make_uint2(a_lo, a_hi);
-                    *reinterpret_cast<uint32_t*>(dst_b + 4 * g) = codes;
-                }
-                // Escapes are rare: the mask and the ranking run only for rows
-                // holding one. Groups g = it*128 + r*32 + lane come in
-                // ascending order per (it, r) row, so a warp scan ranks the
-                // row's escapes (the whole warp takes part).
-                if (__any_sync(0xffffffffu, (esc_lo | esc_hi) != 0)) {
-                    const uint32_t mask = escape_mask(esc_lo, esc_hi);
-                    const uint32_t c = __popc(mask);
-                    uint32_t excl, total;
-                    if (!__any_sync(0xffffffffu, c > 1)) {  // sparse row: one ballot ranks it
-                        const uint32_t b = __ballot_sync(0xffffffffu, c != 0);
-                        excl = __popc(b & ((1u << lane) - 1));
-                        total = __popc(b);
-                    } else {
-                        uint32_t incl = c;
-#pragma unroll
-                        for (int o = 1; o < 32; o <<= 1) {
-                            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                            if (lane >= o) incl += t;
-                        }
-                        excl = incl - c;
-                        total = __shfl_sync(0xffffffffu, incl, 31);
-                    }
-                    uint32_t j = cnt + excl;
-                    for (uint32_t bits = mask; bits; bits &= bits - 1, j++) {
-                        const uint32_t b = __ffs(bits) - 1;
-                        const uint32_t e = ((b < 4 ? e_lo : e_hi) >> (8 * (b & 3))) & 0xFF;
-                        if (j < kListCap) st_u32_keep(list + j, (8 * g + b) | (e << 16), keep);
-                    }
-                    cnt += total;
-                    mbytes[it] |= mask << (8 * r);
-                }
-            }
-        }
-        if (cnt > kListCap) {  // the list overflowed: keep the masks instead
-            uint8_t* gmask = p.masks + u * kUnitGroups;
-#pragma unroll
-            for (int it = 0; it < 2; it++)
-#pragma unroll
-                for (int r = 0; r < 4; r++)
-                    st_u8_keep(gmask + it * 128 + r * 32 + lane, (mbytes[it] >> (8 * r)) & 0xFF, keep);
-        }
-        if (lane == 0) {
-            st_u32_keep(p.counts + u, cnt, keep);
-            if (cnt) {
-                if (!cleared) {  // the segment totals are zeroed by the launch before this one
-                    wait_for_prerequisite();
-                    cleared = true;
-                }
-                atomicAdd(&p.segs[u >> p.seg_shift], cnt);
-            }
-        }
-    }
+    for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride)
+        publish_unit(p, u, dense_unit_bf16<false>(p, u, s_tab, p.lists + u * kListCap, p.masks + u * kUnitGroups, keep),
+                     keep, cleared);
     // The grid completes only after the clearing launch has (the escape
     // pass, which waits for this grid, reads the totals).
     if (threadIdx.x == 0) wait_for_prerequisite();
@@ -389,139 +420,141 @@ __device__ __forceinline__ uint32_t escape_mask_pairs(uint32_t escs) {
     return (((escs & 0x03030303u) * 0x41041u) >> 18) & 0xFFu;
 }
 
-// The dense pass for E5M2 input: as encode_dense_kernel, one warp per unit
-// of 2048 values in grid-stride order, but each lane takes 32 consecutive
-// values per step (two 16-byte loads; 12 bytes of packed fields and 16 bytes
-// of codes stored), so a row of the warp covers 1024 values in ascending
-// lane order and its escapes are ranked with one scan.
-__global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5m2_kernel(const Params p) {
-    __shared__ uint8_t s_tab[32];
-    __shared__ uint16_t s_pair[kPairEntries];
+// The dense pass for E5M2 input: as for BF16, one warp per unit of 2048
+// values, but each lane takes 32 consecutive values per step (two 16-byte
+// loads; 12 bytes of packed fields and 16 bytes of codes stored), so a row of
+// the warp covers 1024 values in ascending lane order and its escapes are
+// ranked with one scan; a unit whose list overflows keeps 32-bit mask words
+// (word s = unit positions 32 s ..). s_pair: the table of exponent pairs.
+template <bool kSmem>
+__device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u, const uint16_t* s_pair,
+                                                    uint32_t* list, uint8_t* masks, uint64_t keep) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t ubase = u * kUnit;
+    const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
+    const uint8_t* src = p.in8 + ubase;
+    uint8_t* dst_a = p.out + p.L.off_a + u * (kUnit / 8 * 3);
+    uint8_t* dst_b = p.out + p.L.off_b + u * (kUnit / 2);
+    const bool full = ulen == kUnit;
+    uint32_t cnt = 0;
+    uint32_t mwords[2] = {0, 0};
+    // both rows' loads first: a lane has 64 bytes in flight per unit
+    uint32_t wall[2][8];
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        const uint32_t v0 = 32 * (it * 32 + lane);
+        uint32_t* w = wall[it];
+        if (full || v0 + 32 <= ulen) {
+            const uint4 x0 = ld_stream_v4(src + v0), x1 = ld_stream_v4(src + v0 + 16);
+            w[0] = x0.x, w[1] = x0.y, w[2] = x0.z, w[3] = x0.w;
+            w[4] = x1.x, w[5] = x1.y, w[6] = x1.z, w[7] = x1.w;
+        } else {  // the tensor's ragged tail
+#pragma unroll
+            for (int k = 0; k < 8; k++) w[k] = 0;
+#pragma unroll
+            for (uint32_t i = 0; i < 32; i++)
+                if (v0 + i < ulen) w[i / 4] |= (uint32_t)src[v0 + i] << (8 * (i & 3));
+        }
+    }
+#pragma unroll
+    for (int it = 0; it < 2; it++) {
+        const uint32_t slot = it * 32 + lane;
+        const uint32_t v0 = 32 * slot;  // this lane's values v0 .. v0 + 31 of the unit
+        const uint32_t* w = wall[it];
+        uint32_t codes[4], fields[4], escs[4];
+        uint32_t escany = 0;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            encode_group_e5m2(w[2 * q], w[2 * q + 1], s_pair, codes[q], fields[q], escs[q]);
+            escany |= escs[q];
+        }
+        const uint32_t valid = ulen > v0 ? min(ulen - v0, 32u) : 0u;
+        if (valid < 32) {  // only real values have codes and fields (escapes: masked below)
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                const uint32_t vq = valid > 8u * q ? min(valid - 8u * q, 8u) : 0u;
+                if (vq < 8) {
+                    codes[q] &= (1u << (4 * vq)) - 1;
+                    fields[q] &= (1u << (3 * vq)) - 1;
+                }
+            }
+        }
+        // four 24-bit field words -> 12 bytes: one byte permute per 4 bytes
+        const uint32_t f0 = prmt(fields[0], fields[1], 0x4210), f1 = prmt(fields[1], fields[2], 0x5421),
+                       f2 = prmt(fields[2], fields[3], 0x6542);
+        if (valid == 32) {
+            *reinterpret_cast<uint4*>(dst_b + 16 * slot) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+            uint32_t* fa = reinterpret_cast<uint32_t*>(dst_a + 12 * slot);
+            fa[0] = f0;
+            fa[1] = f1;
+            fa[2] = f2;
+        } else if (valid > 0) {  // the last groups of the tensor: nothing past their bytes
+            const uint32_t gv = (valid + 7) / 8;
+#pragma unroll
+            for (uint32_t q = 0; q < 4; q++)
+                if (q < gv) *reinterpret_cast<uint32_t*>(dst_b + 16 * slot + 4 * q) = codes[q];
+#pragma unroll
+            for (uint32_t b = 0; b < 12; b++)
+                if (b < 3 * gv) dst_a[12 * slot + b] = (uint8_t)((b < 4 ? f0 : b < 8 ? f1 : f2) >> (8 * (b & 3)));
+        }
+        // Escapes of this row (1024 values, lane-major): one scan ranks them.
+        if (__any_sync(0xffffffffu, (escany & 0x03030303u) != 0)) {
+            uint32_t emask = 0;
+#pragma unroll
+            for (int q = 0; q < 4; q++) emask |= escape_mask_pairs(escs[q]) << (8 * q);
+            if (valid < 32) emask &= (1u << valid) - 1;  // (valid == 0: no bits)
+            const uint32_t c = __popc(emask);
+            uint32_t incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            uint32_t j = cnt + incl - c;
+            for (uint32_t bits = emask; bits; bits &= bits - 1, j++) {
+                const uint32_t b = __ffs(bits) - 1;
+                const uint32_t k = b >> 2;  // input word of value b, chosen in registers
+                const uint32_t lo = (k & 2) ? ((k & 1) ? w[3] : w[2]) : ((k & 1) ? w[1] : w[0]);
+                const uint32_t hi = (k & 2) ? ((k & 1) ? w[7] : w[6]) : ((k & 1) ? w[5] : w[4]);
+                const uint32_t e = (((k & 4) ? hi : lo) >> (8 * (b & 3) + 2)) & 0x1F;
+                if (j < kListCap) put_u32<kSmem>(list + j, (v0 + b) | (e << 16), keep);
+            }
+            cnt += __shfl_sync(0xffffffffu, incl, 31);
+            mwords[it] = emask;
+        }
+    }
+    if (cnt > kListCap) {  // the list overflowed: keep the masks (word s = unit positions 32 s ..)
+#pragma unroll
+        for (int it = 0; it < 2; it++) put_u32<kSmem>(reinterpret_cast<uint32_t*>(masks) + it * 32 + lane, mwords[it], keep);
+    }
+    return cnt;
+}
+
+// The pair table: entry (ea | eb << 5) of the 1024 pairs, from the 32-entry
+// table of code | escape << 7 in s_tab (built by the first 32 threads).
+__device__ __forceinline__ void build_pair_table(const Params& p, uint8_t* s_tab, uint16_t* s_pair) {
     if (threadIdx.x < 32)
         s_tab[threadIdx.x] = p.cb[UZIP_CB_ENC + threadIdx.x] | (p.cb[UZIP_CB_ESC + threadIdx.x] ? 0x80 : 0);
     __syncthreads();
-    for (uint32_t i = threadIdx.x; i < kPairEntries; i += kThreads) {
+    for (uint32_t i = threadIdx.x; i < kPairEntries; i += blockDim.x) {
         const uint32_t ta = s_tab[i & 31], tb = s_tab[i >> 5];
         s_pair[i] = (uint16_t)((ta & 0xF) | ((tb & 0xF) << 4) | ((ta >> 7) << 8) | ((tb >> 7) << 9));
     }
+}
+
+__global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5m2_kernel(const Params p) {
+    __shared__ uint8_t s_tab[32];
+    __shared__ uint16_t s_pair[kPairEntries];
+    build_pair_table(p, s_tab, s_pair);
     __syncthreads();
     allow_dependent_launch();
 
-    const uint32_t lane = threadIdx.x & 31;
     const uint64_t stride = (uint64_t)gridDim.x * kWarps;
     const uint64_t keep = l2_policy_evict_last();
     bool cleared = false;
-    for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride) {
-        const uint64_t ubase = u * kUnit;
-        const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
-        const uint8_t* src = p.in8 + ubase;
-        uint8_t* dst_a = p.out + p.L.off_a + u * (kUnit / 8 * 3);
-        uint8_t* dst_b = p.out + p.L.off_b + u * (kUnit / 2);
-        uint32_t* list = p.lists + u * kListCap;
-        const bool full = ulen == kUnit;
-        uint32_t cnt = 0;
-        uint32_t mwords[2] = {0, 0};
-        // both rows' loads first: a lane has 64 bytes in flight per unit
-        uint32_t wall[2][8];
-#pragma unroll
-        for (int it = 0; it < 2; it++) {
-            const uint32_t v0 = 32 * (it * 32 + lane);
-            uint32_t* w = wall[it];
-            if (full || v0 + 32 <= ulen) {
-                const uint4 x0 = ld_stream_v4(src + v0), x1 = ld_stream_v4(src + v0 + 16);
-                w[0] = x0.x, w[1] = x0.y, w[2] = x0.z, w[3] = x0.w;
-                w[4] = x1.x, w[5] = x1.y, w[6] = x1.z, w[7] = x1.w;
-            } else {  // the tensor's ragged tail
-#pragma unroll
-                for (int k = 0; k < 8; k++) w[k] = 0;
-#pragma unroll
-                for (uint32_t i = 0; i < 32; i++)
-                    if (v0 + i < ulen) w[i / 4] |= (uint32_t)src[v0 + i] << (8 * (i & 3));
-            }
-        }
-#pragma unroll
-        for (int it = 0; it < 2; it++) {
-            const uint32_t slot = it * 32 + lane;
-            const uint32_t v0 = 32 * slot;  // this lane's values v0 .. v0 + 31 of the unit
-            const uint32_t* w = wall[it];
-            uint32_t codes[4], fields[4], escs[4];
-            uint32_t escany = 0;
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                encode_group_e5m2(w[2 * q], w[2 * q + 1], s_pair, codes[q], fields[q], escs[q]);
-                escany |= escs[q];
-            }
-            const uint32_t valid = ulen > v0 ? min(ulen - v0, 32u) : 0u;
-            if (valid < 32) {  // only real values have codes and fields (escapes: masked below)
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    const uint32_t vq = valid > 8u * q ? min(valid - 8u * q, 8u) : 0u;
-                    if (vq < 8) {
-                        codes[q] &= (1u << (4 * vq)) - 1;
-                        fields[q] &= (1u << (3 * vq)) - 1;
-                    }
-                }
-            }
-            // four 24-bit field words -> 12 bytes: one byte permute per 4 bytes
-            const uint32_t f0 = prmt(fields[0], fields[1], 0x4210), f1 = prmt(fields[1], fields[2], 0x5421),
-                           f2 = prmt(fields[2], fields[3], 0x6542);
-            if (valid == 32) {
-                *reinterpret_cast<uint4*>(dst_b + 16 * slot) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
-                uint32_t* fa = reinterpret_cast<uint32_t*>(dst_a + 12 * slot);
-                fa[0] = f0;
-                fa[1] = f1;
-                fa[2] = f2;
-            } else if (valid > 0) {  // the last groups of the tensor: nothing past their bytes
-                const uint32_t gv = (valid + 7) / 8;
-#pragma unroll
-                for (uint32_t q = 0; q < 4; q++)
-                    if (q < gv) *reinterpret_cast<uint32_t*>(dst_b + 16 * slot + 4 * q) = codes[q];
-#pragma unroll
-                for (uint32_t b = 0; b < 12; b++)
-                    if (b < 3 * gv) dst_a[12 * slot + b] = (uint8_t)((b < 4 ? f0 : b < 8 ? f1 : f2) >> (8 * (b & 3)));
-            }
-            // Escapes of this row (1024 values, lane-major): one scan ranks them.
-            if (__any_sync(0xffffffffu, (escany & 0x03030303u) != 0)) {
-                uint32_t emask = 0;
-#pragma unroll
-                for (int q = 0; q < 4; q++) emask |= escape_mask_pairs(escs[q]) << (8 * q);
-                if (valid < 32) emask &= (1u << valid) - 1;  // (valid == 0: no bits)
-                const uint32_t c = __popc(emask);
-                uint32_t incl = c;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += t;
-                }
-                uint32_t j = cnt + incl - c;
-                for (uint32_t bits = emask; bits; bits &= bits - 1, j++) {
-                    const uint32_t b = __ffs(bits) - 1;
-                    const uint32_t k = b >> 2;  // input word of value b, chosen in registers
-                    const uint32_t lo = (k & 2) ? ((k & 1) ? w[3] : w[2]) : ((k & 1) ? w[1] : w[0]);
-                    const uint32_t hi = (k & 2) ? ((k & 1) ? w[7] : w[6]) : ((k & 1) ? w[5] : w[4]);
-                    const uint32_t e = (((k & 4) ? hi : lo) >> (8 * (b & 3) + 2)) & 0x1F;
-                    if (j < kListCap) st_u32_keep(list + j, (v0 + b) | (e << 16), keep);
-                }
-                cnt += __shfl_sync(0xffffffffu, incl, 31);
-                mwords[it] = emask;
-            }
-        }
-        if (cnt > kListCap) {  // the list overflowed: keep the masks (word s = unit positions 32 s ..)
-            uint8_t* gmask = p.masks + u * kUnitGroups;
-#pragma unroll
-            for (int it = 0; it < 2; it++) st_u32_keep(gmask + 4 * (it * 32 + lane), mwords[it], keep);
-        }
-        if (lane == 0) {
-            st_u32_keep(p.counts + u, cnt, keep);
-            if (cnt) {
-                if (!cleared) {  // the segment totals are zeroed by the launch before this one
-                    wait_for_prerequisite();
-                    cleared = true;
-                }
-                atomicAdd(&p.segs[u >> p.seg_shift], cnt);
-            }
-        }
-    }
+    for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride)
+        publish_unit(p, u, dense_unit_e5m2<false>(p, u, s_pair, p.lists + u * kListCap, p.masks + u * kUnitGroups, keep),
+                     keep, cleared);
     // The grid completes only after the clearing launch has (the escape
     // pass, which waits for this grid, reads the totals).
     if (threadIdx.x == 0) wait_for_prerequisite();
@@ -1024,6 +1057,142 @@ __global__ void __launch_bounds__(kThreads, UZIP_ESC_MIN_BLOCKS) encode_escape_k
     }
 }
 
+// ------------------------------------------------------------ short inputs
+//
+// An input of at most kSmallUnits units and kSmallChunks chunks is encoded by
+// one CTA in one launch. A warp per unit runs the dense pass with the unit's
+// escape list (or mask bytes) in shared memory; after a barrier the CTA scans
+// the unit counts, finds each chunk's first escape (a binary search of the
+// chunk's start in its unit's list), writes the offsets and places every
+// escape (a thread per escape: its unit from the unit prefixes, its chunk
+// from its position). Nothing goes through the workspace: the input is read,
+// the stream written, and a message costs one kernel launch instead of two.
+#ifndef UZIP_SMALL_UNITS
+#define UZIP_SMALL_UNITS 32
+#endif
+constexpr uint32_t kSmallUnits = UZIP_SMALL_UNITS;  // inputs of up to this many units of 2048 values
+constexpr uint32_t kSmallChunks = 4096;  // chunk offsets held in shared memory
+constexpr int kSmallThreads = 32 * kSmallUnits;
+
+// Position in its unit of the j-th escape of a unit that kept mask bits
+// (bit b of word w: position 32 w + b).
+__device__ uint32_t nth_mask_bit(const uint32_t* words, uint32_t j) {
+    for (uint32_t w = 0;; w++) {
+        uint32_t x = words[w];
+        const uint32_t c = __popc(x);
+        if (j < c) {
+            for (; j; j--) x &= x - 1;
+            return 32 * w + (__ffs(x) - 1);
+        }
+        j -= c;
+    }
+}
+
+template <bool kE5>
+__global__ void __launch_bounds__(kSmallThreads, 1) encode_small_kernel(const Params p) {
+    __shared__ uint32_t s_list[kSmallUnits][kListCap];
+    __shared__ __align__(16) uint32_t s_masks[kSmallUnits][kUnitGroups / 4];
+    __shared__ uint32_t s_pre[kSmallUnits + 1];   // escapes before unit u; s_pre[units] = M
+    __shared__ uint32_t s_off[kSmallChunks + 1];  // the chunk offsets
+    __shared__ uint32_t s_tab_words[64];
+    __shared__ uint16_t s_pair[kE5 ? kPairEntries : 2];
+    uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_tab_words);
+    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (kE5) {
+        build_pair_table(p, s_tab, s_pair);
+    } else if (tid < 256) {
+        s_tab[tid] = p.cb[UZIP_CB_ENC + tid] | (p.cb[UZIP_CB_ESC + tid] ? 0x80 : 0);
+    }
+    __syncthreads();
+    const uint32_t units = (uint32_t)p.units, nc = (uint32_t)p.L.nc;
+
+    // 1. the dense pass, a warp per unit
+    if (warp < units) {
+        uint8_t* masks = reinterpret_cast<uint8_t*>(s_masks[warp]);
+        const uint32_t cnt = kE5 ? dense_unit_e5m2<true>(p, warp, s_pair, s_list[warp], masks, 0)
+                                 : dense_unit_bf16<true>(p, warp, s_tab, s_list[warp], masks, 0);
+        if (lane == 0) s_pre[warp + 1] = cnt;
+    }
+    __syncthreads();
+    // 2. the unit prefix
+    if (warp == 0) {
+        const uint32_t c = lane < units ? s_pre[lane + 1] : 0u;
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= (uint32_t)o) incl += t;
+        }
+        if (lane < units) s_pre[lane + 1] = incl;
+        if (lane == 0) s_pre[0] = 0;
+    }
+    __syncthreads();
+    const uint32_t m = s_pre[units];
+    // 3. each chunk's first escape: chunk q starts at position x of unit u
+    for (uint32_t q = tid; q < nc; q += blockDim.x) {
+        const uint32_t st = q * p.chunk, u = st / kUnit, x = st % kUnit;
+        const uint32_t cu = s_pre[u + 1] - s_pre[u];
+        uint32_t below = 0;  // escapes of unit u before x
+        if (cu <= kListCap) {
+            uint32_t hi = cu;
+            while (below < hi) {
+                const uint32_t mid = (below + hi) >> 1;
+                if ((s_list[u][mid] & 0xFFFF) < x) below = mid + 1;
+                else hi = mid;
+            }
+        } else {
+            for (uint32_t w = 0; w < x / 32; w++) below += __popc(s_masks[u][w]);
+            if (x % 32) below += __popc(s_masks[u][x / 32] & ((1u << (x % 32)) - 1));
+        }
+        s_off[q] = s_pre[u] + below;
+    }
+    if (tid == 0) s_off[nc] = m;
+    __syncthreads();
+    uint8_t* offs = p.out + p.L.off_c;
+    for (uint32_t q = tid; q <= nc; q += blockDim.x) *reinterpret_cast<uint32_t*>(offs + 4ull * q) = s_off[q];
+    // 4. every escape: its unit, its place in the unit, its chunk; every byte
+    //    below out_capacity
+    const bool sent = p.fmt == kSentinel;
+    const uint64_t dbase = p.L.off_d;
+    for (uint32_t gi = tid; gi < m; gi += blockDim.x) {
+        uint32_t lo = 0, hi = units;  // s_pre[lo] <= gi < s_pre[hi]
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (s_pre[mid] <= gi) lo = mid;
+            else hi = mid;
+        }
+        const uint32_t j = gi - s_pre[lo], cu = s_pre[lo + 1] - s_pre[lo];
+        uint32_t pos, expo;
+        if (cu <= kListCap) {
+            const uint32_t e = s_list[lo][j];
+            pos = e & 0xFFFF;
+            expo = e >> 16;
+        } else {
+            pos = nth_mask_bit(s_masks[lo], j);
+            const uint32_t i = lo * kUnit + pos;
+            expo = kE5 ? (p.in8[i] >> 2) & 0x1F : (p.in[i] >> 7) & 0xFF;
+        }
+        const uint32_t i = lo * kUnit + pos, q = div_chunk(p, i);
+        const uint32_t o = s_off[q], r = gi - o;
+        if (sent) {
+            if (dbase + gi < p.cap) p.out[dbase + gi] = (uint8_t)expo;
+        } else {
+            const uint32_t k = s_off[q + 1] - o, pq = i - q * p.chunk;
+            const uint64_t bp = dbase + 3ull * o + 2 * r, bv = dbase + 3ull * o + 2 * k + r;
+            if (bp < p.cap) p.out[bp] = (uint8_t)(pq & 0xFF);
+            if (bp + 1 < p.cap) p.out[bp + 1] = (uint8_t)(pq >> 8);
+            if (bv < p.cap) p.out[bv] = (uint8_t)expo;
+        }
+    }
+    // 5. padding and header
+    if (tid == 0) {
+        zero_words(p.out, p.L.off_c + 4 * (p.L.nc + 1), p.L.off_d);
+        zero_bytes(p.out, p.L.off_a + p.a_bytes, p.L.off_b);
+        zero_words(p.out, p.L.off_b + 4 * ((p.n + 7) / 8), p.L.off_c);
+        write_header(p, m, stream_total(p, m) > p.cap ? UZIP_FLAG_CAPACITY : 0u);
+    }
+}
+
 // n == 0: header, offsets[0] = 0 and padding only.
 __global__ void encode_empty_kernel(const Params p) {
     *reinterpret_cast<uint32_t*>(p.out + p.L.off_c) = 0;
@@ -1137,6 +1306,10 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
 
     if (n == 0) {
         encode_empty_kernel<<<1, 1, 0, s>>>(p);
+        UZIP_CUDA_TRY(cudaGetLastError());
+    } else if (g.units <= kSmallUnits && L.nc <= kSmallChunks) {  // one CTA, one launch
+        if (fmt == kE5M2) encode_small_kernel<true><<<1, kSmallThreads, 0, s>>>(p);
+        else encode_small_kernel<false><<<1, kSmallThreads, 0, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
     } else {
         DeviceFacts f;
