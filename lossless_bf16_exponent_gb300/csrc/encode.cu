@@ -251,19 +251,21 @@ __device__ __forceinline__ void put_u8(uint8_t* q, uint32_t v, uint64_t keep) {
 // ------------------------------------------------------------ dense kernel
 
 // One unit of kUnit values, by the whole warp: sign-mantissa bytes and packed
-// codes to the stream; the unit's escapes, ascending, to `list` (up to
-// kListCap (position, exponent) entries), or, past kListCap of them, its
-// escape-mask bytes to `masks`. Returns the unit's escape count (the same in
-// every lane).
+// codes to the stream; the unit's escapes, ascending, to its list in `lists`
+// (up to kListCap (position, exponent) entries per unit), or, past kListCap of
+// them, its escape-mask bytes to its row of `masks` (the workspace's arrays,
+// or the one-CTA encoder's shared ones). Returns the unit's escape count (the
+// same in every lane).
 template <bool kSmem>
 __device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u, const uint8_t* s_tab,
-                                                    uint32_t* list, uint8_t* masks, uint64_t keep) {
+                                                    uint32_t* lists, uint8_t* masks_all, uint64_t keep) {
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t ubase = u * kUnit;
     const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
     const uint4* src = reinterpret_cast<const uint4*>(p.in + ubase);
     uint8_t* dst_a = p.out + p.L.off_a + ubase;
     uint8_t* dst_b = p.out + p.L.off_b + ubase / 2;
+    uint32_t* list = lists + u * kListCap;
     const bool full = ulen == kUnit;  // every unit but the tensor's last
     uint32_t cnt = 0;                 // escapes so far in this unit (uniform across the warp)
     uint32_t mbytes[2] = {0, 0};      // this lane's 8 mask bytes, in case the list overflows
@@ -335,6 +337,7 @@ __device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u,
         }
     }
     if (cnt > kListCap) {  // the list overflowed: keep the masks instead
+        uint8_t* masks = masks_all + u * kUnitGroups;
 #pragma unroll
         for (int it = 0; it < 2; it++)
 #pragma unroll
@@ -372,8 +375,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
     const uint64_t keep = l2_policy_evict_last();  // counts, lists, masks: read by the escape kernel
     bool cleared = false;
     for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride)
-        publish_unit(p, u, dense_unit_bf16<false>(p, u, s_tab, p.lists + u * kListCap, p.masks + u * kUnitGroups, keep),
-                     keep, cleared);
+        publish_unit(p, u, dense_unit_bf16<false>(p, u, s_tab, p.lists, p.masks, keep), keep, cleared);
     // The grid completes only after the clearing launch has (the escape
     // pass, which waits for this grid, reads the totals).
     if (threadIdx.x == 0) wait_for_prerequisite();
@@ -428,13 +430,14 @@ __device__ __forceinline__ uint32_t escape_mask_pairs(uint32_t escs) {
 // (word s = unit positions 32 s ..). s_pair: the table of exponent pairs.
 template <bool kSmem>
 __device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u, const uint16_t* s_pair,
-                                                    uint32_t* list, uint8_t* masks, uint64_t keep) {
+                                                    uint32_t* lists, uint8_t* masks_all, uint64_t keep) {
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t ubase = u * kUnit;
     const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
     const uint8_t* src = p.in8 + ubase;
     uint8_t* dst_a = p.out + p.L.off_a + u * (kUnit / 8 * 3);
     uint8_t* dst_b = p.out + p.L.off_b + u * (kUnit / 2);
+    uint32_t* list = lists + u * kListCap;
     const bool full = ulen == kUnit;
     uint32_t cnt = 0;
     uint32_t mwords[2] = {0, 0};
@@ -524,6 +527,7 @@ __device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u,
         }
     }
     if (cnt > kListCap) {  // the list overflowed: keep the masks (word s = unit positions 32 s ..)
+        uint8_t* masks = masks_all + u * kUnitGroups;
 #pragma unroll
         for (int it = 0; it < 2; it++) put_u32<kSmem>(reinterpret_cast<uint32_t*>(masks) + it * 32 + lane, mwords[it], keep);
     }
@@ -553,8 +557,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5
     const uint64_t keep = l2_policy_evict_last();
     bool cleared = false;
     for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride)
-        publish_unit(p, u, dense_unit_e5m2<false>(p, u, s_pair, p.lists + u * kListCap, p.masks + u * kUnitGroups, keep),
-                     keep, cleared);
+        publish_unit(p, u, dense_unit_e5m2<false>(p, u, s_pair, p.lists, p.masks, keep), keep, cleared);
     // The grid completes only after the clearing launch has (the escape
     // pass, which waits for this grid, reads the totals).
     if (threadIdx.x == 0) wait_for_prerequisite();
@@ -1108,9 +1111,9 @@ __global__ void __launch_bounds__(kSmallThreads, 1) encode_small_kernel(const Pa
 
     // 1. the dense pass, a warp per unit
     if (warp < units) {
-        uint8_t* masks = reinterpret_cast<uint8_t*>(s_masks[warp]);
-        const uint32_t cnt = kE5 ? dense_unit_e5m2<true>(p, warp, s_pair, s_list[warp], masks, 0)
-                                 : dense_unit_bf16<true>(p, warp, s_tab, s_list[warp], masks, 0);
+        uint8_t* masks = reinterpret_cast<uint8_t*>(&s_masks[0][0]);
+        const uint32_t cnt = kE5 ? dense_unit_e5m2<true>(p, warp, s_pair, &s_list[0][0], masks, 0)
+                                 : dense_unit_bf16<true>(p, warp, s_tab, &s_list[0][0], masks, 0);
         if (lane == 0) s_pre[warp + 1] = cnt;
     }
     __syncthreads();
