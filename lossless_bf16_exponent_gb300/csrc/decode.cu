@@ -244,13 +244,17 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_kernel(c
 
 // ------------------------------------------------------------ FP8 E5M2
 
-// The low twelve bits of packed 3-bit fields (four values) -> four bytes,
-// field i in byte i (higher input bits are ignored). Fields 0 and 2 move by 0
-// and 10 bits, fields 1 and 3 by 5 and 15: one multiply for each pair, whose
-// two shifted copies never overlap (so no carries), then a mask keeps the
-// wanted copy of each field.
+// The low twelve bits of packed 3-bit fields (four values, field i = sign << 2
+// | mantissa at bits 3i..3i+2; higher bits ignored) -> four E5M2 bytes without
+// their exponents: field i's sign at bit 8i + 7, its mantissa at 8i..8i+1. The
+// bits that move by 5 or 15 (signs of fields 0 and 2, mantissas of fields 1
+// and 3) take one multiply by 2^5 + 2^15; the bits that move by 0, 10 or 20
+// (mantissas of fields 0 and 2, signs of fields 1 and 3) one by 2^0 + 2^10 +
+// 2^20. Shifted copies that land on the same bit (only at bits 11 and 21 of
+// the second product) carry into bits 12 and 22, which, like every other
+// copy, the masks drop (checked for all 4096 field words).
 __device__ __forceinline__ uint32_t spread_fields4(uint32_t f12) {
-    return (((f12 & 0x1C7u) * 0x401u) & 0x00070007u) | (((f12 & 0xE38u) * 0x8020u) & 0x07000700u);
+    return (((f12 & 0x71Cu) * 0x8020u) & 0x03800380u) | (((f12 & 0x8E3u) * 0x100401u) & 0x80038003u);
 }
 
 // Decoder for FP8 E5M2 streams (page §4.2 / appendix C): tiles of
@@ -385,10 +389,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_DEC_MIN_BLOCKS) decode_e5m2_ker
                     e8[1] = (e8[1] & ~m1) | ((sv.y << 2) & 0x7C7C7C7Cu & m1);
                 }
 #pragma unroll
-                for (int hh = 0; hh < 2; hh++) {
-                    const uint32_t a4 = spread_fields4(hh ? g24[q] >> 12 : g24[q]);
-                    o[2 * q + hh] = ((a4 << 5) & 0x80808080u) | (a4 & 0x03030303u) | e8[hh];
-                }
+                for (int hh = 0; hh < 2; hh++) o[2 * q + hh] = spread_fields4(hh ? g24[q] >> 12 : g24[q]) | e8[hh];
             }
             const uint32_t ge = e0 + v0;
             if (v0 + 32 <= tlen) {

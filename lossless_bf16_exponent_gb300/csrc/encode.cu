@@ -399,9 +399,14 @@ __device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, cons
     uint32_t t[4], f[2];
 #pragma unroll
     for (int h = 0; h < 2; h++) {
-        const uint32_t a4 = ((w[h] >> 5) & 0x04040404u) | (w[h] & 0x03030303u);  // sign << 2 | mantissa
-        const uint32_t pr = a4 | (a4 >> 5);  // bits 0..5: a0 | a1 << 3; bits 16..21: a2 | a3 << 3
-        f[h] = (pr & 0x3Fu) | ((pr >> 10) & 0xFC0u);
+        // Field i = sign << 2 | mantissa of byte i, at bits 3i..3i+2: the bits
+        // that move down by 5 or 15 (signs of values 0 and 2, mantissas of 1
+        // and 3) take one multiply by 2^10 + 2^0 and a shift by 15, those that
+        // move down by 0, 10 or 20 (mantissas of 0 and 2, signs of 1 and 3)
+        // one by 2^20 + 2^10 + 2^0 and a shift by 20; no two shifted copies
+        // meet, and the unwanted ones fall below the shift or past bit 31
+        // (checked for all 4096 sign-mantissa patterns).
+        f[h] = (((w[h] & 0x03800380u) * 0x401u) >> 15) | (((w[h] & 0x80038003u) * 0x100401u) >> 20);
         // Exponent bytes e0..e3 -> e0 | e1 << 5 in bits 0..9 and e2 | e3 << 5 in
         // bits 16..25 (bits 13..15 pick up e2's low bits and are not used).
         const uint32_t e4 = (w[h] >> 2) & 0x1F1F1F1Fu;
