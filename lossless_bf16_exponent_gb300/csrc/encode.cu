@@ -66,6 +66,9 @@ constexpr uint32_t kParallelAbove = 32;       // pass 2 goes escape-parallel whe
 #ifndef UZIP_ENC_MIN_BLOCKS
 #define UZIP_ENC_MIN_BLOCKS 4
 #endif
+#ifndef UZIP_ENC_E5_MIN_BLOCKS
+#define UZIP_ENC_E5_MIN_BLOCKS 5  // E5M2 is issue-bound: 48 registers, a fifth CTA per SM
+#endif
 #ifndef UZIP_ENC_ITER_UNROLL
 #define UZIP_ENC_ITER_UNROLL 2
 #endif
@@ -551,7 +554,7 @@ __device__ __forceinline__ void build_pair_table(const Params& p, uint8_t* s_tab
     }
 }
 
-__global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_e5m2_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, UZIP_ENC_E5_MIN_BLOCKS) encode_dense_e5m2_kernel(const Params p) {
     __shared__ uint8_t s_tab[32];
     __shared__ uint16_t s_pair[kPairEntries];
     build_pair_table(p, s_tab, s_pair);
