@@ -153,6 +153,14 @@ __device__ __forceinline__ void count_one(uint32_t* col, uint32_t e) {
     atomicAdd(col + (e >> 1) * kPrivThreads, 1u << (16 * (e & 1)));
 }
 
+// The same from the bin pair (row) and the bin's low bit (half) directly: the
+// half's increment 1 or 2^16 is 1 + half * 0xFFFF, a multiply-add beside the
+// saturated ALU pipe. For BF16 the row is the value's high byte without the
+// sign, the half its bit 7.
+__device__ __forceinline__ void count_row(uint32_t* col, uint32_t row, uint32_t half) {
+    atomicAdd(col + row * kPrivThreads, half * 0xFFFFu + 1u);
+}
+
 template <int kFmt>
 __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(const void* __restrict__ xv, uint64_t n,
                                                                             uint8_t* __restrict__ cb) {
@@ -182,9 +190,9 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
             if (kFmt == kE5M2) {
 #pragma unroll
                 for (int b = 0; b < 4; b++) count_one(col, (w[q] >> (8 * b + 2)) & 0x1F);
-            } else {
-                count_one(col, (w[q] >> 7) & 0xFF);
-                count_one(col, (w[q] >> 23) & 0xFF);
+            } else {  // two values per word: rows from bits 8..14 and 24..30, halves bits 7 and 23
+                count_row(col, (w[q] >> 8) & 0x7F, (w[q] >> 7) & 1);
+                count_row(col, (w[q] >> 24) & 0x7F, (w[q] >> 23) & 1);
             }
         }
     };
