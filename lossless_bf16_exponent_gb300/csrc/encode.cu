@@ -256,9 +256,10 @@ __device__ __forceinline__ void put_u8(uint8_t* q, uint32_t v, uint64_t keep) {
 // One unit of kUnit values, by the whole warp: sign-mantissa bytes and packed
 // codes to the stream; the unit's escapes, ascending, to its list in `lists`
 // (up to kListCap (position, exponent) entries per unit), or, past kListCap of
-// them, its escape-mask bytes to its row of `masks` (the workspace's arrays,
-// or the one-CTA encoder's shared ones). Returns the unit's escape count (the
-// same in every lane).
+// them, its escape-mask bytes to its row of `masks` (the one-CTA encoder's
+// shared arrays when kSmem, else the workspace's). Each row holding an escape
+// ranks its escapes at once. Returns the unit's escape count (the same in
+// every lane).
 template <bool kSmem>
 __device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u, const uint8_t* s_tab,
                                                     uint32_t* lists, uint8_t* masks_all, uint64_t keep) {
@@ -350,6 +351,98 @@ __device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u,
     return cnt;
 }
 
+// The grid encoder's unit: as dense_unit_bf16, but rows holding an escape
+// only note it (the row's escape-mask bytes, and the exponent bytes of the
+// groups that escape) in the warp's shared memory; the unit's escapes are
+// ranked once, at its end, by one warp scan. Lane l then owns positions
+// 64 l .. 64 l + 63 (groups 8 l .. 8 l + 7, all in row l / 4) and writes their
+// list entries in position order. On escape-heavy inputs this replaces up to
+// eight per-row scans and lane loops with one; the flags double as the mask
+// bytes when the list overflows.
+__device__ __forceinline__ uint32_t dense_unit_bf16_deferred(const Params& p, uint64_t u, const uint8_t* s_tab,
+                                                             uint8_t* s_flag, uint8_t* s_exb, uint64_t keep) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t ubase = u * kUnit;
+    const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
+    const uint4* src = reinterpret_cast<const uint4*>(p.in + ubase);
+    uint8_t* dst_a = p.out + p.L.off_a + ubase;
+    uint8_t* dst_b = p.out + p.L.off_b + ubase / 2;
+    const bool full = ulen == kUnit;
+    uint32_t rows = 0;  // bit it * 4 + r: row (it, r), groups it*128 + r*32 + 0..31, holds an escape
+#pragma unroll kIterUnroll
+    for (int it = 0; it < 2; it++) {
+        uint4 v[4];
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const uint32_t g = it * 128 + r * 32 + lane;
+            v[r] = make_uint4(0, 0, 0, 0);
+            if (full || 8 * g + 8 <= ulen) {
+                v[r] = ld_stream_v4(src + g);
+            } else if (8 * g < ulen) {  // ragged tail of the tensor (< 8 values)
+                uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (uint32_t i = 0; i < 8; i++)
+                    if (8 * g + i < ulen) w[i / 2] |= (uint32_t)p.in[ubase + 8 * g + i] << (16 * (i & 1));
+                v[r] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 4; r++) {
+            const uint32_t g = it * 128 + r * 32 + lane;
+            uint32_t esc_lo = 0, esc_hi = 0, e_lo = 0, e_hi = 0;
+            if (full || 8 * g < ulen) {
+                uint32_t a_lo, a_hi, codes;
+                encode_group(v[r], s_tab, a_lo, a_hi, codes, esc_lo, esc_hi, e_lo, e_hi);
+                if (!full && 8 * g + 8 > ulen) {  // codes and escapes of real values only
+                    const uint32_t valid = ulen - 8 * g;
+                    const uint64_t live = (1ull << (8 * valid)) - 1;
+                    esc_lo &= (uint32_t)live;
+                    esc_hi &= (uint32_t)(live >> 32);
+                    codes &= (1u << (4 * valid)) - 1;
+                }
+                *reinterpret_cast<uint2*>(dst_a + 8 * g) = make_uint2(a_lo, a_hi);
+                *reinterpret_cast<uint32_t*>(dst_b + 4 * g) = codes;
+            }
+            if (__any_sync(0xffffffffu, (esc_lo | esc_hi) != 0)) {
+                s_flag[g] = (uint8_t)escape_mask(esc_lo, esc_hi);
+                if (esc_lo | esc_hi) *reinterpret_cast<uint2*>(s_exb + 8 * g) = make_uint2(e_lo, e_hi);
+                rows |= 1u << (it * 4 + r);
+            }
+        }
+    }
+    if (rows == 0) return 0;  // uniform: rows is built from warp votes
+    __syncwarp();
+    uint2 fw = make_uint2(0, 0);
+    if ((rows >> (lane >> 2)) & 1) fw = *reinterpret_cast<const uint2*>(s_flag + 8 * lane);
+    const uint32_t c = __popc(fw.x) + __popc(fw.y);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const uint32_t cnt = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t* list = p.lists + u * kListCap;
+    uint32_t j = incl - c;
+    uint32_t lo = fw.x, hi = fw.y;
+    while (lo | hi) {
+        const bool in_lo = lo != 0;
+        const uint32_t bp = (uint32_t)(__ffs(in_lo ? lo : hi) - 1) + (in_lo ? 0u : 32u);
+        if (in_lo) lo &= lo - 1;
+        else hi &= hi - 1;
+        const uint32_t pos = 64 * lane + bp;
+        if (j < kListCap) st_u32_keep(list + j, pos | ((uint32_t)s_exb[pos] << 16), keep);
+        j++;
+    }
+    if (cnt > kListCap) {  // the list overflowed: keep the masks instead
+        uint32_t* gm = reinterpret_cast<uint32_t*>(p.masks + u * kUnitGroups);
+        st_u32_keep(gm + 2 * lane, fw.x, keep);
+        st_u32_keep(gm + 2 * lane + 1, fw.y, keep);
+    }
+    __syncwarp();
+    return cnt;
+}
+
 // Publish a unit for the escape kernel: its count, and its escapes added to
 // its segment's total (zeroed by the launch before the dense kernel, which
 // is waited for before the first total update).
@@ -377,8 +470,11 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
     const uint64_t stride = (uint64_t)gridDim.x * kWarps;
     const uint64_t keep = l2_policy_evict_last();  // counts, lists, masks: read by the escape kernel
     bool cleared = false;
+    __shared__ __align__(16) uint8_t s_flag[kWarps][kUnitGroups];  // per warp: escape mask of each group
+    __shared__ __align__(16) uint8_t s_exb[kWarps][kUnit];         // per warp: exponent bytes of escaping groups
+    const uint32_t wid = threadIdx.x >> 5;
     for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride)
-        publish_unit(p, u, dense_unit_bf16<false>(p, u, s_tab, p.lists, p.masks, keep), keep, cleared);
+        publish_unit(p, u, dense_unit_bf16_deferred(p, u, s_tab, s_flag[wid], s_exb[wid], keep), keep, cleared);
     // The grid completes only after the clearing launch has (the escape
     // pass, which waits for this grid, reads the totals).
     if (threadIdx.x == 0) wait_for_prerequisite();
