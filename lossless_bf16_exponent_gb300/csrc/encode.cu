@@ -506,12 +506,15 @@ __device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, cons
         // meet, and the unwanted ones fall below the shift or past bit 31
         // (checked for all 4096 sign-mantissa patterns).
         f[h] = (((w[h] & 0x03800380u) * 0x401u) >> 15) | (((w[h] & 0x80038003u) * 0x100401u) >> 20);
-        // Exponent bytes e0..e3 -> e0 | e1 << 5 in bits 0..9 and e2 | e3 << 5 in
-        // bits 16..25 (bits 13..15 pick up e2's low bits and are not used).
-        const uint32_t e4 = (w[h] >> 2) & 0x1F1F1F1Fu;
-        const uint32_t ix = (e4 & 0x001F001Fu) | ((e4 >> 3) & 0xFFE0FFE0u);
-        t[2 * h] = pair[ix & 0x3FFu];  // values 0, 1 of the word
-        t[2 * h + 1] = pair[ix >> 16];  // values 2, 3
+        // Exponent bytes e0..e3 -> the byte offsets in the table of the pairs
+        // (e0, e1) and (e2, e3): 2 (e0 | e1 << 5) in bits 1..10 and
+        // 2 (e2 | e3 << 5) in bits 17..26, taken with one mask and one shift
+        // (offsets rather than indices: no scaling before the loads).
+        const uint32_t e2 = (w[h] >> 1) & 0x3E3E3E3Eu;  // 2 e in each byte
+        const uint32_t ix2 = (e2 & 0x003E003Eu) | ((e2 >> 3) & 0x07C007C0u);
+        const char* pb = reinterpret_cast<const char*>(pair);
+        t[2 * h] = *reinterpret_cast<const uint16_t*>(pb + (ix2 & 0x7FEu));  // values 0, 1 of the word
+        t[2 * h + 1] = *reinterpret_cast<const uint16_t*>(pb + (ix2 >> 16));  // values 2, 3
     }
     const uint32_t x = prmt(t[0], t[1], 0x5140), y = prmt(t[2], t[3], 0x5140);
     codes = prmt(x, y, 0x5410);
