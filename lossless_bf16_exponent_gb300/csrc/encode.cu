@@ -498,14 +498,14 @@ __device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, cons
     uint32_t t[4], f[2];
 #pragma unroll
     for (int h = 0; h < 2; h++) {
-        // Field i = sign << 2 | mantissa of byte i, at bits 3i..3i+2: the bits
-        // that move down by 5 or 15 (signs of values 0 and 2, mantissas of 1
-        // and 3) take one multiply by 2^10 + 2^0 and a shift by 15, those that
-        // move down by 0, 10 or 20 (mantissas of 0 and 2, signs of 1 and 3)
-        // one by 2^20 + 2^10 + 2^0 and a shift by 20; no two shifted copies
-        // meet, and the unwanted ones fall below the shift or past bit 31
-        // (checked for all 4096 sign-mantissa patterns).
-        f[h] = (((w[h] & 0x03800380u) * 0x401u) >> 15) | (((w[h] & 0x80038003u) * 0x100401u) >> 20);
+        // Field i = sign << 2 | mantissa of byte i, at bits 20 + 3i..22 + 3i
+        // (bits 0..19 are left over and dropped below): the bits that move
+        // up by 15 or 5 (signs of values 0 and 2, mantissas of 1 and 3) take
+        // one multiply by 2^15 + 2^5, those that move up by 20, 10 or 0
+        // (mantissas of 0 and 2, signs of 1 and 3) one by 2^20 + 2^10 + 2^0;
+        // no two copies meet at bits 20..31, and the others fall below them
+        // or past bit 31 (checked for all 4096 sign-mantissa patterns).
+        f[h] = ((w[h] & 0x03800380u) * 0x8020u) | ((w[h] & 0x80038003u) * 0x100401u);
         // Exponent bytes e0..e3 -> the byte offsets in the table of the pairs
         // (e0, e1) and (e2, e3): 2 (e0 | e1 << 5) in bits 1..10 and
         // 2 (e2 | e3 << 5) in bits 17..26, taken with one mask and one shift
@@ -519,7 +519,7 @@ __device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, cons
     const uint32_t x = prmt(t[0], t[1], 0x5140), y = prmt(t[2], t[3], 0x5140);
     codes = prmt(x, y, 0x5410);
     escs = prmt(x, y, 0x7632);
-    fields = f[1] * 4096u + f[0];  // f[0] < 2^12: the same as f[0] | f[1] << 12, on the multiply-add pipe
+    fields = (f[0] >> 20) | ((f[1] >> 8) & 0x00FFF000u);  // the two 12-bit field words, side by side
 }
 
 // Escape flags of encode_group_e5m2 (pair k's two bits in byte k) -> 8-bit
