@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(256) clear_segments_kernel(uint32_t* segs, uin
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < words; i += gridDim.x * blockDim.x) segs[i] = 0;
 }
 
-// Stores of a unit's escape list, mask bytes and mask words: to the global
+// Stores of an E5M2 unit's escape list and mask words: to the global
 // workspace with an L2 evict-last policy (the escape kernel reads them back),
 // or, for the one-CTA encoder of short inputs, to shared memory.
 template <bool kSmem>
@@ -245,24 +245,19 @@ __device__ __forceinline__ void put_u32(uint32_t* q, uint32_t v, uint64_t keep) 
     if (kSmem) *q = v;
     else st_u32_keep(q, v, keep);
 }
-template <bool kSmem>
-__device__ __forceinline__ void put_u8(uint8_t* q, uint32_t v, uint64_t keep) {
-    if (kSmem) *q = (uint8_t)v;
-    else st_u8_keep(q, v, keep);
-}
 
 // ------------------------------------------------------------ dense kernel
 
-// One unit of kUnit values, by the whole warp: sign-mantissa bytes and packed
-// codes to the stream; the unit's escapes, ascending, to its list in `lists`
-// (up to kListCap (position, exponent) entries per unit), or, past kListCap of
-// them, its escape-mask bytes to its row of `masks` (the one-CTA encoder's
-// shared arrays when kSmem, else the workspace's). Each row holding an escape
-// ranks its escapes at once. Returns the unit's escape count (the same in
-// every lane).
-template <bool kSmem>
-__device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u, const uint8_t* s_tab,
-                                                    uint32_t* lists, uint8_t* masks_all, uint64_t keep) {
+// The one-CTA encoder's unit of kUnit values, by the whole warp:
+// sign-mantissa bytes and packed codes to the stream; the unit's escapes,
+// ascending, to its row of the CTA's shared lists (up to kListCap (position,
+// exponent) entries per unit), or, past kListCap of them, its escape-mask
+// bytes to its row of the shared masks. Each row holding an escape ranks its
+// escapes at once (the grid encoder's dense_unit_bf16 defers the ranking to
+// the unit's end, which needs 2.3 KB of shared memory per warp). Returns the
+// unit's escape count (the same in every lane).
+__device__ __forceinline__ uint32_t dense_unit_bf16_shared(const Params& p, uint64_t u, const uint8_t* s_tab,
+                                                           uint32_t* lists, uint8_t* masks_all) {
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t ubase = u * kUnit;
     const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
@@ -299,9 +294,9 @@ __device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u,
                 encode_group(v[r], s_tab, a_lo, a_hi, codes, esc_lo, esc_hi, e_lo, e_hi);
                 if (!full && 8 * g + 8 > ulen) {  // codes and escapes of real values only
                     const uint32_t valid = ulen - 8 * g;
-                    const uint64_t keep = (1ull << (8 * valid)) - 1;
-                    esc_lo &= (uint32_t)keep;
-                    esc_hi &= (uint32_t)(keep >> 32);
+                    const uint64_t live = (1ull << (8 * valid)) - 1;
+                    esc_lo &= (uint32_t)live;
+                    esc_hi &= (uint32_t)(live >> 32);
                     codes &= (1u << (4 * valid)) - 1;
                 }
                 *reinterpret_cast<uint2*>(dst_a + 8 * g) = make_uint2(a_lo, a_hi);
@@ -333,7 +328,7 @@ __device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u,
                 for (uint32_t bits = mask; bits; bits &= bits - 1, j++) {
                     const uint32_t b = __ffs(bits) - 1;
                     const uint32_t e = ((b < 4 ? e_lo : e_hi) >> (8 * (b & 3))) & 0xFF;
-                    if (j < kListCap) put_u32<kSmem>(list + j, (8 * g + b) | (e << 16), keep);
+                    if (j < kListCap) list[j] = (8 * g + b) | (e << 16);
                 }
                 cnt += total;
                 mbytes[it] |= mask << (8 * r);
@@ -346,21 +341,23 @@ __device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u,
         for (int it = 0; it < 2; it++)
 #pragma unroll
             for (int r = 0; r < 4; r++)
-                put_u8<kSmem>(masks + it * 128 + r * 32 + lane, (mbytes[it] >> (8 * r)) & 0xFF, keep);
+                masks[it * 128 + r * 32 + lane] = (uint8_t)(mbytes[it] >> (8 * r));
     }
     return cnt;
 }
 
-// The grid encoder's unit: as dense_unit_bf16, but rows holding an escape
-// only note it (the row's escape-mask bytes, and the exponent bytes of the
-// groups that escape) in the warp's shared memory; the unit's escapes are
-// ranked once, at its end, by one warp scan. Lane l then owns positions
+// The grid encoder's unit: as dense_unit_bf16_shared, but the list or mask
+// words go to the workspace (row u, L2 evict-last policy `keep`), and rows
+// holding an escape only note it (the row's escape-mask bytes, and the
+// exponent bytes of the groups that escape) in the warp's shared memory
+// s_flag / s_exb; the unit's escapes are ranked once, at its end, by one warp
+// scan. Lane l then owns positions
 // 64 l .. 64 l + 63 (groups 8 l .. 8 l + 7, all in row l / 4) and writes their
 // list entries in position order. On escape-heavy inputs this replaces up to
 // eight per-row scans and lane loops with one; the flags double as the mask
 // bytes when the list overflows.
-__device__ __forceinline__ uint32_t dense_unit_bf16_deferred(const Params& p, uint64_t u, const uint8_t* s_tab,
-                                                             uint8_t* s_flag, uint8_t* s_exb, uint64_t keep) {
+__device__ __forceinline__ uint32_t dense_unit_bf16(const Params& p, uint64_t u, const uint8_t* s_tab,
+                                                    uint8_t* s_flag, uint8_t* s_exb, uint64_t keep) {
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t ubase = u * kUnit;
     const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
@@ -474,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
     __shared__ __align__(16) uint8_t s_exb[kWarps][kUnit];         // per warp: exponent bytes of escaping groups
     const uint32_t wid = threadIdx.x >> 5;
     for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride)
-        publish_unit(p, u, dense_unit_bf16_deferred(p, u, s_tab, s_flag[wid], s_exb[wid], keep), keep, cleared);
+        publish_unit(p, u, dense_unit_bf16(p, u, s_tab, s_flag[wid], s_exb[wid], keep), keep, cleared);
     // The grid completes only after the clearing launch has (the escape
     // pass, which waits for this grid, reads the totals).
     if (threadIdx.x == 0) wait_for_prerequisite();
@@ -1220,7 +1217,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) encode_small_kernel(const Pa
     if (warp < units) {
         uint8_t* masks = reinterpret_cast<uint8_t*>(&s_masks[0][0]);
         const uint32_t cnt = kE5 ? dense_unit_e5m2<true>(p, warp, s_pair, &s_list[0][0], masks, 0)
-                                 : dense_unit_bf16<true>(p, warp, s_tab, &s_list[0][0], masks, 0);
+                                 : dense_unit_bf16_shared(p, warp, s_tab, &s_list[0][0], masks);
         if (lane == 0) s_pre[warp + 1] = cnt;
     }
     __syncthreads();

@@ -116,9 +116,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
 __device__ __forceinline__ void st_u32_keep(void* p, uint32_t v, uint64_t pol) {
     asm volatile("st.global.L2::cache_hint.u32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
 }
-__device__ __forceinline__ void st_u8_keep(void* p, uint32_t v, uint64_t pol) {
-    asm volatile("st.global.L2::cache_hint.u8 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
-}
 
 // Launchers shared by the entry points (calibrate.cu, encode.cu).
 int calibrate_impl(const void* d_sample_bf16, size_t n_sample, void* d_codebook, cudaStream_t stream,
