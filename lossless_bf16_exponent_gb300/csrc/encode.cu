@@ -480,15 +480,39 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_MIN_BLOCKS) encode_dense_ke
 // ------------------------------------------------------- FP8 E5M2 dense kernel
 
 // E5M2 exponents have 5 bits, so a table of every exponent pair fits in
-// 2 KB of shared memory: entry (ea | eb << 5) = code(ea) | code(eb) << 4 (the
-// packed code byte of two neighbouring values) | esc(ea) << 8 | esc(eb) << 9.
-// One lookup then encodes two values.
+// shared memory: the entry of (ea, eb) = code(ea) | code(eb) << 4 (the packed
+// code byte of two neighbouring values) | esc(ea) << 8 | esc(eb) << 9. One
+// lookup then encodes two values. Two layouts:
+//  - wide (the grid encoder, 31.9 KB): the entry of (ea, eb) at byte offset
+//    (ea << 2 | eb << 10) ^ (eb & 7) << 4, i.e. the exponent bits of the byte
+//    pair in place, with eb's low three bits folded into the bank bits (in
+//    place alone, the bank would be ea's, and the pairs of a warp that share
+//    ea would queue on one bank); both pairs of a word take one mask, one
+//    shift and one three-input operation;
+//  - compact (the one-CTA encoder, whose shared memory holds its lists):
+//    2 KB, the entry at byte offset 2 (ea | eb << 5).
 constexpr uint32_t kPairEntries = 1024;
+constexpr uint32_t kWidePairHalfwords = 0x7C7C / 2 + 2;  // largest offset / 2, + 1, rounded to a word
+__host__ __device__ constexpr uint32_t wide_pair_offset(uint32_t ea, uint32_t eb) {
+    return ((ea << 2) | (eb << 10)) ^ ((eb & 7) << 4);
+}
+// Every pair has its own halfword of the wide table, inside it.
+constexpr bool wide_pairs_distinct() {
+    bool used[kWidePairHalfwords] = {};
+    for (uint32_t i = 0; i < kPairEntries; i++) {
+        const uint32_t o = wide_pair_offset(i & 31, i >> 5);
+        if (o % 2 || o / 2 >= kWidePairHalfwords || used[o / 2]) return false;
+        used[o / 2] = true;
+    }
+    return true;
+}
+static_assert(wide_pairs_distinct(), "wide pair table: offsets must be distinct, even and in range");
 
 // Eight E5M2 values (w0, w1: value i in byte i) -> their 8 codes (one word,
 // value i in nibble i), their 3-bit sign-mantissa fields (24 bits, value i at
 // bits 3i) and their escape flags (byte k: bit 0 for value 2k, bit 1 for
-// value 2k + 1).
+// value 2k + 1). `pair`: the wide pair table if kWide, else the compact one.
+template <bool kWide>
 __device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, const uint16_t* pair, uint32_t& codes,
                                                   uint32_t& fields, uint32_t& escs) {
     const uint32_t w[2] = {w0, w1};
@@ -503,15 +527,19 @@ __device__ __forceinline__ void encode_group_e5m2(uint32_t w0, uint32_t w1, cons
         // no two copies meet at bits 20..31, and the others fall below them
         // or past bit 31 (checked for all 4096 sign-mantissa patterns).
         f[h] = ((w[h] & 0x03800380u) * 0x8020u) | ((w[h] & 0x80038003u) * 0x100401u);
-        // Exponent bytes e0..e3 -> the byte offsets in the table of the pairs
-        // (e0, e1) and (e2, e3): 2 (e0 | e1 << 5) in bits 1..10 and
-        // 2 (e2 | e3 << 5) in bits 17..26, taken with one mask and one shift
-        // (offsets rather than indices: no scaling before the loads).
-        const uint32_t e2 = (w[h] >> 1) & 0x3E3E3E3Eu;  // 2 e in each byte
-        const uint32_t ix2 = (e2 & 0x003E003Eu) | ((e2 >> 3) & 0x07C007C0u);
+        // Exponent bytes e0..e3 -> the byte offsets of the pairs (e0, e1) and
+        // (e2, e3) in the table, in bits 0..15 and 16..31 (offsets rather
+        // than indices: no scaling before the loads).
         const char* pb = reinterpret_cast<const char*>(pair);
-        t[2 * h] = *reinterpret_cast<const uint16_t*>(pb + (ix2 & 0x7FEu));  // values 0, 1 of the word
-        t[2 * h + 1] = *reinterpret_cast<const uint16_t*>(pb + (ix2 >> 16));  // values 2, 3
+        uint32_t o;
+        if (kWide) {
+            o = (w[h] & 0x7C7C7C7Cu) ^ ((w[h] >> 6) & 0x00700070u);  // wide_pair_offset of both pairs
+        } else {
+            const uint32_t e2 = (w[h] >> 1) & 0x3E3E3E3Eu;  // 2 e in each byte
+            o = (e2 & 0x003E003Eu) | ((e2 >> 3) & 0x07C007C0u);  // 2 (e0 | e1 << 5), 2 (e2 | e3 << 5)
+        }
+        t[2 * h] = *reinterpret_cast<const uint16_t*>(pb + (o & 0xFFFFu));  // values 0, 1 of the word
+        t[2 * h + 1] = *reinterpret_cast<const uint16_t*>(pb + (o >> 16));  // values 2, 3
     }
     const uint32_t x = prmt(t[0], t[1], 0x5140), y = prmt(t[2], t[3], 0x5140);
     codes = prmt(x, y, 0x5410);
@@ -531,7 +559,8 @@ __device__ __forceinline__ uint32_t escape_mask_pairs(uint32_t escs) {
 // loads; 12 bytes of packed fields and 16 bytes of codes stored), so a row of
 // the warp covers 1024 values in ascending lane order and its escapes are
 // ranked with one scan; a unit whose list overflows keeps 32-bit mask words
-// (word s = unit positions 32 s ..). s_pair: the table of exponent pairs.
+// (word s = unit positions 32 s ..). s_pair: the table of exponent pairs
+// (the wide layout for the workspace path, the compact one when kSmem).
 template <bool kSmem>
 __device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u, const uint16_t* s_pair,
                                                     uint32_t* lists, uint8_t* masks_all, uint64_t keep) {
@@ -572,7 +601,7 @@ __device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u,
         uint32_t escany = 0;
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-            encode_group_e5m2(w[2 * q], w[2 * q + 1], s_pair, codes[q], fields[q], escs[q]);
+            encode_group_e5m2<!kSmem>(w[2 * q], w[2 * q + 1], s_pair, codes[q], fields[q], escs[q]);
             escany |= escs[q];
         }
         const uint32_t valid = ulen > v0 ? min(ulen - v0, 32u) : 0u;
@@ -638,22 +667,25 @@ __device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u,
     return cnt;
 }
 
-// The pair table: entry (ea | eb << 5) of the 1024 pairs, from the 32-entry
-// table of code | escape << 7 in s_tab (built by the first 32 threads).
+// The pair table (wide or compact layout) of the 1024 pairs, from the
+// 32-entry table of code | escape << 7 in s_tab (built by the first 32
+// threads). The wide table's other halfwords are never read.
+template <bool kWide>
 __device__ __forceinline__ void build_pair_table(const Params& p, uint8_t* s_tab, uint16_t* s_pair) {
     if (threadIdx.x < 32)
         s_tab[threadIdx.x] = p.cb[UZIP_CB_ENC + threadIdx.x] | (p.cb[UZIP_CB_ESC + threadIdx.x] ? 0x80 : 0);
     __syncthreads();
     for (uint32_t i = threadIdx.x; i < kPairEntries; i += blockDim.x) {
         const uint32_t ta = s_tab[i & 31], tb = s_tab[i >> 5];
-        s_pair[i] = (uint16_t)((ta & 0xF) | ((tb & 0xF) << 4) | ((ta >> 7) << 8) | ((tb >> 7) << 9));
+        s_pair[kWide ? wide_pair_offset(i & 31, i >> 5) / 2 : i] =
+            (uint16_t)((ta & 0xF) | ((tb & 0xF) << 4) | ((ta >> 7) << 8) | ((tb >> 7) << 9));
     }
 }
 
 __global__ void __launch_bounds__(kThreads, UZIP_ENC_E5_MIN_BLOCKS) encode_dense_e5m2_kernel(const Params p) {
     __shared__ uint8_t s_tab[32];
-    __shared__ uint16_t s_pair[kPairEntries];
-    build_pair_table(p, s_tab, s_pair);
+    __shared__ __align__(16) uint16_t s_pair[kWidePairHalfwords];
+    build_pair_table<true>(p, s_tab, s_pair);
     __syncthreads();
     allow_dependent_launch();
 
@@ -1206,7 +1238,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1) encode_small_kernel(const Pa
     uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_tab_words);
     const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (kE5) {
-        build_pair_table(p, s_tab, s_pair);
+        build_pair_table<false>(p, s_tab, s_pair);
     } else if (tid < 256) {
         s_tab[tid] = p.cb[UZIP_CB_ENC + tid] | (p.cb[UZIP_CB_ESC + tid] ? 0x80 : 0);
     }
