@@ -1046,7 +1046,9 @@ def run_workloads(args):
     res = {}
     for k in (args.only,) if args.only else (1, 2, 3, 5):
         x, sample = W.workload(k, device=dev)
-        if args.n and k == 3:  # a smaller instance of the law (profiling cases)
+        if args.n and k == 1:  # fewer rows of 128 (a short message: profiling cases)
+            x = W.rows_lognormal_scale(max(1, args.n // 128), 128, device=dev).reshape(-1)
+        elif args.n and k == 3:  # a smaller instance of the law (profiling cases)
             x = W.heavy_tailed(args.n, device=dev)
         elif args.n and k == 5:
             x = W.gradient_like(args.n, device=dev)
@@ -1116,7 +1118,8 @@ def main(argv=None):
     ap.add_argument("--only", type=int, choices=[1, 2, 3, 5], default=0,
                     help="workloads mode: run this workload alone")
     ap.add_argument("--n", type=int, default=0,
-                    help="workloads mode: values of the heavy-tailed (3) or gradient-like (5) law")
+                    help="workloads mode: values of the row-scaled (1, rounded to rows of 128), "
+                         "heavy-tailed (3) or gradient-like (5) law")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
