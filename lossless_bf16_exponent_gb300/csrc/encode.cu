@@ -248,23 +248,22 @@ __device__ __forceinline__ void put_u32(uint32_t* q, uint32_t v, uint64_t keep) 
 
 // ------------------------------------------------------------ dense kernel
 
-// The one-CTA encoder's unit of kUnit values, by the whole warp:
+// The short-input encoders' unit of kUnit values, by the whole warp:
 // sign-mantissa bytes and packed codes to the stream; the unit's escapes,
-// ascending, to its row of the CTA's shared lists (up to kListCap (position,
-// exponent) entries per unit), or, past kListCap of them, its escape-mask
-// bytes to its row of the shared masks. Each row holding an escape ranks its
+// ascending, to `list` (its row of the CTA's shared lists: up to kListCap
+// (position, exponent) entries), or, past kListCap of them, its escape-mask
+// bytes to `masks` (its row of the shared masks). Each row holding an escape ranks its
 // escapes at once (the grid encoder's dense_unit_bf16 defers the ranking to
 // the unit's end, which needs 2.3 KB of shared memory per warp). Returns the
 // unit's escape count (the same in every lane).
 __device__ __forceinline__ uint32_t dense_unit_bf16_shared(const Params& p, uint64_t u, const uint8_t* s_tab,
-                                                           uint32_t* lists, uint8_t* masks_all) {
+                                                           uint32_t* list, uint8_t* masks) {
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t ubase = u * kUnit;
     const uint32_t ulen = (uint32_t)min((uint64_t)kUnit, p.n - ubase);
     const uint4* src = reinterpret_cast<const uint4*>(p.in + ubase);
     uint8_t* dst_a = p.out + p.L.off_a + ubase;
     uint8_t* dst_b = p.out + p.L.off_b + ubase / 2;
-    uint32_t* list = lists + u * kListCap;
     const bool full = ulen == kUnit;  // every unit but the tensor's last
     uint32_t cnt = 0;                 // escapes so far in this unit (uniform across the warp)
     uint32_t mbytes[2] = {0, 0};      // this lane's 8 mask bytes, in case the list overflows
@@ -336,7 +335,6 @@ __device__ __forceinline__ uint32_t dense_unit_bf16_shared(const Params& p, uint
         }
     }
     if (cnt > kListCap) {  // the list overflowed: keep the masks instead
-        uint8_t* masks = masks_all + u * kUnitGroups;
 #pragma unroll
         for (int it = 0; it < 2; it++)
 #pragma unroll
@@ -560,9 +558,10 @@ __device__ __forceinline__ uint32_t escape_mask_pairs(uint32_t escs) {
 // the warp covers 1024 values in ascending lane order and its escapes are
 // ranked with one scan; a unit whose list overflows keeps 32-bit mask words
 // (word s = unit positions 32 s ..). s_pair: the table of exponent pairs
-// (the wide layout for the workspace path, the compact one when kSmem).
+// (the wide layout for the workspace path, the compact one when kSmem); `row`:
+// the unit's row of `lists` and `masks_all` (u itself for the workspace).
 template <bool kSmem>
-__device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u, const uint16_t* s_pair,
+__device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u, uint64_t row, const uint16_t* s_pair,
                                                     uint32_t* lists, uint8_t* masks_all, uint64_t keep) {
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t ubase = u * kUnit;
@@ -570,7 +569,7 @@ __device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u,
     const uint8_t* src = p.in8 + ubase;
     uint8_t* dst_a = p.out + p.L.off_a + u * (kUnit / 8 * 3);
     uint8_t* dst_b = p.out + p.L.off_b + u * (kUnit / 2);
-    uint32_t* list = lists + u * kListCap;
+    uint32_t* list = lists + row * kListCap;
     const bool full = ulen == kUnit;
     uint32_t cnt = 0;
     uint32_t mwords[2] = {0, 0};
@@ -660,7 +659,7 @@ __device__ __forceinline__ uint32_t dense_unit_e5m2(const Params& p, uint64_t u,
         }
     }
     if (cnt > kListCap) {  // the list overflowed: keep the masks (word s = unit positions 32 s ..)
-        uint8_t* masks = masks_all + u * kUnitGroups;
+        uint8_t* masks = masks_all + row * kUnitGroups;
 #pragma unroll
         for (int it = 0; it < 2; it++) put_u32<kSmem>(reinterpret_cast<uint32_t*>(masks) + it * 32 + lane, mwords[it], keep);
     }
@@ -693,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, UZIP_ENC_E5_MIN_BLOCKS) encode_dense
     const uint64_t keep = l2_policy_evict_last();
     bool cleared = false;
     for (uint64_t u = (uint64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); u < p.units; u += stride)
-        publish_unit(p, u, dense_unit_e5m2<false>(p, u, s_pair, p.lists, p.masks, keep), keep, cleared);
+        publish_unit(p, u, dense_unit_e5m2<false>(p, u, u, s_pair, p.lists, p.masks, keep), keep, cleared);
     // The grid completes only after the clearing launch has (the escape
     // pass, which waits for this grid, reads the totals).
     if (threadIdx.x == 0) wait_for_prerequisite();
@@ -1214,9 +1213,10 @@ constexpr uint32_t kSmallChunks = 4096;  // chunk offsets held in shared memory
 constexpr int kSmallThreads = 32 * kSmallUnits;
 
 // Position in its unit of the j-th escape of a unit that kept mask bits
-// (bit b of word w: position 32 w + b).
+// (bit b of word w: position 32 w + b; j is below the unit's count, so the
+// walk ends inside its kUnit / 32 words).
 __device__ uint32_t nth_mask_bit(const uint32_t* words, uint32_t j) {
-    for (uint32_t w = 0;; w++) {
+    for (uint32_t w = 0; w < kUnit / 32; w++) {
         uint32_t x = words[w];
         const uint32_t c = __popc(x);
         if (j < c) {
@@ -1225,6 +1225,91 @@ __device__ uint32_t nth_mask_bit(const uint32_t* words, uint32_t j) {
         }
         j -= c;
     }
+    return kUnit;  // not reached
+}
+
+// Escapes of a unit before its position x, from its list (cu <= kListCap
+// entries, ascending positions) or its mask words.
+__device__ __forceinline__ uint32_t escapes_before(const uint32_t* list, const uint32_t* masks, uint32_t cu,
+                                                   uint32_t x) {
+    uint32_t below = 0;
+    if (cu <= kListCap) {
+        uint32_t hi = cu;
+        while (below < hi) {
+            const uint32_t mid = (below + hi) >> 1;
+            if ((list[mid] & 0xFFFF) < x) below = mid + 1;
+            else hi = mid;
+        }
+    } else {
+        for (uint32_t w = 0; w < x / 32; w++) below += __popc(masks[w]);
+        if (x % 32) below += __popc(masks[x / 32] & ((1u << (x % 32)) - 1));
+    }
+    return below;
+}
+
+// The j-th escape of local unit i (count cu) of a short-input CTA, from the
+// CTA's shared lists or mask words: its position in the unit and its
+// exponent (re-read from the input for a unit that kept mask bits; ubase =
+// the unit's first value).
+template <bool kE5>
+__device__ __forceinline__ void unit_escape(const Params& p, const uint32_t* list, const uint32_t* masks, uint32_t cu,
+                                            uint32_t j, uint32_t ubase, uint32_t& pos, uint32_t& expo) {
+    if (cu <= kListCap) {
+        const uint32_t e = list[j];
+        pos = e & 0xFFFF;
+        expo = e >> 16;
+    } else {
+        pos = nth_mask_bit(masks, j);
+        const uint32_t i = ubase + pos;
+        expo = kE5 ? (p.in8[i] >> 2) & 0x1F : (p.in[i] >> 7) & 0xFF;
+    }
+}
+
+// Escape gi (global rank) at value i, in chunk q with offsets o .. o1: its
+// bytes in the stream (the sentinel format keeps the value only); every byte
+// below out_capacity.
+__device__ __forceinline__ void put_escape(const Params& p, uint32_t gi, uint32_t i, uint32_t q, uint32_t o,
+                                           uint32_t o1, uint32_t expo) {
+    const uint64_t dbase = p.L.off_d;
+    if (p.fmt == kSentinel) {
+        if (dbase + gi < p.cap) p.out[dbase + gi] = (uint8_t)expo;
+    } else {
+        const uint32_t r = gi - o, k = o1 - o, pq = i - q * p.chunk;
+        const uint64_t bp = dbase + 3ull * o + 2 * r, bv = dbase + 3ull * o + 2 * k + r;
+        if (bp < p.cap) p.out[bp] = (uint8_t)(pq & 0xFF);
+        if (bp + 1 < p.cap) p.out[bp + 1] = (uint8_t)(pq >> 8);
+        if (bv < p.cap) p.out[bv] = (uint8_t)expo;
+    }
+}
+
+// A warp's inclusive scan.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v, uint32_t lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= (uint32_t)o) v += t;
+    }
+    return v;
+}
+
+// The code tables of a short-input CTA (BF16 / sentinel: the 256-byte
+// code | escape << 7 table; E5M2: the compact pair table).
+template <bool kE5>
+__device__ __forceinline__ void build_small_tables(const Params& p, uint8_t* s_tab, uint16_t* s_pair) {
+    if (kE5) {
+        build_pair_table<false>(p, s_tab, s_pair);
+    } else if (threadIdx.x < 256) {
+        s_tab[threadIdx.x] = p.cb[UZIP_CB_ENC + threadIdx.x] | (p.cb[UZIP_CB_ESC + threadIdx.x] ? 0x80 : 0);
+    }
+    __syncthreads();
+}
+
+// Padding and header, by one thread, once every escape is counted.
+__device__ void finish_stream(const Params& p, uint32_t m) {
+    zero_words(p.out, p.L.off_c + 4 * (p.L.nc + 1), p.L.off_d);
+    zero_bytes(p.out, p.L.off_a + p.a_bytes, p.L.off_b);
+    zero_words(p.out, p.L.off_b + 4 * ((p.n + 7) / 8), p.L.off_c);
+    write_header(p, m, stream_total(p, m) > p.cap ? UZIP_FLAG_CAPACITY : 0u);
 }
 
 template <bool kE5>
@@ -1237,31 +1322,20 @@ __global__ void __launch_bounds__(kSmallThreads, 1) encode_small_kernel(const Pa
     __shared__ uint16_t s_pair[kE5 ? kPairEntries : 2];
     uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_tab_words);
     const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (kE5) {
-        build_pair_table<false>(p, s_tab, s_pair);
-    } else if (tid < 256) {
-        s_tab[tid] = p.cb[UZIP_CB_ENC + tid] | (p.cb[UZIP_CB_ESC + tid] ? 0x80 : 0);
-    }
-    __syncthreads();
+    build_small_tables<kE5>(p, s_tab, s_pair);
     const uint32_t units = (uint32_t)p.units, nc = (uint32_t)p.L.nc;
 
     // 1. the dense pass, a warp per unit
     if (warp < units) {
-        uint8_t* masks = reinterpret_cast<uint8_t*>(&s_masks[0][0]);
-        const uint32_t cnt = kE5 ? dense_unit_e5m2<true>(p, warp, s_pair, &s_list[0][0], masks, 0)
-                                 : dense_unit_bf16_shared(p, warp, s_tab, &s_list[0][0], masks);
+        uint8_t* masks = reinterpret_cast<uint8_t*>(s_masks[warp]);
+        const uint32_t cnt = kE5 ? dense_unit_e5m2<true>(p, warp, 0, s_pair, s_list[warp], masks, 0)
+                                 : dense_unit_bf16_shared(p, warp, s_tab, s_list[warp], masks);
         if (lane == 0) s_pre[warp + 1] = cnt;
     }
     __syncthreads();
     // 2. the unit prefix
     if (warp == 0) {
-        const uint32_t c = lane < units ? s_pre[lane + 1] : 0u;
-        uint32_t incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= (uint32_t)o) incl += t;
-        }
+        const uint32_t incl = warp_incl_scan(lane < units ? s_pre[lane + 1] : 0u, lane);
         if (lane < units) s_pre[lane + 1] = incl;
         if (lane == 0) s_pre[0] = 0;
     }
@@ -1270,29 +1344,13 @@ __global__ void __launch_bounds__(kSmallThreads, 1) encode_small_kernel(const Pa
     // 3. each chunk's first escape: chunk q starts at position x of unit u
     for (uint32_t q = tid; q < nc; q += blockDim.x) {
         const uint32_t st = q * p.chunk, u = st / kUnit, x = st % kUnit;
-        const uint32_t cu = s_pre[u + 1] - s_pre[u];
-        uint32_t below = 0;  // escapes of unit u before x
-        if (cu <= kListCap) {
-            uint32_t hi = cu;
-            while (below < hi) {
-                const uint32_t mid = (below + hi) >> 1;
-                if ((s_list[u][mid] & 0xFFFF) < x) below = mid + 1;
-                else hi = mid;
-            }
-        } else {
-            for (uint32_t w = 0; w < x / 32; w++) below += __popc(s_masks[u][w]);
-            if (x % 32) below += __popc(s_masks[u][x / 32] & ((1u << (x % 32)) - 1));
-        }
-        s_off[q] = s_pre[u] + below;
+        s_off[q] = s_pre[u] + escapes_before(s_list[u], s_masks[u], s_pre[u + 1] - s_pre[u], x);
     }
     if (tid == 0) s_off[nc] = m;
     __syncthreads();
     uint8_t* offs = p.out + p.L.off_c;
     for (uint32_t q = tid; q <= nc; q += blockDim.x) *reinterpret_cast<uint32_t*>(offs + 4ull * q) = s_off[q];
-    // 4. every escape: its unit, its place in the unit, its chunk; every byte
-    //    below out_capacity
-    const bool sent = p.fmt == kSentinel;
-    const uint64_t dbase = p.L.off_d;
+    // 4. every escape: its unit, its place in the unit, its chunk
     for (uint32_t gi = tid; gi < m; gi += blockDim.x) {
         uint32_t lo = 0, hi = units;  // s_pre[lo] <= gi < s_pre[hi]
         while (hi - lo > 1) {
@@ -1300,36 +1358,143 @@ __global__ void __launch_bounds__(kSmallThreads, 1) encode_small_kernel(const Pa
             if (s_pre[mid] <= gi) lo = mid;
             else hi = mid;
         }
-        const uint32_t j = gi - s_pre[lo], cu = s_pre[lo + 1] - s_pre[lo];
         uint32_t pos, expo;
-        if (cu <= kListCap) {
-            const uint32_t e = s_list[lo][j];
-            pos = e & 0xFFFF;
-            expo = e >> 16;
-        } else {
-            pos = nth_mask_bit(s_masks[lo], j);
-            const uint32_t i = lo * kUnit + pos;
-            expo = kE5 ? (p.in8[i] >> 2) & 0x1F : (p.in[i] >> 7) & 0xFF;
-        }
+        unit_escape<kE5>(p, s_list[lo], s_masks[lo], s_pre[lo + 1] - s_pre[lo], gi - s_pre[lo], lo * kUnit, pos,
+                         expo);
         const uint32_t i = lo * kUnit + pos, q = div_chunk(p, i);
-        const uint32_t o = s_off[q], r = gi - o;
-        if (sent) {
-            if (dbase + gi < p.cap) p.out[dbase + gi] = (uint8_t)expo;
-        } else {
-            const uint32_t k = s_off[q + 1] - o, pq = i - q * p.chunk;
-            const uint64_t bp = dbase + 3ull * o + 2 * r, bv = dbase + 3ull * o + 2 * k + r;
-            if (bp < p.cap) p.out[bp] = (uint8_t)(pq & 0xFF);
-            if (bp + 1 < p.cap) p.out[bp + 1] = (uint8_t)(pq >> 8);
-            if (bv < p.cap) p.out[bv] = (uint8_t)expo;
-        }
+        put_escape(p, gi, i, q, s_off[q], s_off[q + 1], expo);
     }
     // 5. padding and header
-    if (tid == 0) {
-        zero_words(p.out, p.L.off_c + 4 * (p.L.nc + 1), p.L.off_d);
-        zero_bytes(p.out, p.L.off_a + p.a_bytes, p.L.off_b);
-        zero_words(p.out, p.L.off_b + 4 * ((p.n + 7) / 8), p.L.off_c);
-        write_header(p, m, stream_total(p, m) > p.cap ? UZIP_FLAG_CAPACITY : 0u);
+    if (tid == 0) finish_stream(p, m);
+}
+
+// ------------------------------------------------------------ mid-size inputs
+//
+// Inputs of more than kSmallUnits and at most kClusterUnits units (and at
+// most kSmallChunks chunks) in one launch of one thread-block cluster: C <=
+// kMaxCluster CTAs of kSmallThreads threads on C SMs, CTA b taking U units
+// (b U .., a warp per unit; the grid is the cluster, C = ceil(units / U)).
+// Each CTA runs the one-CTA encoder's dense pass and unit scan in its shared
+// memory and counts, for every chunk that starts in its values, the escapes
+// between its first value and that start. After a cluster barrier each CTA
+// reads the others' escape totals from their shared memory (distributed
+// shared memory, no global memory and no atomics), writes the offsets of the
+// chunks that start in its values and places its own escapes; the offsets of
+// the at most two chunks it shares with other CTAs (the one its first value
+// lies in, the first one after its values) come from their owners' shared
+// memory. A second cluster barrier, after the last of those reads, keeps every
+// CTA's shared memory in place while others read it. Clusters of up to 16
+// CTAs (above the portable 8, allowed per kernel; the host checks that such
+// a cluster fits before taking this path): against the two-kernel path,
+// 96-256 units encode 0.8-1.9 us sooner; from 256 units on, 16 SMs' share of
+// the bandwidth is the limit and the two-kernel path is as fast.
+#ifndef UZIP_MAX_CLUSTER
+#define UZIP_MAX_CLUSTER 16
+#endif
+constexpr uint32_t kMaxCluster = UZIP_MAX_CLUSTER;
+constexpr uint32_t kClusterUnits = 256;  // 524,288 values
+static_assert(kMaxCluster <= 32, "the CTA totals are scanned by one warp");
+
+__device__ __forceinline__ uint32_t shared_addr(const void* q) { return (uint32_t)__cvta_generic_to_shared(q); }
+
+// The word at shared address a (this CTA's layout) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t a, uint32_t rank) {
+    uint32_t r, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(r) : "memory");
+    return v;
+}
+
+// Every thread of every CTA of the cluster; orders shared-memory writes
+// before the barrier with reads after it, across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <bool kE5>
+__global__ void __launch_bounds__(kSmallThreads, 1) encode_cluster_kernel(const Params p, uint32_t U) {
+    __shared__ uint32_t s_list[kSmallUnits][kListCap];
+    __shared__ __align__(16) uint32_t s_masks[kSmallUnits][kUnitGroups / 4];
+    __shared__ uint32_t s_pre[kSmallUnits + 1];    // escapes before this CTA's unit i, from its first value
+    __shared__ uint32_t s_below[kSmallChunks];     // chunk qa + k: escapes from this CTA's first value to its start
+    __shared__ uint32_t s_total;                   // this CTA's escapes (read by the others)
+    __shared__ uint32_t s_cpre[kMaxCluster + 1];   // escapes before CTA c
+    __shared__ uint32_t s_edge[2];                 // offsets of the chunks shared with other CTAs
+    __shared__ uint32_t s_tab_words[64];
+    __shared__ uint16_t s_pair[kE5 ? kPairEntries : 2];
+    uint8_t* s_tab = reinterpret_cast<uint8_t*>(s_tab_words);
+    const uint32_t tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t b = blockIdx.x, C = gridDim.x;
+    build_small_tables<kE5>(p, s_tab, s_pair);
+    const uint32_t units = (uint32_t)p.units, nc = (uint32_t)p.L.nc, chunk = p.chunk, n32 = (uint32_t)p.n;
+    const uint32_t span = U * kUnit;                        // values per CTA (< 2^20)
+    const uint32_t u0 = b * U, nu = min(U, units - u0);     // C = ceil(units / U): nu >= 1
+    const uint32_t v0 = u0 * kUnit, v1 = min(n32, v0 + nu * kUnit);
+
+    // 1. the dense pass, a warp per unit
+    if (warp < nu) {
+        uint8_t* masks = reinterpret_cast<uint8_t*>(s_masks[warp]);
+        const uint32_t cnt = kE5 ? dense_unit_e5m2<true>(p, u0 + warp, 0, s_pair, s_list[warp], masks, 0)
+                                 : dense_unit_bf16_shared(p, u0 + warp, s_tab, s_list[warp], masks);
+        if (lane == 0) s_pre[warp + 1] = cnt;
     }
+    __syncthreads();
+    // 2. this CTA's unit prefix
+    if (warp == 0) {
+        const uint32_t incl = warp_incl_scan(lane < nu ? s_pre[lane + 1] : 0u, lane);
+        if (lane < nu) s_pre[lane + 1] = incl;
+        if (lane == 0) s_pre[0] = 0;
+    }
+    __syncthreads();
+    const uint32_t total = s_pre[nu];
+    // 3. escapes from this CTA's first value to each chunk start in its values
+    const uint32_t qa = (v0 + chunk - 1) / chunk, qb = (v1 + chunk - 1) / chunk;  // chunk starts in [v0, v1)
+    for (uint32_t q = qa + tid; q < qb; q += blockDim.x) {
+        const uint32_t st = q * chunk, i = st / kUnit - u0, x = st % kUnit;
+        s_below[q - qa] = s_pre[i] + escapes_before(s_list[i], s_masks[i], s_pre[i + 1] - s_pre[i], x);
+    }
+    if (tid == 0) s_total = total;
+    cluster_sync();
+    // 4. escapes before each CTA; the shared chunks' offsets from their owners
+    if (warp == 0) {
+        const uint32_t incl = warp_incl_scan(lane < C ? ld_cluster_u32(shared_addr(&s_total), lane) : 0u, lane);
+        if (lane < C) s_cpre[lane + 1] = incl;
+        if (lane == 0) s_cpre[0] = 0;
+        __syncwarp();
+        if (lane < 2) {
+            const uint32_t q = lane == 0 ? v0 / chunk : qb;  // the chunk holding v0; the first one after v1
+            uint32_t o = s_cpre[C];                          // past the last chunk: M
+            if (q < nc) {
+                const uint32_t ob = q * chunk / span, oqa = (ob * span + chunk - 1) / chunk;
+                o = s_cpre[ob] + (ob == b ? s_below[q - qa] : ld_cluster_u32(shared_addr(&s_below[q - oqa]), ob));
+            }
+            s_edge[lane] = o;
+        }
+    }
+    cluster_sync();  // the last reads of other CTAs' shared memory are done
+    const uint32_t cpre = s_cpre[b], m = s_cpre[C];
+    uint8_t* offs = p.out + p.L.off_c;
+    for (uint32_t q = qa + tid; q < qb; q += blockDim.x)
+        *reinterpret_cast<uint32_t*>(offs + 4ull * q) = cpre + s_below[q - qa];
+    if (b == C - 1 && tid == 0) *reinterpret_cast<uint32_t*>(offs + 4ull * nc) = m;
+    // 5. this CTA's escapes: unit, place in the unit, chunk
+    for (uint32_t r = tid; r < total; r += blockDim.x) {
+        uint32_t lo = 0, hi = nu;  // s_pre[lo] <= r < s_pre[hi]
+        while (hi - lo > 1) {
+            const uint32_t mid = (lo + hi) >> 1;
+            if (s_pre[mid] <= r) lo = mid;
+            else hi = mid;
+        }
+        uint32_t pos, expo;
+        unit_escape<kE5>(p, s_list[lo], s_masks[lo], s_pre[lo + 1] - s_pre[lo], r - s_pre[lo], (u0 + lo) * kUnit, pos,
+                         expo);
+        const uint32_t i = (u0 + lo) * kUnit + pos, q = div_chunk(p, i);
+        const uint32_t o = q >= qa ? cpre + s_below[q - qa] : s_edge[0];
+        const uint32_t o1 = q + 1 < qb ? cpre + s_below[q + 1 - qa] : s_edge[1];
+        put_escape(p, cpre + r, i, q, o, o1, expo);
+    }
+    // 6. padding and header
+    if (b == 0 && tid == 0) finish_stream(p, m);
 }
 
 // n == 0: header, offsets[0] = 0 and padding only.
@@ -1352,10 +1517,17 @@ extern "C" UZIP_API size_t uzip_encode_workspace_bytes(size_t n, uint32_t chunk)
 namespace uzip {
 namespace {
 
+#define CUDA_RET(x)                            \
+    do {                                       \
+        const cudaError_t e_ = (x);            \
+        if (e_ != cudaSuccess) return e_;      \
+    } while (0)
+
 // Per-device launch facts, looked up on the first call on each device (the
 // results are the same whichever thread gets there first).
 struct DeviceFacts {
     int dev, sms, per_sm1, per_sm1e;
+    bool cluster;  // a cluster of kMaxCluster CTAs of encode_cluster_kernel can run (both formats)
 };
 constexpr int kMaxFactDevices = 64;
 std::atomic<int> g_facts_ready[kMaxFactDevices];
@@ -1398,11 +1570,125 @@ int device_facts(DeviceFacts& f) {
     UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f.per_sm1e, encode_dense_e5m2_kernel, kThreads, 0));
     UZIP_CUDA_TRY(allow_escape_smem());
     if (f.sms < 1 || f.per_sm1 < 1 || f.per_sm1e < 1) return UZIP_ERR_CUDA;
+    // Whether a cluster of kMaxCluster CTAs of the cluster encoder can run
+    // here; if not, mid-size inputs take the two-kernel path.
+    f.cluster = true;
+    void (*ck[2])(Params, uint32_t) = {encode_cluster_kernel<false>, encode_cluster_kernel<true>};
+    for (int k = 0; k < 2; k++) {
+        if (kMaxCluster > 8 &&
+            cudaFuncSetAttribute(ck[k], cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+            (void)cudaGetLastError();  // not this call's error
+            f.cluster = false;
+            continue;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kMaxCluster);
+        cfg.blockDim = dim3(kSmallThreads);
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = kMaxCluster;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, ck[k], &cfg) != cudaSuccess || clusters < 1) {
+            (void)cudaGetLastError();  // not this call's error
+            f.cluster = false;
+        }
+    }
     if (dev < kMaxFactDevices) {
         g_facts[dev] = f;
         g_facts_ready[dev].store(1, std::memory_order_release);
     }
     return UZIP_OK;
+}
+
+// Inputs of more than kSmallUnits and at most kClusterUnits units: one
+// cluster of C CTAs of encode_cluster_kernel, U units each.
+cudaError_t launch_cluster(const Params& p, const Geometry& g, uint32_t fmt, cudaStream_t s) {
+    if (kMaxCluster > 8) {  // a cluster above the portable size: allowed per function and context
+        cudaError_t e = cudaFuncSetAttribute(encode_cluster_kernel<false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(encode_cluster_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    const uint32_t U = (uint32_t)((g.units + kMaxCluster - 1) / kMaxCluster);
+    const uint32_t C = (uint32_t)((g.units + U - 1) / U);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(kSmallThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = C;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return fmt == kE5M2 ? cudaLaunchKernelEx(&cfg, encode_cluster_kernel<true>, p, U)
+                        : cudaLaunchKernelEx(&cfg, encode_cluster_kernel<false>, p, U);
+}
+
+// Longer inputs: the segment-total clear (when there are several segments),
+// the dense kernel and the escape kernel, each a programmatic dependent of
+// the one before.
+cudaError_t launch_two_kernels(Params p, const Geometry& g, const Layout& L, const DeviceFacts& f, uint32_t fmt,
+                               cudaStream_t s) {
+    const uint32_t chunk = p.chunk;
+    // Dense kernel: one resident wave.
+    const uint64_t grid1 = std::min<uint64_t>((g.units + kWarps - 1) / kWarps,
+                                              (uint64_t)f.sms * (fmt == kE5M2 ? f.per_sm1e : f.per_sm1));
+    // Escape kernel: ranges of whole chunks, sized so every resident warp
+    // gets at most one (the per-range cost is mostly load latency).
+    const int two_rounds = chunk > 32 * kUnit - 2040 && chunk % kUnit != 0;
+    const uint32_t rc_max =
+        std::max<uint32_t>(1, std::min<uint32_t>(kMaxRangeChunks, kMaxRangeUnits * kUnit / chunk));
+    // Residency at the largest chunk table this chunk size can need.
+    int per_sm2 = f.dev < kMaxFactDevices ? g_escape_per_sm[f.dev][two_rounds][rc_max].load() : 0;
+    if (per_sm2 < 1) {
+        CUDA_RET(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &per_sm2, two_rounds ? encode_escape_kernel<2> : encode_escape_kernel<1>, kThreads,
+            escape_smem(rc_max, two_rounds + 1)));
+        if (per_sm2 > 0 && f.dev < kMaxFactDevices) g_escape_per_sm[f.dev][two_rounds][rc_max].store(per_sm2);
+    }
+    if (per_sm2 < 1) return cudaErrorInvalidConfiguration;
+    const uint64_t warps2 = (uint64_t)f.sms * per_sm2 * kWarps;
+    p.range_chunks = (uint32_t)std::min<uint64_t>(rc_max, std::max<uint64_t>(1, (L.nc + warps2 - 1) / warps2));
+    p.ranges = (L.nc + p.range_chunks - 1) / p.range_chunks;
+    const uint64_t grid2 = std::min<uint64_t>((p.ranges + kWarps - 1) / kWarps, (uint64_t)f.sms * per_sm2);
+
+    // Segment totals start at zero; the last segment's is never read (no
+    // escape lies after it), so a single-segment input (up to 64 units)
+    // needs no clearing. The clearing kernel lets the dense kernel
+    // launch behind it at once (programmatic dependent launch).
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg1 = {};
+    cfg1.gridDim = dim3((unsigned)grid1);
+    cfg1.blockDim = dim3(kThreads);
+    cfg1.stream = s;
+    if (g.nseg > 1) {
+        clear_segments_kernel<<<1, 256, 0, s>>>(p.segs, g.nseg - 1);
+        CUDA_RET(cudaGetLastError());
+        cfg1.attrs = pdl;
+        cfg1.numAttrs = 1;
+    }
+    CUDA_RET(cudaLaunchKernelEx(&cfg1, fmt == kE5M2 ? encode_dense_e5m2_kernel : encode_dense_kernel, p));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid2);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = escape_smem(p.range_chunks, two_rounds + 1);
+    if (cfg.dynamicSmemBytes > 48 * 1024) CUDA_RET(allow_escape_smem());
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return two_rounds ? cudaLaunchKernelEx(&cfg, encode_escape_kernel<2>, p)
+                      : cudaLaunchKernelEx(&cfg, encode_escape_kernel<1>, p);
 }
 
 }  // namespace
@@ -1454,59 +1740,9 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         DeviceFacts f;
         const int rc = device_facts(f);
         if (rc != UZIP_OK) return rc;
-        // Dense kernel: one resident wave.
-        const uint64_t grid1 = std::min<uint64_t>((g.units + kWarps - 1) / kWarps,
-                                                  (uint64_t)f.sms * (fmt == kE5M2 ? f.per_sm1e : f.per_sm1));
-        // Escape kernel: ranges of whole chunks, sized so every resident warp
-        // gets at most one (the per-range cost is mostly load latency).
-        const int two_rounds = chunk > 32 * kUnit - 2040 && chunk % kUnit != 0;
-        const uint32_t rc_max =
-            std::max<uint32_t>(1, std::min<uint32_t>(kMaxRangeChunks, kMaxRangeUnits * kUnit / chunk));
-        // Residency at the largest chunk table this chunk size can need.
-        int per_sm2 = f.dev < kMaxFactDevices ? g_escape_per_sm[f.dev][two_rounds][rc_max].load() : 0;
-        if (per_sm2 < 1) {
-            UZIP_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &per_sm2, two_rounds ? encode_escape_kernel<2> : encode_escape_kernel<1>, kThreads,
-                escape_smem(rc_max, two_rounds + 1)));
-            if (per_sm2 > 0 && f.dev < kMaxFactDevices) g_escape_per_sm[f.dev][two_rounds][rc_max].store(per_sm2);
-        }
-        if (per_sm2 < 1) return UZIP_ERR_CUDA;
-        const uint64_t warps2 = (uint64_t)f.sms * per_sm2 * kWarps;
-        p.range_chunks = (uint32_t)std::min<uint64_t>(rc_max, std::max<uint64_t>(1, (L.nc + warps2 - 1) / warps2));
-        p.ranges = (L.nc + p.range_chunks - 1) / p.range_chunks;
-        const uint64_t grid2 = std::min<uint64_t>((p.ranges + kWarps - 1) / kWarps, (uint64_t)f.sms * per_sm2);
-
-        // Segment totals start at zero; the last segment's is never read (no
-        // escape lies after it), so a single-segment input (up to 64 units)
-        // needs no clearing. The clearing kernel lets the dense kernel
-        // launch behind it at once (programmatic dependent launch).
-        cudaLaunchAttribute pdl[1];
-        pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        pdl[0].val.programmaticStreamSerializationAllowed = 1;
-        cudaLaunchConfig_t cfg1 = {};
-        cfg1.gridDim = dim3((unsigned)grid1);
-        cfg1.blockDim = dim3(kThreads);
-        cfg1.stream = s;
-        if (g.nseg > 1) {
-            clear_segments_kernel<<<1, 256, 0, s>>>(p.segs, g.nseg - 1);
-            UZIP_CUDA_TRY(cudaGetLastError());
-            cfg1.attrs = pdl;
-            cfg1.numAttrs = 1;
-        }
-        UZIP_CUDA_TRY(cudaLaunchKernelEx(&cfg1, fmt == kE5M2 ? encode_dense_e5m2_kernel : encode_dense_kernel, p));
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)grid2);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = escape_smem(p.range_chunks, two_rounds + 1);
-        if (cfg.dynamicSmemBytes > 48 * 1024) UZIP_CUDA_TRY(allow_escape_smem());
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        UZIP_CUDA_TRY(two_rounds ? cudaLaunchKernelEx(&cfg, encode_escape_kernel<2>, p)
-                                 : cudaLaunchKernelEx(&cfg, encode_escape_kernel<1>, p));
+        UZIP_CUDA_TRY(f.cluster && g.units <= kClusterUnits && L.nc <= kSmallChunks
+                          ? launch_cluster(p, g, fmt, s)                // one cluster, one launch
+                          : launch_two_kernels(p, g, L, f, fmt, s));  // dense + escape kernels
     }
     if (h_out_bytes) {
         uint32_t hdr[16];

@@ -1,9 +1,13 @@
 """Short inputs (at most 32 units of 2048 values and 4096 chunks) are encoded
-by one CTA in one launch, with the escape lists in shared memory; longer ones
-by the dense and escape kernels. Both must give the oracle's stream byte for
-byte (SplitZip review page, §3.2), in all three formats, on both sides of the
-boundary, with units whose escapes overflow their list, and with an output
-buffer too small for the escapes. Integer work: the tolerance is zero."""
+by one CTA in one launch, with the escape lists in shared memory; mid-size
+ones (at most 256 units and 4096 chunks) by one thread-block cluster of up to
+16 CTAs, which exchange their escape counts through distributed shared
+memory; longer ones by the dense and escape kernels. All must give the
+oracle's stream byte for byte (SplitZip review page, §3.2), in all three
+formats, on both sides of every limit, with chunks that span several of a
+cluster's CTAs, with units whose escapes overflow their list, and with an
+output buffer too small for the escapes. Integer work: the tolerance is
+zero."""
 import numpy as np
 import pytest
 import torch
@@ -74,12 +78,41 @@ def test_both_sides_of_the_boundary(uz, orc, fmt, chunk, sizes):
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "e5m2", "sentinel"])
+@pytest.mark.parametrize("chunk,sizes", [
+    (1024, [33 * 2048 - 5, 48 * 2048, 96 * 2048 + 7, 256 * 2048, 256 * 2048 + 1]),  # 256 units: the last cluster input
+    (104, [409600]),                 # 3939 chunks: a cluster
+    (96, [409600]),                  # 4267 chunks: the two kernels
+    (128, [4096 * 128, 4096 * 128 + 8]),
+    (65536, [40 * 2048, 100 * 2048 + 3]),  # one chunk over many CTAs of the cluster
+    (8200, [77 * 2048 + 11]),        # chunks crossing the CTAs' boundaries
+])
+def test_both_sides_of_the_cluster_limits(uz, orc, fmt, chunk, sizes):
+    rng = np.random.default_rng(chunk + 5)
+    for n in sizes:
+        if fmt == "e5m2":
+            xh = rng.integers(0, 256, n).astype(np.uint8)
+            xh[rng.random(n) < 0.7] = 0x3C
+            exps = orc.e5m2_calibrate(xh[: max(1, n // 2)])
+        else:
+            xh = _gauss(rng, n)
+            xh[rng.integers(0, n, max(1, n // 40))] = 0x7F80
+            exps = orc.calibrate(_gauss(rng, 1 << 14))
+        _check(uz, orc, xh, exps, chunk, fmt)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "e5m2", "sentinel"])
 @pytest.mark.parametrize("chunk", [8, 1000, 2048])
 def test_units_whose_escapes_overflow_their_list(uz, orc, fmt, chunk):
     """Every unit, or every other one, holds more escapes than its list (64):
-    the one-CTA encoder places them from its mask bits and the input."""
+    the one-CTA and cluster encoders place them from their mask bits and the
+    input (chunk 8 on the longer input: more than 4096 chunks, the two
+    kernels)."""
     rng = np.random.default_rng(chunk + 3)
-    n = 20 * 2048 + 333
+    for n in (20 * 2048 + 333, 100 * 2048 + 333):  # one CTA; a cluster of 15
+        _overflowing(uz, orc, fmt, chunk, rng, n)
+
+
+def _overflowing(uz, orc, fmt, chunk, rng, n):
     if fmt == "e5m2":
         xh = rng.integers(0, 256, n).astype(np.uint8)
         exps = np.arange(16, dtype=np.uint8)
@@ -91,8 +124,9 @@ def test_units_whose_escapes_overflow_their_list(uz, orc, fmt, chunk):
     _check(uz, orc, xh, exps, chunk, fmt)
 
 
-def test_capacity_overflow_of_a_short_input(uz):
-    x = W.heavy_tailed(40_000, seed=8, device="cuda")
+@pytest.mark.parametrize("n", [40_000, 300_000])  # one CTA; a cluster
+def test_capacity_overflow_of_a_short_input(uz, n):
+    x = W.heavy_tailed(n, seed=8, device="cuda")
     cb = uz.calibrate(W.gaussian(1 << 16, seed=9, device="cuda"))
     n = x.numel()
     cap = uz.compressed_size(n, 0, 1024) + 30  # room for 10 escapes only
