@@ -1372,8 +1372,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1) encode_small_kernel(const Pa
 //
 // Inputs of more than kSmallUnits and at most kClusterUnits units (and at
 // most kSmallChunks chunks) in one launch of one thread-block cluster: C <=
-// kMaxCluster CTAs of kSmallThreads threads on C SMs, CTA b taking U units
-// (b U .., a warp per unit; the grid is the cluster, C = ceil(units / U)).
+// kMaxCluster CTAs on C SMs, CTA b taking U units (b U .., a warp per unit,
+// at least 256 threads; the grid is the cluster, C = ceil(units / U)).
 // Each CTA runs the one-CTA encoder's dense pass and unit scan in its shared
 // memory and counts, for every chunk that starts in its values, the escapes
 // between its first value and that start. After a cluster barrier each CTA
@@ -1617,7 +1617,7 @@ cudaError_t launch_cluster(const Params& p, const Geometry& g, uint32_t fmt, cud
     const uint32_t C = (uint32_t)((g.units + U - 1) / U);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(C);
-    cfg.blockDim = dim3(kSmallThreads);
+    cfg.blockDim = dim3(std::max<uint32_t>(256, 32 * U));  // a warp per unit, at least the table's 256 threads
     cfg.stream = s;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
@@ -1733,8 +1733,10 @@ int encode_impl(const void* d_in_bf16, size_t n, uint32_t chunk, const void* d_c
         encode_empty_kernel<<<1, 1, 0, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
     } else if (g.units <= kSmallUnits && L.nc <= kSmallChunks) {  // one CTA, one launch
-        if (fmt == kE5M2) encode_small_kernel<true><<<1, kSmallThreads, 0, s>>>(p);
-        else encode_small_kernel<false><<<1, kSmallThreads, 0, s>>>(p);
+        // a warp per unit, and at least the 256 threads that build the code table
+        const uint32_t threads = std::max<uint32_t>(256, 32 * (uint32_t)g.units);
+        if (fmt == kE5M2) encode_small_kernel<true><<<1, threads, 0, s>>>(p);
+        else encode_small_kernel<false><<<1, threads, 0, s>>>(p);
         UZIP_CUDA_TRY(cudaGetLastError());
     } else {
         DeviceFacts f;
