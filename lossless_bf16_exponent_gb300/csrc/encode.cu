@@ -1,5 +1,6 @@
 // encode.cu -- SplitZip encoder for sm_103a: one pass over the input (a one-block
-// clear of the segment totals, a dense kernel, an escape kernel).
+// clear of the segment totals, a dense kernel, an escape kernel; short inputs
+// in one launch).
 //
 // SplitZip review page, §3.2: encoding is (1) a dense transform -- split each
 // BF16 value into its exponent and sign-mantissa byte, store the latter
@@ -40,7 +41,11 @@
 // The input is read from HBM once; the escape lists cost about 4 bytes per
 // escape written and read. FP8 E5M2 input (page §4.2) has its own dense
 // kernel (one lookup per exponent pair, 32 values per lane and step) and
-// shares the escape kernel.
+// shares the escape kernel. Short inputs take one launch instead: up to 32
+// units one CTA (encode_small_kernel), up to 256 units one thread-block
+// cluster of up to 16 CTAs that meet through distributed shared memory
+// (encode_cluster_kernel); both keep the escape lists in shared memory and
+// use no workspace.
 #include <algorithm>
 #include <atomic>
 
