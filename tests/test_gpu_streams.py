@@ -14,10 +14,14 @@ import lossless_bf16_exponent_gb300.workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def test_two_streams_at_once_match_sequential_calls(uz):
+# 4 Mi values each: the two-kernel path, enough blocks for the two to overlap;
+# 150,000 each: one thread-block cluster each, side by side
+@pytest.mark.parametrize("values", [1 << 22, 150_000])
+def test_two_streams_at_once_match_sequential_calls(uz, values):
     dev = torch.device("cuda")
-    shape = (8, 2, 8, 256, 128)  # 4 Mi values each: enough blocks for the two to overlap
-    xs = [W.kv_cache(shape, seed=21, device=dev).reshape(-1), W.heavy_tailed(1 << 22, seed=22, device=dev)]
+    shape = (values // (2 * 8 * 256 * 128) or 1, 2, 8, 256, 128)
+    kv = W.kv_cache(shape, seed=21, device=dev).reshape(-1)[:values]
+    xs = [kv.contiguous(), W.heavy_tailed(values, seed=22, device=dev)]
     samples = [W.kv_cache_sample(device=dev), W.gaussian(1 << 16, seed=23, device=dev)]
     chunks = [1024, 256]
     cbs = [uz.calibrate(s) for s in samples]
