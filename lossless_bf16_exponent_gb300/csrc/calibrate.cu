@@ -139,7 +139,10 @@ __global__ void __launch_bounds__(kHistThreads) calibrate_kernel(const void* __r
 // memory's latency. Every 65,408 values per thread (before a half can carry
 // into the other) the block folds the counters into per-bin totals and
 // clears them. The next round's 16 loads per thread are issued before the
-// current round is counted. The last block ranks, as above.
+// current round is counted; whole rounds load without bounds tests, and every
+// loaded vector is counted: the last round's out-of-range vectors are loaded
+// as zeros, counted into bin 0 like any zero, and their number is taken off
+// bin 0's total once (no test per vector). The last block ranks, as above.
 constexpr int kPrivThreads = 384;
 constexpr int kPrivLoads = 16;
 constexpr uint32_t kEpochValues = 65408;  // per thread between folds, + one tail value < 65536
@@ -167,9 +170,10 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
     constexpr uint32_t kPerVec = kFmt == kE5M2 ? 16 : 8;
 #ifdef UZIP_HIST_EPOCH_ROUNDS
     constexpr uint32_t kRoundsPerEpoch = UZIP_HIST_EPOCH_ROUNDS;  // shorter epochs (tests of the fold)
-    static_assert(kRoundsPerEpoch * kPrivLoads * kPerVec <= kEpochValues, "16-bit counters");
+    static_assert((kRoundsPerEpoch + 1) * kPrivLoads * kPerVec <= kEpochValues, "16-bit counters");
 #else
-    constexpr uint32_t kRoundsPerEpoch = kEpochValues / (kPrivLoads * kPerVec);
+    // one round short of the counters' limit: the last round's padding is counted too
+    constexpr uint32_t kRoundsPerEpoch = kEpochValues / (kPrivLoads * kPerVec) - 1;
 #endif
     extern __shared__ uint4 s_dyn[];
     const uint32_t* cnt = reinterpret_cast<const uint32_t*>(s_dyn);  // [bin pair][thread]
@@ -211,7 +215,9 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
         __syncthreads();
     };
 
+    __shared__ uint32_t s_pad;  // zero values counted for the padding of partial rounds
     clear();
+    if (tid == 0) s_pad = 0;
     __syncthreads();
     const uint64_t groups = n / kPerVec;
     if (blockIdx.x == 0 && (uint64_t)tid < n - groups * kPerVec) {  // ragged tail: one value per thread
@@ -221,24 +227,33 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
     }
     const uint64_t per_round = (uint64_t)gridDim.x * kPrivThreads * kPrivLoads;
     const uint64_t rounds = (groups + per_round - 1) / per_round;
+    uint32_t pad = 0;
     auto load_round = [&](uint64_t r, uint4* v) {
         const uint64_t base = (r * gridDim.x + blockIdx.x) * (uint64_t)kPrivThreads * kPrivLoads + tid;
+        const uint4* src = reinterpret_cast<const uint4*>(x8) + base;
+        if (base + (uint64_t)(kPrivLoads - 1) * kPrivThreads < groups) {  // a whole round
 #pragma unroll
-        for (int j = 0; j < kPrivLoads; j++) {
-            const uint64_t g = base + (uint64_t)j * kPrivThreads;
-            v[j] = g < groups ? ld_stream_v4(x8 + 16 * g) : make_uint4(0, 0, 0, 0);
+            for (int j = 0; j < kPrivLoads; j++) v[j] = ld_stream_v4(src + j * kPrivThreads);
+        } else {
+#pragma unroll
+            for (int j = 0; j < kPrivLoads; j++) {
+                const bool in = base + (uint64_t)j * kPrivThreads < groups;
+                v[j] = in ? ld_stream_v4(src + j * kPrivThreads) : make_uint4(0, 0, 0, 0);
+                pad += in ? 0u : kPerVec;  // counted as zeros below (bin 0), taken off at the end
+            }
         }
+    };
+    auto count_round = [&](const uint4* v) {
+#pragma unroll
+        for (int j = 0; j < kPrivLoads; j++) count_vec(v[j]);
     };
     uint4 v[kPrivLoads], nv[kPrivLoads];
     if (rounds) load_round(0, v);
     for (uint64_t r0 = 0; r0 < rounds; r0 += kRoundsPerEpoch) {
         const uint64_t r1 = min(rounds, r0 + kRoundsPerEpoch);
-        for (uint64_t r = r0; r < r1; r++) {
+        for (uint64_t r = r0; r < r1; r++) {  // the next round's loads in flight while one is counted
             if (r + 1 < rounds) load_round(r + 1, nv);
-            const uint64_t base = (r * gridDim.x + blockIdx.x) * (uint64_t)kPrivThreads * kPrivLoads + tid;
-#pragma unroll
-            for (int j = 0; j < kPrivLoads; j++)
-                if (base + (uint64_t)j * kPrivThreads < groups) count_vec(v[j]);
+            count_round(v);
 #pragma unroll
             for (int j = 0; j < kPrivLoads; j++) v[j] = nv[j];
         }
@@ -248,7 +263,9 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
             __syncthreads();
         }
     }
+    if (pad) atomicAdd(&s_pad, pad);
     fold();
+    if (tid == 0) total -= s_pad;  // bin 0: the padding's zeros (fold ends with a barrier)
     pdl_wait();  // the blob's totals and counter are zeroed by the launch before this one
     if (tid < 256 && total) atomicAdd(&hist[tid], (unsigned long long)total);
     // The last block ranks the totals.
