@@ -156,12 +156,16 @@ __device__ __forceinline__ void count_one(uint32_t* col, uint32_t e) {
     atomicAdd(col + (e >> 1) * kPrivThreads, 1u << (16 * (e & 1)));
 }
 
-// The same from the bin pair (row) and the bin's low bit (half) directly: the
-// half's increment 1 or 2^16 is 1 + half * 0xFFFF, a multiply-add beside the
-// saturated ALU pipe. For BF16 the row is the value's high byte without the
-// sign, the half its bit 7.
-__device__ __forceinline__ void count_row(uint32_t* col, uint32_t row, uint32_t half) {
-    atomicAdd(col + row * kPrivThreads, half * 0xFFFFu + 1u);
+// A BF16 value's row (bin pair) is its high byte without the sign, its half
+// (the bin's low bit) its bit 7. The row's byte offset, row * 4 kPrivThreads =
+// row * 256 * 6, is the value's masked high byte times 6, and the half's
+// increment, 1 or 2^16, is 1 + half * 0xFFFF: both multiply-adds, beside the
+// saturated ALU pipe.
+static_assert(4 * kPrivThreads == 6 * 256, "the row stride is 6 times 256 bytes");
+__device__ __forceinline__ void count_bf16_pair(uint32_t* col, uint32_t x) {  // the two values of word x
+    char* c = reinterpret_cast<char*>(col);
+    atomicAdd(reinterpret_cast<uint32_t*>(c + (x & 0x7F00u) * 6u), ((x >> 7) & 1u) * 0xFFFFu + 1u);
+    atomicAdd(reinterpret_cast<uint32_t*>(c + ((x >> 16) & 0x7F00u) * 6u), ((x >> 23) & 1u) * 0xFFFFu + 1u);
 }
 
 template <int kFmt>
@@ -195,8 +199,7 @@ __global__ void __launch_bounds__(kPrivThreads, 1) histogram_private_kernel(cons
 #pragma unroll
                 for (int b = 0; b < 4; b++) count_one(col, (w[q] >> (8 * b + 2)) & 0x1F);
             } else {  // two values per word: rows from bits 8..14 and 24..30, halves bits 7 and 23
-                count_row(col, (w[q] >> 8) & 0x7F, (w[q] >> 7) & 1);
-                count_row(col, (w[q] >> 24) & 0x7F, (w[q] >> 23) & 1);
+                count_bf16_pair(col, w[q]);
             }
         }
     };
